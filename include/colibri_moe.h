@@ -1,0 +1,157 @@
+/*
+ * colibri_moe.h -- C ABI of a GB300 (sm_103a) Mixture-of-Experts layer forward.
+ *
+ * One call of colibri_moe_forward runs, on the caller's CUDA stream:
+ *   1. router: logits L = x W_r^T (+ b_r), top-2 experts per token, gates
+ *      (zskr.cn/news/2272131 "Colibri: a lightweight C MoE inference engine for
+ *      edge devices" 3.2; hnwysp.cn/news/30485 3.1);
+ *   2. dispatch: per-expert counts, offsets, tokens gathered into
+ *      expert-contiguous rows (zskr.cn 2.1 "Dispatch", 3.2 "expert_counts");
+ *   3. expert FFN as grouped GEMMs with the activation fused
+ *      (zskr.cn 2.1 "Compute: grouped GEMM"; m.nxbn.cn/news/48047 2.1, 3.1);
+ *   4. gate-weighted combine in fp32 (m.nxbn.cn 3.3 "output aggregation";
+ *      hnwysp.cn 2.2).
+ *
+ * Math of the layer (all row-major, nn.Linear [out, in] weight layout):
+ *   L[t,e]   = sum_j x[t,j] W_r[e,j] (+ b_r[e])
+ *   (a, b)   = the two experts ranked first by (L descending, expert index ascending)
+ *   g_a      = 1 / (1 + exp(L[t,b] - L[t,a])),  g_b = 1 - g_a   (softmax over the pair)
+ *   SwiGLU:  y_e(x) = W2_e (silu(W1_e x) * (W3_e x))      W1 = W_gate, W3 = W_up, W2 = W_down
+ *   ReLU:    y_e(x) = W2_e max(W1_e x + b1_e, 0) + b2_e
+ *   out[t]   = g_a y_a(x_t) + g_b y_b(x_t)                (fp32 sum; no residual add)
+ *
+ * Conventions (m.nxbn.cn 3.3 and 5.1: int status codes, 0 = success;
+ * zskr.cn 5.3: one context per thread; hnwysp.cn 2.1: no allocation on the
+ * forward path; m.nxbn.cn 3.1: maximum batch fixed at initialisation):
+ *   - Every function returns 0 or a negative COLIBRI_ERR_* code; none aborts.
+ *   - A context owns all device memory it allocates; the caller owns x, out,
+ *     the stream and any buffer it passes in.
+ *   - A context is not thread-safe: use one per host thread.
+ *   - `stream` arguments are cudaStream_t values passed as void* (NULL = the
+ *     legacy default stream).  Kernel faults are asynchronous and surface at
+ *     the caller's next synchronisation.
+ */
+#ifndef COLIBRI_MOE_H
+#define COLIBRI_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define COLIBRI_API __attribute__((visibility("default")))
+#else
+#define COLIBRI_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (m.nxbn.cn 5.1: -1 size exceeded, -2 out of memory, -3 corrupt weights) ---- */
+#define COLIBRI_OK 0
+#define COLIBRI_ERR_INVALID_ARG (-1)  /* NULL pointer, T < 0 or T > max_tokens, host pointer where a
+                                         device pointer is required, aliasing x/out, top_k != 2,
+                                         num_experts outside 2..16, bad enum value */
+#define COLIBRI_ERR_OOM (-2)          /* a device allocation failed */
+#define COLIBRI_ERR_BAD_WEIGHTS (-3)  /* a required weight or bias pointer is NULL, or one is given
+                                         that the activation does not use */
+#define COLIBRI_ERR_CUDA (-4)         /* a CUDA runtime / driver call failed (includes: no device) */
+#define COLIBRI_ERR_STATE (-5)        /* forward before load_weights, or no forward yet */
+#define COLIBRI_ERR_UNSUPPORTED (-6)  /* shape/dtype combination this build does not run */
+#define COLIBRI_ERR_DEVICE (-7)       /* a kernel reported a failure through the device status word */
+
+/* ---- enums (stored as int32_t in the structs) ---- */
+#define COLIBRI_DTYPE_F32 0   /* fp32 activations and weights: SIMT fp32 path           */
+#define COLIBRI_DTYPE_BF16 1  /* bf16 activations and weights: tcgen05 tensor-core path  */
+#define COLIBRI_ACT_RELU_BIAS 0 /* y = W2 max(W1 x + b1, 0) + b2 (b1, b2 required)       */
+#define COLIBRI_ACT_SWIGLU 1    /* y = W2 (silu(W1 x) * (W3 x)), no biases                 */
+
+#define COLIBRI_MAX_EXPERTS 16
+
+typedef struct colibri_moe colibri_moe_t; /* opaque */
+
+typedef struct {
+  int32_t d_model;         /* d: hidden size.  Multiple of 8; bf16 also needs d % 256 == 0        */
+  int32_t d_ff;            /* f: expert inner size.  bf16 SwiGLU: f % 128 == 0; bf16 ReLU: f % 256 */
+  int32_t num_experts;     /* E, 2..16                                                              */
+  int32_t top_k;           /* must be 2                                                             */
+  int32_t max_tokens;      /* largest T any forward will be given (> 0); sizes the workspace        */
+  int32_t dtype;           /* COLIBRI_DTYPE_*: dtype of x and of all weights                         */
+  int32_t act;             /* COLIBRI_ACT_*                                                          */
+  int32_t has_router_bias; /* 0/1: b_r present                                                       */
+  int32_t out_dtype;       /* COLIBRI_DTYPE_*: dtype of out (the combine itself is fp32)             */
+} colibri_moe_config_t;
+
+/* Per-tensor pointers, nn.Linear [out, in] row-major, dtype = config.dtype for weights and fp32 for
+ * biases.  Each pointer may be a host or a device pointer; load_weights copies (it never keeps
+ * them).  Arrays of E pointers are host arrays. */
+typedef struct {
+  const void* w_router;      /* [E, d]                                             */
+  const float* b_router;     /* [E] fp32, required iff has_router_bias, else NULL  */
+  const void* const* w1;     /* E x [f, d]: ReLU W1, SwiGLU W_gate                 */
+  const void* const* w3;     /* E x [f, d]: SwiGLU W_up; NULL for ReLU             */
+  const void* const* w2;     /* E x [d, f]: W2 / W_down                            */
+  const float* const* b1;    /* E x [f] fp32: ReLU only (required), else NULL      */
+  const float* const* b2;    /* E x [d] fp32: ReLU only (required), else NULL      */
+} colibri_moe_weights_t;
+
+/* Validates the config, selects `device`, and allocates the workspace for max_tokens tokens
+ * (expert-contiguous activation rows, routing arrays, per-chunk histograms, staging for
+ * forward_host).  On success *out receives the context; on failure *out is NULL. */
+COLIBRI_API int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_t** out);
+
+/* Copies all weights into one device arena (each expert's block 256-byte aligned, experts
+ * contiguous; zskr.cn 2.2) in the layout the kernels read, builds the TMA descriptors, then
+ * synchronises `stream`.  May be called again to replace the weights. */
+COLIBRI_API int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_weights_t* w, void* stream);
+
+/* out[T, d] = MoE layer applied to x[T, d].  x (config.dtype) and out (config.out_dtype) are device
+ * pointers, row-major and contiguous, and must not overlap.  Asynchronous on `stream`: no host
+ * synchronisation and no allocation.  T == 0 is a no-op.  Calls on one context must be ordered
+ * (same stream, or synchronised): the workspace is shared. */
+COLIBRI_API int colibri_moe_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t T, void* stream);
+
+/* Same as forward with HOST buffers: copies x host->device into the context's staging buffer,
+ * runs forward, copies out device->host, then synchronises `stream`.  Pinned host memory gives
+ * asynchronous copies; pageable memory works but copies synchronously. */
+COLIBRI_API int colibri_moe_forward_host(colibri_moe_t* ctx, const void* x_host, void* out_host, int32_t T, void* stream);
+
+/* Routing of the most recent forward, copied into caller DEVICE buffers on `stream` (any may be
+ * NULL): idx[T,2] int32 (slot 0 = higher logit), gate[T,2] fp32, counts[E] int32,
+ * offsets[E+1] int32 (row where each expert's segment starts; segments padded to 128 rows),
+ * row_of[T,2] int32 (row of token t's slot s; row_of - offsets[e] is t's rank among e's tokens). */
+COLIBRI_API int colibri_moe_get_routing(colibri_moe_t* ctx, int32_t* idx, float* gate, int32_t* counts, int32_t* offsets,
+                            int32_t* row_of, void* stream);
+
+/* Debug view of internal device buffers (read-only use; valid until destroy or the next forward):
+ *   which = 0: Xp, gathered token rows [rows, d] (config.dtype);
+ *           1: H, expert hidden activations [rows, f] (bf16 on the bf16 path, fp32 on the fp32 path);
+ *           2: Y, expert outputs before the combine [rows, d] (fp32);
+ *           3: token_of_row [rows] (int32).
+ * Only rows inside an expert's segment [offsets[e], offsets[e] + counts[e]) of the last forward
+ * hold defined values; padding rows hold stale data.  *ptr receives the device address and *rows
+ * the allocated row count (may be NULL). */
+COLIBRI_API int colibri_moe_debug_buffer(colibri_moe_t* ctx, int32_t which, void** ptr, int64_t* rows);
+
+/* Number of pipeline stages (kernel launches) forward enqueues, for a nonzero T. */
+COLIBRI_API int colibri_moe_num_stages(const colibri_moe_t* ctx, int32_t* n_stages);
+
+/* Stage timing: with n == num_stages + 1 cudaEvent_t values (passed as void*), every later forward
+ * records events[i] just before stage i and events[n-1] after the last stage, on its stream.
+ * events == NULL (n == 0) turns it off.  The caller owns the events. */
+COLIBRI_API int colibri_moe_set_stage_events(colibri_moe_t* ctx, void* const* events, int32_t n);
+
+/* Reads (synchronously) and clears the device status word that kernels set when a bounded wait
+ * gives up or an index check fails: *status = 0 means none did. */
+COLIBRI_API int colibri_moe_device_status(colibri_moe_t* ctx, int32_t* status);
+
+/* Frees everything the context owns.  NULL-safe. */
+COLIBRI_API void colibri_moe_destroy(colibri_moe_t* ctx);
+
+/* Static string for a status code. */
+COLIBRI_API const char* colibri_moe_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,539 @@
+// Host side of the C ABI declared in include/colibri_moe.h: context, device weight arena,
+// workspace, argument validation and the launch sequence of one forward.
+//
+// Allocation happens in create (workspace sized for max_tokens) and load_weights (weight arena);
+// forward only enqueues kernels (hnwysp.cn/news/30485 2.1: buffers allocated once, none on the
+// forward path; m.nxbn.cn/news/48047 3.1: the maximum batch is fixed at initialisation).
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "colibri_moe.h"
+#include "moe_internal.cuh"
+
+using namespace colibri;
+
+struct colibri_moe {
+  colibri_moe_config_t cfg{};
+  int device = 0;
+  int num_sms = 0;
+  int64_t rows_alloc = 0;   // rows of Xp / H / Y
+  int nchunks_max = 0;      // router chunks at max_tokens
+  int dchunk = 0;           // router: W_r columns per shared-memory pass
+  size_t esize = 0;         // bytes per element of x and weights
+  size_t out_esize = 0;
+  int n_up = 0;             // weight rows per expert of the up projection (2f SwiGLU bf16, f otherwise)
+
+  // weight arena (one allocation, every block 256-byte aligned)
+  void* warena = nullptr;
+  size_t warena_bytes = 0;
+  void* w_router = nullptr;
+  float* b_router = nullptr;
+  void* w13 = nullptr;  // bf16 SwiGLU: [E, 2f, d], gate/up interleaved in blocks of 128 rows; else W1 [E, f, d]
+  void* w3 = nullptr;   // fp32 SwiGLU: W_up [E, f, d]
+  void* w2 = nullptr;   // [E, d, f]
+  float* b1 = nullptr;  // [E, f]
+  float* b2 = nullptr;  // [E, d]
+  bool loaded = false;
+
+  // workspace (one allocation)
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  void* xp = nullptr;
+  void* h = nullptr;
+  float* y = nullptr;
+  int32_t* idx = nullptr;
+  float* gate = nullptr;
+  int32_t* row_of = nullptr;
+  int32_t* tok_of_row = nullptr;
+  int32_t* hist = nullptr;
+  Sched* sched = nullptr;
+  void* x_stage = nullptr;
+  void* out_stage = nullptr;
+
+  CUtensorMap tm_xp{}, tm_h{}, tm_w13{}, tm_w2{};
+  int32_t last_T = -1;
+  std::vector<cudaEvent_t> events;
+  uint64_t timeout_ns = 2000000000ull;
+};
+
+namespace {
+
+constexpr int kNumStages = 5;  // router, gather, up GEMM, down GEMM, combine
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2D bf16 tensor [rows, inner] row-major; box = 64 (inner) x box_rows, 128-byte swizzle.
+bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A pointer the kernels may read/write: device (or managed) memory on the context's device.
+bool is_device_ptr(const void* p, int device) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (at.type == cudaMemoryTypeManaged) return true;
+  return at.type == cudaMemoryTypeDevice && at.device == device;
+}
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const char *pa = static_cast<const char*>(a), *pb = static_cast<const char*>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+int check_config(const colibri_moe_config_t* c) {
+  if (!c) return COLIBRI_ERR_INVALID_ARG;
+  if (c->top_k != 2 || c->num_experts < 2 || c->num_experts > COLIBRI_MAX_EXPERTS) return COLIBRI_ERR_INVALID_ARG;
+  if (c->d_model <= 0 || c->d_ff <= 0 || c->max_tokens <= 0 || c->max_tokens > (1 << 24))
+    return COLIBRI_ERR_INVALID_ARG;
+  if ((c->dtype != COLIBRI_DTYPE_F32 && c->dtype != COLIBRI_DTYPE_BF16) ||
+      (c->out_dtype != COLIBRI_DTYPE_F32 && c->out_dtype != COLIBRI_DTYPE_BF16) ||
+      (c->act != COLIBRI_ACT_RELU_BIAS && c->act != COLIBRI_ACT_SWIGLU) ||
+      (c->has_router_bias != 0 && c->has_router_bias != 1))
+    return COLIBRI_ERR_INVALID_ARG;
+  if (c->d_model % 8 || c->d_ff % 8) return COLIBRI_ERR_UNSUPPORTED;
+  if (c->dtype == COLIBRI_DTYPE_BF16) {
+    const int bn = tc_gemm_block_n();
+    if (c->d_model % bn) return COLIBRI_ERR_UNSUPPORTED;
+    if (c->act == COLIBRI_ACT_SWIGLU && c->d_ff % (bn / 2)) return COLIBRI_ERR_UNSUPPORTED;
+    if (c->act == COLIBRI_ACT_RELU_BIAS && c->d_ff % bn) return COLIBRI_ERR_UNSUPPORTED;
+  }
+  return COLIBRI_OK;
+}
+
+uint64_t env_timeout_ns() {
+  const char* s = std::getenv("COLIBRI_MOE_WAIT_TIMEOUT_MS");
+  if (s) {
+    long v = std::strtol(s, nullptr, 10);
+    if (v > 0) return static_cast<uint64_t>(v) * 1000000ull;
+  }
+  return 2000000000ull;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* colibri_moe_strerror(int code) {
+  switch (code) {
+    case COLIBRI_OK: return "ok";
+    case COLIBRI_ERR_INVALID_ARG: return "invalid argument";
+    case COLIBRI_ERR_OOM: return "device allocation failed";
+    case COLIBRI_ERR_BAD_WEIGHTS: return "missing or unexpected weight tensor";
+    case COLIBRI_ERR_CUDA: return "CUDA call failed";
+    case COLIBRI_ERR_STATE: return "call out of order (weights not loaded, or no forward yet)";
+    case COLIBRI_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case COLIBRI_ERR_DEVICE: return "a kernel reported a failure in the device status word";
+    default: return "unknown status code";
+  }
+}
+
+void colibri_moe_destroy(colibri_moe_t* ctx) {
+  if (!ctx) return;
+  {
+    DeviceGuard g(ctx->device);
+    if (ctx->warena) cudaFree(ctx->warena);
+    if (ctx->ws) cudaFree(ctx->ws);
+  }
+  delete ctx;
+}
+
+int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_t** out) {
+  if (!out) return COLIBRI_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
+    cudaGetLastError();
+    return COLIBRI_ERR_CUDA;
+  }
+  if (device < 0 || device >= ndev) return COLIBRI_ERR_INVALID_ARG;
+  DeviceGuard g(device);
+  if (!g.ok) return COLIBRI_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return COLIBRI_ERR_CUDA;
+  if (major != 10 || minor != 3) return COLIBRI_ERR_UNSUPPORTED;  // built for sm_103a only
+
+  colibri_moe_t* c = new (std::nothrow) colibri_moe_t();
+  if (!c) return COLIBRI_ERR_OOM;
+  c->cfg = *cfg;
+  c->device = device;
+  c->num_sms = sms;
+  c->timeout_ns = env_timeout_ns();
+  const int64_t d = cfg->d_model, f = cfg->d_ff, E = cfg->num_experts, T = cfg->max_tokens;
+  c->esize = cfg->dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
+  c->out_esize = cfg->out_dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
+  c->n_up = (cfg->dtype == COLIBRI_DTYPE_BF16 && cfg->act == COLIBRI_ACT_SWIGLU) ? 2 * cfg->d_ff : cfg->d_ff;
+  c->rows_alloc = ((2 * T + (kRowTile - 1) * E) + kRowTile - 1) / kRowTile * kRowTile;
+  c->nchunks_max = static_cast<int>((T + kRouterChunk - 1) / kRouterChunk);
+  {
+    // W_r columns staged per router pass: at most 96 KB of shared memory
+    const int vec_span = 32 * (16 / static_cast<int>(c->esize));
+    const int emax = E <= 4 ? 4 : (E <= 8 ? 8 : 16);
+    int dc = (96 * 1024) / (emax * static_cast<int>(c->esize));
+    dc = dc / vec_span * vec_span;
+    c->dchunk = static_cast<int>(d) < dc ? static_cast<int>(d) : dc;
+  }
+  const size_t h_es = cfg->dtype == COLIBRI_DTYPE_BF16 ? 2 : 4;
+  size_t off = 0;
+  auto carve = [&](size_t bytes) {
+    size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  const size_t o_xp = carve(c->rows_alloc * d * c->esize);
+  const size_t o_h = carve(c->rows_alloc * f * h_es);
+  const size_t o_y = carve(c->rows_alloc * d * 4);
+  const size_t o_idx = carve(2 * T * 4);
+  const size_t o_gate = carve(2 * T * 4);
+  const size_t o_row = carve(2 * T * 4);
+  const size_t o_tok = carve(c->rows_alloc * 4);
+  const size_t o_hist = carve(static_cast<size_t>(c->nchunks_max) * E * 4);
+  const size_t o_sched = carve(sizeof(Sched));
+  const size_t o_xs = carve(T * d * c->esize);
+  const size_t o_os = carve(T * d * c->out_esize);
+  c->ws_bytes = off;
+  if (cudaMalloc(&c->ws, c->ws_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete c;
+    return COLIBRI_ERR_OOM;
+  }
+  char* b = static_cast<char*>(c->ws);
+  c->xp = b + o_xp;
+  c->h = b + o_h;
+  c->y = reinterpret_cast<float*>(b + o_y);
+  c->idx = reinterpret_cast<int32_t*>(b + o_idx);
+  c->gate = reinterpret_cast<float*>(b + o_gate);
+  c->row_of = reinterpret_cast<int32_t*>(b + o_row);
+  c->tok_of_row = reinterpret_cast<int32_t*>(b + o_tok);
+  c->hist = reinterpret_cast<int32_t*>(b + o_hist);
+  c->sched = reinterpret_cast<Sched*>(b + o_sched);
+  c->x_stage = b + o_xs;
+  c->out_stage = b + o_os;
+  if (cudaMemset(c->ws, 0, c->ws_bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    colibri_moe_destroy(c);
+    return COLIBRI_ERR_CUDA;
+  }
+  if (cfg->dtype == COLIBRI_DTYPE_BF16) {
+    if (!make_tmap(&c->tm_xp, c->xp, d, c->rows_alloc, kRowTile) ||
+        !make_tmap(&c->tm_h, c->h, f, c->rows_alloc, kRowTile)) {
+      colibri_moe_destroy(c);
+      return COLIBRI_ERR_CUDA;
+    }
+  }
+  *out = c;
+  return COLIBRI_OK;
+}
+
+int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_weights_t* w, void* stream) {
+  if (!ctx || !w) return COLIBRI_ERR_INVALID_ARG;
+  const colibri_moe_config_t& c = ctx->cfg;
+  const int E = c.num_experts;
+  const bool swiglu = c.act == COLIBRI_ACT_SWIGLU;
+  // presence checks: every tensor the activation needs, and none it does not use
+  if (!w->w_router || !w->w1 || !w->w2) return COLIBRI_ERR_BAD_WEIGHTS;
+  if ((c.has_router_bias != 0) != (w->b_router != nullptr)) return COLIBRI_ERR_BAD_WEIGHTS;
+  if (swiglu && (!w->w3 || w->b1 || w->b2)) return COLIBRI_ERR_BAD_WEIGHTS;
+  if (!swiglu && (w->w3 || !w->b1 || !w->b2)) return COLIBRI_ERR_BAD_WEIGHTS;
+  for (int e = 0; e < E; ++e) {
+    if (!w->w1[e] || !w->w2[e]) return COLIBRI_ERR_BAD_WEIGHTS;
+    if (swiglu && !w->w3[e]) return COLIBRI_ERR_BAD_WEIGHTS;
+    if (!swiglu && (!w->b1[e] || !w->b2[e])) return COLIBRI_ERR_BAD_WEIGHTS;
+  }
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return COLIBRI_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t d = c.d_model, f = c.d_ff, es = ctx->esize;
+  size_t off = 0;
+  auto carve = [&](size_t bytes) {
+    size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  const size_t o_wr = carve(E * d * es);
+  const size_t o_br = carve(E * 4);
+  const size_t o_w13 = carve(E * static_cast<size_t>(ctx->n_up) * d * es);
+  const size_t o_w3 = (swiglu && c.dtype == COLIBRI_DTYPE_F32) ? carve(E * f * d * es) : 0;
+  const size_t o_w2 = carve(E * d * f * es);
+  const size_t o_b1 = carve(E * f * 4);
+  const size_t o_b2 = carve(E * d * 4);
+  if (ctx->warena && ctx->warena_bytes != off) {
+    cudaFree(ctx->warena);
+    ctx->warena = nullptr;
+  }
+  ctx->loaded = false;
+  if (!ctx->warena) {
+    if (cudaMalloc(&ctx->warena, off) != cudaSuccess) {
+      cudaGetLastError();
+      return COLIBRI_ERR_OOM;
+    }
+    ctx->warena_bytes = off;
+  }
+  char* b = static_cast<char*>(ctx->warena);
+  ctx->w_router = b + o_wr;
+  ctx->b_router = c.has_router_bias ? reinterpret_cast<float*>(b + o_br) : nullptr;
+  ctx->w13 = b + o_w13;
+  ctx->w3 = (swiglu && c.dtype == COLIBRI_DTYPE_F32) ? b + o_w3 : nullptr;
+  ctx->w2 = b + o_w2;
+  ctx->b1 = swiglu ? nullptr : reinterpret_cast<float*>(b + o_b1);
+  ctx->b2 = swiglu ? nullptr : reinterpret_cast<float*>(b + o_b2);
+
+  bool ok = cudaMemcpyAsync(ctx->w_router, w->w_router, E * d * es, cudaMemcpyDefault, s) == cudaSuccess;
+  if (ok && ctx->b_router)
+    ok = cudaMemcpyAsync(ctx->b_router, w->b_router, E * 4, cudaMemcpyDefault, s) == cudaSuccess;
+  const size_t mat = f * d * es;  // bytes of one [f, d] matrix
+  for (int e = 0; ok && e < E; ++e) {
+    char* w13e = static_cast<char*>(ctx->w13) + static_cast<size_t>(e) * ctx->n_up * d * es;
+    if (swiglu && c.dtype == COLIBRI_DTYPE_BF16) {
+      // gate rows [128j, 128j+128) -> arena rows [256j, 256j+128); up rows -> [256j+128, 256j+256)
+      const size_t blk = 128 * d * es;
+      ok = cudaMemcpy2DAsync(w13e, 2 * blk, w->w1[e], blk, blk, f / 128, cudaMemcpyDefault, s) == cudaSuccess &&
+           cudaMemcpy2DAsync(w13e + blk, 2 * blk, w->w3[e], blk, blk, f / 128, cudaMemcpyDefault, s) == cudaSuccess;
+    } else {
+      ok = cudaMemcpyAsync(w13e, w->w1[e], mat, cudaMemcpyDefault, s) == cudaSuccess;
+      if (ok && ctx->w3)
+        ok = cudaMemcpyAsync(static_cast<char*>(ctx->w3) + e * mat, w->w3[e], mat, cudaMemcpyDefault, s) ==
+             cudaSuccess;
+    }
+    if (ok)
+      ok = cudaMemcpyAsync(static_cast<char*>(ctx->w2) + e * mat, w->w2[e], mat, cudaMemcpyDefault, s) ==
+           cudaSuccess;
+    if (ok && !swiglu)
+      ok = cudaMemcpyAsync(ctx->b1 + e * f, w->b1[e], f * 4, cudaMemcpyDefault, s) == cudaSuccess &&
+           cudaMemcpyAsync(ctx->b2 + e * d, w->b2[e], d * 4, cudaMemcpyDefault, s) == cudaSuccess;
+  }
+  if (ok) ok = cudaStreamSynchronize(s) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    return COLIBRI_ERR_CUDA;
+  }
+  if (c.dtype == COLIBRI_DTYPE_BF16) {
+    const int bn = tc_gemm_block_n();
+    if (!make_tmap(&ctx->tm_w13, ctx->w13, d, static_cast<uint64_t>(E) * ctx->n_up, bn) ||
+        !make_tmap(&ctx->tm_w2, ctx->w2, f, static_cast<uint64_t>(E) * d, bn))
+      return COLIBRI_ERR_CUDA;
+  }
+  ctx->loaded = true;
+  return COLIBRI_OK;
+}
+
+static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t T, cudaStream_t s) {
+  const colibri_moe_config_t& c = ctx->cfg;
+  const int E = c.num_experts, d = c.d_model, f = c.d_ff;
+  const bool bf16 = c.dtype == COLIBRI_DTYPE_BF16;
+  const bool swiglu = c.act == COLIBRI_ACT_SWIGLU;
+  const bool timed = static_cast<int>(ctx->events.size()) == kNumStages + 1;
+  auto mark = [&](int i) {
+    if (timed) cudaEventRecord(ctx->events[i], s);
+  };
+  const int nchunks = (T + kRouterChunk - 1) / kRouterChunk;
+  int64_t max_mtiles = (2 * static_cast<int64_t>(T) + (kRowTile - 1) * E) / kRowTile;
+  if (max_mtiles > ctx->rows_alloc / kRowTile) max_mtiles = ctx->rows_alloc / kRowTile;
+
+  mark(0);
+  RouterArgs ra{x, ctx->w_router, ctx->b_router, T, d, E, ctx->dchunk, ctx->idx, ctx->gate, ctx->row_of,
+                ctx->hist, ctx->sched};
+  if (launch_router(c.dtype, ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  mark(1);
+  GatherArgs ga{x, ctx->idx, ctx->row_of, ctx->hist, T, d, E, ctx->rows_alloc, ctx->xp, ctx->tok_of_row, ctx->sched};
+  if (launch_gather(c.dtype, ga, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  mark(2);
+  if (bf16) {
+    const int bn = tc_gemm_block_n();
+    GemmArgs up{ctx->sched, E, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns,
+                 &ctx->sched->status};
+    int64_t tiles = max_mtiles * up.n_tiles;
+    int grid = static_cast<int>(tiles < ctx->num_sms ? tiles : ctx->num_sms);
+    if (launch_tc_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, ctx->tm_xp, ctx->tm_w13, up, grid, s) != cudaSuccess)
+      return COLIBRI_ERR_CUDA;
+    mark(3);
+    GemmArgs dn{ctx->sched, E, f, d, d / bn, ctx->y, d, ctx->b2, d, ctx->timeout_ns, &ctx->sched->status};
+    tiles = max_mtiles * dn.n_tiles;
+    grid = static_cast<int>(tiles < ctx->num_sms ? tiles : ctx->num_sms);
+    if (launch_tc_gemm(kEpiStoreF32, ctx->tm_h, ctx->tm_w2, dn, grid, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  } else {
+    SimtGemmArgs up{ctx->sched, E, d, f, static_cast<const float*>(ctx->xp), static_cast<const float*>(ctx->w13),
+                    static_cast<const float*>(ctx->w3), ctx->b1, static_cast<float*>(ctx->h)};
+    if (launch_simt_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, up, static_cast<int>(max_mtiles), s) != cudaSuccess)
+      return COLIBRI_ERR_CUDA;
+    mark(3);
+    SimtGemmArgs dn{ctx->sched, E, f, d, static_cast<const float*>(ctx->h), static_cast<const float*>(ctx->w2),
+                    nullptr, ctx->b2, ctx->y};
+    if (launch_simt_gemm(kEpiStoreF32, dn, static_cast<int>(max_mtiles), s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  }
+  mark(4);
+  CombineArgs ca{ctx->y, ctx->row_of, ctx->gate, T, d, out};
+  if (launch_combine(c.out_dtype, ca, ctx->num_sms, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  mark(5);
+  ctx->last_T = T;
+  return COLIBRI_OK;
+}
+
+int colibri_moe_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t T, void* stream) {
+  if (!ctx) return COLIBRI_ERR_INVALID_ARG;
+  if (T < 0 || T > ctx->cfg.max_tokens) return COLIBRI_ERR_INVALID_ARG;
+  if (!ctx->loaded) return COLIBRI_ERR_STATE;
+  if (T == 0) return COLIBRI_OK;
+  if (!x || !out) return COLIBRI_ERR_INVALID_ARG;
+  const size_t xb = static_cast<size_t>(T) * ctx->cfg.d_model * ctx->esize;
+  const size_t ob = static_cast<size_t>(T) * ctx->cfg.d_model * ctx->out_esize;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15) return COLIBRI_ERR_INVALID_ARG;
+  if (overlap(x, xb, out, ob)) return COLIBRI_ERR_INVALID_ARG;
+  if (!is_device_ptr(x, ctx->device) || !is_device_ptr(out, ctx->device)) return COLIBRI_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return COLIBRI_ERR_CUDA;
+  return enqueue_forward(ctx, x, out, T, static_cast<cudaStream_t>(stream));
+}
+
+int colibri_moe_forward_host(colibri_moe_t* ctx, const void* x_host, void* out_host, int32_t T, void* stream) {
+  if (!ctx) return COLIBRI_ERR_INVALID_ARG;
+  if (T < 0 || T > ctx->cfg.max_tokens) return COLIBRI_ERR_INVALID_ARG;
+  if (!ctx->loaded) return COLIBRI_ERR_STATE;
+  if (T == 0) return COLIBRI_OK;
+  if (!x_host || !out_host) return COLIBRI_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return COLIBRI_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t xb = static_cast<size_t>(T) * ctx->cfg.d_model * ctx->esize;
+  const size_t ob = static_cast<size_t>(T) * ctx->cfg.d_model * ctx->out_esize;
+  if (cudaMemcpyAsync(ctx->x_stage, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    cudaGetLastError();
+    return COLIBRI_ERR_CUDA;
+  }
+  int rc = enqueue_forward(ctx, ctx->x_stage, ctx->out_stage, T, s);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(out_host, ctx->out_stage, ob, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return COLIBRI_ERR_CUDA;
+  }
+  return COLIBRI_OK;
+}
+
+int colibri_moe_get_routing(colibri_moe_t* ctx, int32_t* idx, float* gate, int32_t* counts, int32_t* offsets,
+                            int32_t* row_of, void* stream) {
+  if (!ctx) return COLIBRI_ERR_INVALID_ARG;
+  if (ctx->last_T < 0) return COLIBRI_ERR_STATE;
+  const void* ptrs[5] = {idx, gate, counts, offsets, row_of};
+  for (const void* p : ptrs)
+    if (p && !is_device_ptr(p, ctx->device)) return COLIBRI_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return COLIBRI_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t T = static_cast<size_t>(ctx->last_T), E = ctx->cfg.num_experts;
+  bool ok = true;
+  if (idx && T) ok = ok && cudaMemcpyAsync(idx, ctx->idx, 2 * T * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+  if (gate && T) ok = ok && cudaMemcpyAsync(gate, ctx->gate, 2 * T * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+  if (row_of && T)
+    ok = ok && cudaMemcpyAsync(row_of, ctx->row_of, 2 * T * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+  if (T == 0) {
+    if (counts) ok = ok && cudaMemsetAsync(counts, 0, E * 4, s) == cudaSuccess;
+    if (offsets) ok = ok && cudaMemsetAsync(offsets, 0, (E + 1) * 4, s) == cudaSuccess;
+  } else {
+    if (counts)
+      ok = ok && cudaMemcpyAsync(counts, ctx->sched->counts, E * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+    if (offsets)
+      ok = ok &&
+           cudaMemcpyAsync(offsets, ctx->sched->offsets, (E + 1) * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+  }
+  if (!ok) {
+    cudaGetLastError();
+    return COLIBRI_ERR_CUDA;
+  }
+  return COLIBRI_OK;
+}
+
+int colibri_moe_debug_buffer(colibri_moe_t* ctx, int32_t which, void** ptr, int64_t* rows) {
+  if (!ctx || !ptr) return COLIBRI_ERR_INVALID_ARG;
+  void* p = nullptr;
+  switch (which) {
+    case 0: p = ctx->xp; break;
+    case 1: p = ctx->h; break;
+    case 2: p = ctx->y; break;
+    case 3: p = ctx->tok_of_row; break;
+    default: return COLIBRI_ERR_INVALID_ARG;
+  }
+  *ptr = p;
+  if (rows) *rows = ctx->rows_alloc;
+  return COLIBRI_OK;
+}
+
+int colibri_moe_num_stages(const colibri_moe_t* ctx, int32_t* n_stages) {
+  if (!ctx || !n_stages) return COLIBRI_ERR_INVALID_ARG;
+  *n_stages = kNumStages;
+  return COLIBRI_OK;
+}
+
+int colibri_moe_set_stage_events(colibri_moe_t* ctx, void* const* events, int32_t n) {
+  if (!ctx) return COLIBRI_ERR_INVALID_ARG;
+  if (!events || n == 0) {
+    ctx->events.clear();
+    return COLIBRI_OK;
+  }
+  if (n != kNumStages + 1) return COLIBRI_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i)
+    if (!events[i]) return COLIBRI_ERR_INVALID_ARG;
+  ctx->events.assign(reinterpret_cast<cudaEvent_t const*>(events), reinterpret_cast<cudaEvent_t const*>(events) + n);
+  return COLIBRI_OK;
+}
+
+int colibri_moe_device_status(colibri_moe_t* ctx, int32_t* status) {
+  if (!ctx || !status) return COLIBRI_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return COLIBRI_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(&v, &ctx->sched->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(&ctx->sched->status, 0, 4) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return COLIBRI_ERR_CUDA;
+  }
+  *status = v;
+  return COLIBRI_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,452 @@
+// Grouped expert GEMM on the 5th-generation tensor cores (tcgen05 + TMEM), operands by TMA.
+//
+// The Compute stage of zskr.cn/news/2272131 ("Colibri: a lightweight C MoE inference engine for
+// edge devices") 2.1 is a grouped GEMM, one GEMM per expert over that expert's contiguous rows;
+// the expert weights sit in one contiguous block per expert (2.2), each expert is an affine map
+// with W stored [out, in] (hnwysp.cn/news/30485 3.2), and the activation is fused into the expert
+// kernel (m.nxbn.cn/news/48047 2.1).  Here:
+//
+//   C[rows_e, n-tile] = A[rows_e, K] * B_e[n-tile, K]^T       bf16 x bf16 -> fp32 in TMEM
+//
+// A = expert-contiguous activations (Xp for the up projection, H for the down projection), both
+// operands K-major, which is the nn.Linear [out, in] layout as stored.
+//
+// Design (one CTA per SM, persistent, warp-specialised, 192 threads):
+//   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage, 128-byte swizzle,
+//               STAGES-deep shared-memory ring guarded by full/empty mbarriers;
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators), one lane issues
+//               tcgen05.mma (M=128, N=256, K=16, kind::f16 with bf16 inputs) and commits each
+//               stage back to the producer and each finished accumulator to the epilogue;
+//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time, activation, store.  The two
+//               accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+// Tiles are (expert, 128-row tile, 256-column tile), row tile fastest, so CTAs that run at the same
+// time share one weight tile (read once from HBM, then from L2) while the expert's activation rows
+// stay L2-resident.  Expert segments are padded to 128 rows, so a tile never spans two experts;
+// rows past the expert's count are computed but not stored.
+//
+// Every mbarrier wait is bounded (GemmArgs::timeout_ns): on expiry the kernel raises a bit in the
+// device status word, stops all roles, waits (bounded) for its own TMA copies and MMAs, frees
+// TMEM and returns.
+#include "moe_internal.cuh"
+
+namespace colibri {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
+constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 4 * (3 * kMaxE + 3);
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for the phase of `bar` with parity `parity` to complete.  Returns false if *abort becomes
+// nonzero or timeout_ns elapses first.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Shared-memory matrix descriptor: K-major operand written by TMA with 128-byte swizzle
+// (rows of 128 bytes, 8-row / 1024-byte swizzle atoms stacked along M/N).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused for swizzled K-major)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset: next 8-row group
+  d |= static_cast<uint64_t>(1) << 46;                  // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                  // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both K-major, M x N.
+__host__ __device__ constexpr uint32_t make_idesc_bf16(int m, int n) {
+  return (1u << 4)                                  // D format: fp32
+         | (1u << 7)                                // A format: bf16
+         | (1u << 10)                               // B format: bf16
+         | (static_cast<uint32_t>(n >> 3) << 17)    // N / 8
+         | (static_cast<uint32_t>(m >> 4) << 24);   // M / 16
+}
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// 32 TMEM lanes x 32 consecutive fp32 columns into registers.  The wait is in the same asm
+// statement, so no use of the outputs can be scheduled before the data has arrived.
+__device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+struct TileCoord {
+  int e, m, n;
+};
+
+// tile -> (expert, row tile inside the expert, column tile); row tiles fastest.
+__device__ __forceinline__ TileCoord decode_tile(int tile, const int* mtile_start, int E, int n_tiles) {
+  int e = 0;
+  while (e + 1 < E && mtile_start[e + 1] * n_tiles <= tile) ++e;
+  const int local = tile - mtile_start[e] * n_tiles;
+  const int mt = mtile_start[e + 1] - mtile_start[e];
+  TileCoord c;
+  c.e = e;
+  c.n = local / mt;
+  c.m = local - c.n * mt;
+  return c;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                           const GemmArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_counts = reinterpret_cast<int*>(tmem_slot + 4);
+  int* s_offsets = s_counts + kMaxE;
+  int* s_mstart = s_offsets + kMaxE + 1;
+
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + STAGES);
+  const uint32_t tfull0 = smem_u32(bars + 2 * STAGES);
+  const uint32_t tempty0 = smem_u32(bars + 2 * STAGES + 2);
+  const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = a.E;
+
+  if (threadIdx.x < kMaxE) s_counts[threadIdx.x] = threadIdx.x < E ? a.sched->counts[threadIdx.x] : 0;
+  if (threadIdx.x < kMaxE + 1) {
+    s_offsets[threadIdx.x] = threadIdx.x <= E ? a.sched->offsets[threadIdx.x] : 0;
+    s_mstart[threadIdx.x] = threadIdx.x <= E ? a.sched->mtile_start[threadIdx.x] : 0;
+  }
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull0 + 8 * i, 1);
+      mbar_init(tempty0 + 8 * i, 4);
+    }
+    mbar_init(drain, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total_tiles = s_mstart[E] * a.n_tiles;
+  const int num_kb = (a.K + BK - 1) / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0;  // bit s: full[s] armed at least once
+      uint32_t armed_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const TileCoord c = decode_tile(tile, s_mstart, E, a.n_tiles);
+        const int a_row = s_offsets[c.e] + c.m * BM;
+        const int b_row = c.e * a.n_per_expert + c.n * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, s_abort, a.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full0 + 8 * stage, STAGE_BYTES);
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          tma_load_2d(smem_u32(sA + stage * A_BYTES), &tmA, full0 + 8 * stage, kb * BK, a_row);
+          tma_load_2d(smem_u32(sB + stage * B_BYTES), &tmB, full0 + 8 * stage, kb * BK, b_row);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        if (!*s_abort) atomicOr(a.status, kStatusTimeoutProducer);
+        *s_abort = 1;
+      }
+      // wait (bounded) for every copy this thread issued to land before the CTA can exit
+      for (int s = 0; s < STAGES; ++s)
+        if (armed & (1u << s)) {
+          volatile int never = 0;
+          mbar_wait(full0 + 8 * s, (armed_phase >> s) & 1u, &never, a.timeout_ns);
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = make_idesc_bf16(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, s_abort, a.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, s_abort, a.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            umma_bf16(d_tmem, sw128_desc(a_addr + k * UMMA_K * 2), sw128_desc(b_addr + k * UMMA_K * 2), idesc,
+                      (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty0 + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(tfull0 + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        if (!*s_abort) atomicOr(a.status, kStatusTimeoutMma);
+        *s_abort = 1;
+      }
+      // all MMAs issued by this thread have finished once `drain` completes
+      umma_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never, a.timeout_ns);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      const TileCoord c = decode_tile(tile, s_mstart, E, a.n_tiles);
+      bool ok = mbar_wait(tfull0 + 8 * acc, acc_phase, s_abort, a.timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0 && !*s_abort) atomicOr(a.status, kStatusTimeoutEpilogue);
+        if (lane == 0) *s_abort = 1;
+        break;
+      }
+      tc_fence_after();
+      const int row = s_offsets[c.e] + c.m * BM + q * 32 + lane;
+      const bool valid = row < s_offsets[c.e] + s_counts[c.e];
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if constexpr (EPI == kEpiSwiGLU) {
+        // columns [0,128) = gate, [128,256) = up, for H columns n*128 .. n*128+127
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(row) * a.ldo + c.n * (BN / 2);
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t g[32], u[32];
+          tmem_ld32_sync(tbase + ch * 32, g);
+          tmem_ld32_sync(tbase + 128 + ch * 32, u);
+          uint32_t p[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+            const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+            const float h0 = (g0 / (1.0f + expf(-g0))) * u0;
+            const float h1 = (g1 / (1.0f + expf(-g1))) * u1;
+            p[i] = pack_bf16(h0, h1);
+          }
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
+          }
+        }
+      } else if constexpr (EPI == kEpiReluBias) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(row) * a.ldo + c.n * BN;
+        const float* bias = a.bias + static_cast<size_t>(c.e) * a.out_cols + c.n * BN;
+#pragma unroll 1
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t v[32];
+          tmem_ld32_sync(tbase + ch * 32, v);
+          uint32_t p[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float h0 = fmaxf(__uint_as_float(v[2 * i]) + bias[ch * 32 + 2 * i], 0.f);
+            const float h1 = fmaxf(__uint_as_float(v[2 * i + 1]) + bias[ch * 32 + 2 * i + 1], 0.f);
+            p[i] = pack_bf16(h0, h1);
+          }
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) dst[w] = make_uint4(p[4 * w], p[4 * w + 1], p[4 * w + 2], p[4 * w + 3]);
+          }
+        }
+      } else {
+        float* out = static_cast<float*>(a.out) + static_cast<size_t>(row) * a.ldo + c.n * BN;
+        const float* bias = a.bias ? a.bias + static_cast<size_t>(c.e) * a.out_cols + c.n * BN : nullptr;
+#pragma unroll 1
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t v[32];
+          tmem_ld32_sync(tbase + ch * 32, v);
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(out + ch * 32);
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+              float4 o = make_float4(__uint_as_float(v[4 * w]), __uint_as_float(v[4 * w + 1]),
+                                     __uint_as_float(v[4 * w + 2]), __uint_as_float(v[4 * w + 3]));
+              if (bias) {
+                o.x += bias[ch * 32 + 4 * w];
+                o.y += bias[ch * 32 + 4 * w + 1];
+                o.z += bias[ch * 32 + 4 * w + 2];
+                o.w += bias[ch * 32 + 4 * w + 3];
+              }
+              dst[w] = o;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int EPI>
+cudaError_t launch_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid, cudaStream_t s) {
+  auto k = tc_grouped_gemm_kernel<EPI>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  k<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_gemm_block_n() { return BN; }
+int tc_gemm_threads() { return NUM_THREADS; }
+
+cudaError_t launch_tc_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
+                           cudaStream_t s) {
+  if (grid <= 0) return cudaSuccess;
+  switch (epi) {
+    case kEpiSwiGLU: return launch_t<kEpiSwiGLU>(tmA, tmB, a, grid, s);
+    case kEpiReluBias: return launch_t<kEpiReluBias>(tmA, tmB, a, grid, s);
+    default: return launch_t<kEpiStoreF32>(tmA, tmB, a, grid, s);
+  }
+}
+
+}  // namespace colibri

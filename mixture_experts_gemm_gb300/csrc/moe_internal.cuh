@@ -1,0 +1,109 @@
+// Internal declarations shared by the host code and the kernels of the MoE layer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace colibri {
+
+constexpr int kMaxE = 16;            // experts per layer (upper bound)
+constexpr int kRowTile = 128;        // expert row segments start on multiples of this (GEMM M tile)
+constexpr int kRouterChunk = 32;     // tokens per router CTA (4 per warp)
+constexpr int kRouterThreads = 256;
+
+// Device status word bits (sticky until read by colibri_moe_device_status).
+enum : int32_t {
+  kStatusTimeoutProducer = 1 << 0,
+  kStatusTimeoutMma = 1 << 1,
+  kStatusTimeoutEpilogue = 1 << 2,
+  kStatusBadRow = 1 << 3,
+};
+
+// Routing summary in device memory.  Written by the last CTA of the router kernel, read by
+// every later stage of the same forward.
+struct Sched {
+  int32_t counts[kMaxE];           // rows routed to each expert
+  int32_t offsets[kMaxE + 1];      // first row of each expert segment (segments padded to 128 rows)
+  int32_t mtile_start[kMaxE + 1];  // prefix sum of ceil(counts / 128): M tiles before each expert
+  uint32_t ticket;                 // router CTAs finished (reset to 0 by the last one)
+  int32_t status;                  // device status word (kStatus* bits)
+};
+
+struct RouterArgs {
+  const void* x;           // [T, d] dtype
+  const void* w_router;    // [E, d] dtype
+  const float* b_router;   // [E] or nullptr
+  int T, d, E;
+  int dchunk;              // columns of W_r staged in shared memory per pass
+  int32_t* idx;            // [T, 2]
+  float* gate;             // [T, 2]
+  int32_t* rank;           // [T, 2] rank inside the router chunk; rewritten to the row by gather
+  int32_t* hist;           // [nchunks, E] counts per chunk, rewritten to first row per (chunk, expert)
+  Sched* sched;
+};
+
+struct GatherArgs {
+  const void* x;           // [T, d]
+  const int32_t* idx;      // [T, 2]
+  int32_t* row_of;         // [T, 2] in: rank in chunk, out: row
+  const int32_t* chunk_base;  // [nchunks, E]
+  int T, d, E;
+  int64_t rows_alloc;
+  void* xp;                // [rows_alloc, d]
+  int32_t* token_of_row;   // [rows_alloc]
+  Sched* sched;
+};
+
+struct CombineArgs {
+  const float* y;          // [rows, d] fp32
+  const int32_t* row_of;   // [T, 2]
+  const float* gate;       // [T, 2]
+  int T, d;
+  void* out;               // [T, d] fp32 or bf16
+};
+
+enum GemmEpilogue : int {
+  kEpiSwiGLU = 0,    // up projection, gate/up interleaved -> H = silu(g) * u
+  kEpiReluBias = 1,  // up projection -> H = max(acc + b1, 0)
+  kEpiStoreF32 = 2,  // down projection -> Y = acc (+ b2)
+};
+
+struct GemmArgs {
+  const Sched* sched;
+  int E;
+  int K;                    // reduction length
+  int n_per_expert;         // rows of the weight operand per expert
+  int n_tiles;              // column tiles per expert
+  void* out;                // H or Y
+  int64_t ldo;              // elements per output row
+  const float* bias;        // [E, out_cols] or nullptr
+  int out_cols;             // output columns per expert (f for up, d for down)
+  uint64_t timeout_ns;      // bound on every wait inside the kernel
+  int32_t* status;          // device status word (Sched::status)
+};
+
+// fp32 SIMT grouped GEMM operands (row-major, K contiguous)
+struct SimtGemmArgs {
+  const Sched* sched;
+  int E, K, N;              // N = output columns per expert
+  const float* a;           // [rows, K]
+  const float* b;           // [E * N, K]  (W1 / W_gate / W2)
+  const float* b3;          // [E * N, K]  W_up for SwiGLU, else nullptr
+  const float* bias;        // [E, N] or nullptr
+  float* out;               // [rows, N]
+};
+
+// launchers (return cudaGetLastError() of the launch)
+cudaError_t launch_router(int dtype, const RouterArgs& a, int nchunks, cudaStream_t s);
+cudaError_t launch_gather(int dtype, const GatherArgs& a, cudaStream_t s);
+cudaError_t launch_combine(int out_dtype, const CombineArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_tc_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                           int grid, cudaStream_t s);
+cudaError_t launch_simt_gemm(int epi, const SimtGemmArgs& a, int max_mtiles, cudaStream_t s);
+int router_smem_bytes(int dtype, int E, int dchunk);
+int tc_gemm_block_n();
+int tc_gemm_threads();
+
+}  // namespace colibri

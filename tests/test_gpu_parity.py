@@ -1,0 +1,282 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle, on seeded inputs.
+
+Routing (idx, counts, per-expert ranks) must match bit for bit outside near ties (logit gap < 1e-5);
+outputs within max|err| / RMS(out) <= 1e-4 (fp32 layers) and <= 2e-2 (bf16 layers).  Shapes run
+from a few tiles with ragged tails up to the full benchmark workloads (sampled rows there).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import testgen
+from moe_check import (TOL_BF16, TOL_F32, check_routing, make_layer, rel_err, run, sample_tokens, torch_from_bits,
+                       x_device)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu(cuda_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    torch.cuda.synchronize()
+
+
+def _full_check(li, T=None, tol=None, out_dtype="f32", layer=None):
+    s = li.shape
+    T = s.T if T is None else T
+    own = layer is None
+    if own:
+        layer = make_layer(li, max_tokens=T, out_dtype=out_dtype)
+    x = x_device(li, T)
+    out, r = run(layer, x)
+    L = oracle.OracleLayer.from_inputs(li)
+    ref = L.forward(li.x_f32[:T])
+    check_routing(r, ref["logits"], ref["idx"], ref["gate"], s.num_experts, ref["row_of"], ref["offsets_raw"])
+    tol = tol if tol is not None else (TOL_F32 if s.dtype == "f32" else TOL_BF16)
+    err = rel_err(out, ref["out"])
+    assert err <= tol, f"max|err|/RMS = {err:.3e} > {tol}"
+    assert layer.device_status() == 0
+    return layer, out, r, ref, err
+
+
+# ------------------------------------------------------------------ fp32 path (SIMT)
+def test_tiny_fp32_workload():
+    li = testgen.make_inputs(testgen.CONFIGS["tiny-moe-4e2r"])
+    layer, out, r, ref, err = _full_check(li)
+    # the gather copies rows bit for bit
+    xp = layer.debug_tensor(0).cpu().numpy()
+    tok = layer.debug_tensor(3).cpu().numpy()
+    for t in range(li.shape.T):
+        for s in range(2):
+            row = r["row_of"][t, s]
+            assert tok[row] == t
+            assert np.array_equal(xp[row], li.x_f32[t])
+
+
+def _integer_inputs(shape, T, lo=-3, hi=4, wlo=-2, whi=3, seed=0):
+    """Exact-arithmetic workload: small integers, ReLU with integer biases, identical experts, zero
+    router (gates exactly 1/2).  Every fp32 partial sum is an exact integer below 2^24."""
+    rng = np.random.default_rng(seed)
+    d, f, E = shape.d_model, shape.d_ff, shape.num_experts
+    li = testgen.LayerInputs(shape=shape, seed=seed)
+    li.x_f32 = rng.integers(lo, hi, size=(T, d)).astype(np.float32)
+    li.w_router_f32 = np.zeros((E, d), dtype=np.float32)
+    w1 = rng.integers(wlo, whi, size=(f, d)).astype(np.float32)
+    w2 = rng.integers(wlo, whi, size=(d, f)).astype(np.float32)
+    b1 = rng.integers(-3, 4, size=f).astype(np.float32)
+    b2 = rng.integers(-3, 4, size=d).astype(np.float32)
+    li.w1_f32, li.w2_f32 = [w1] * E, [w2] * E
+    li.b1, li.b2 = [b1] * E, [b2] * E
+    if shape.dtype == "bf16":
+        li.x_bits = testgen.f32_to_bf16_bits(li.x_f32)
+        li.w_router_bits = testgen.f32_to_bf16_bits(li.w_router_f32)
+        li.w1_bits = [testgen.f32_to_bf16_bits(w1)] * E
+        li.w2_bits = [testgen.f32_to_bf16_bits(w2)] * E
+    h = np.maximum(li.x_f32.astype(np.int64) @ w1.astype(np.int64).T + b1.astype(np.int64), 0)
+    y = h @ w2.astype(np.int64).T + b2.astype(np.int64)
+    return li, h, y
+
+
+def test_exact_integers_fp32_bit_exact():
+    shape = testgen.LayerShape("int-f32", 100, 256, 512, 4, testgen.ACT_RELU_BIAS, "f32")
+    li, h, y = _integer_inputs(shape, 100)
+    assert np.abs(y).max() < 2 ** 24
+    layer = make_layer(li)
+    out, r = run(layer, x_device(li))
+    assert np.all(r["idx"] == [0, 1]) and np.all(r["gate"] == 0.5)
+    assert np.array_equal(out, y.astype(np.float64))
+
+
+# ------------------------------------------------------------------ bf16 path (tcgen05)
+def test_exact_integers_bf16_tensor_cores_bit_exact():
+    """x, W in {-1, 0, 1}: H <= 256 in magnitude is exact in bf16, so the tcgen05 GEMMs, the ReLU+bias
+    epilogue and the fp32 down projection must reproduce the int64 result bit for bit."""
+    shape = testgen.LayerShape("int-bf16", 300, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")
+    li, h, y = _integer_inputs(shape, 300, lo=-1, hi=2, wlo=-1, whi=2, seed=1)
+    assert np.abs(h).max() <= 256
+    layer = make_layer(li)
+    out, r = run(layer, x_device(li))
+    assert np.all(r["counts"] == [300, 300, 0, 0])
+    Hd = layer.debug_tensor(1).float().cpu().numpy()
+    for t in (0, 1, 150, 299):
+        assert np.array_equal(Hd[r["row_of"][t, 0]], h[t].astype(np.float32))
+    assert np.array_equal(out, y.astype(np.float64))
+    assert layer.device_status() == 0
+
+
+@pytest.mark.parametrize("T", [1, 37, 300, 1000])
+def test_small_bf16_swiglu(T):
+    shape = testgen.LayerShape("small-swiglu", T, 256, 384, 4, testgen.ACT_SWIGLU, "bf16")
+    li = testgen.make_inputs(shape)
+    _full_check(li)
+
+
+def test_small_bf16_relu_bias_with_router_bias():
+    shape = testgen.LayerShape("small-relu", 500, 512, 512, 6, testgen.ACT_RELU_BIAS, "bf16", zipf_router_bias=True)
+    li = testgen.make_inputs(shape)
+    _full_check(li)
+
+
+def test_1p3b_workload():
+    li = testgen.make_inputs(testgen.CONFIGS["1.3b-8e"])
+    _, _, _, _, err = _full_check(li)
+    assert err < 0.01
+
+
+def test_skewed_16e_workload():
+    s = testgen.CONFIGS["skewed-16e"]
+    li = testgen.make_inputs(s)
+    layer = make_layer(li)
+    out, r = run(layer, x_device(li))
+    L = oracle.OracleLayer.from_inputs(li)
+    logits = L.router_logits(li.x_f32)
+    idx, gate = L.top2(logits)
+    counts, offs, row_of, _ = L.dispatch(idx)
+    check_routing(r, logits, idx, gate, s.num_experts, row_of, offs)
+    assert counts[0] == counts.max() and counts[0] > 2 * np.sort(counts)[-2] * 0.5
+    tokens = sample_tokens(idx, s.num_experts, 256)
+    ref = L.forward_rows(li.x_f32, idx, gate, tokens)
+    err = rel_err(out[tokens], ref)
+    assert err <= TOL_BF16
+    assert layer.device_status() == 0
+
+
+@pytest.fixture(scope="module")
+def mixtral():
+    s = testgen.CONFIGS["mixtral-prefill"]
+    li = testgen.make_inputs(s)
+    layer = make_layer(li)
+    L = oracle.OracleLayer.from_inputs(li)
+    yield li, layer, L
+    layer.close()
+
+
+def test_mixtral_prefill_workload(mixtral):
+    li, layer, L = mixtral
+    s = li.shape
+    out, r = run(layer, x_device(li))
+    logits = L.router_logits(li.x_f32)
+    idx, gate = L.top2(logits)
+    counts, offs, row_of, _ = L.dispatch(idx)
+    check_routing(r, logits, idx, gate, s.num_experts, row_of, offs)
+    tokens = sample_tokens(idx, s.num_experts, 48)
+    ref = L.forward_rows(li.x_f32, idx, gate, tokens)
+    err = rel_err(out[tokens], ref)
+    assert err <= TOL_BF16, err
+    assert np.isfinite(out).all()
+    assert layer.device_status() == 0
+
+
+@pytest.mark.parametrize("T", testgen.DECODE_TOKENS)
+def test_mixtral_decode_workload(mixtral, T):
+    li, layer, L = mixtral
+    out, r = run(layer, x_device(li, T))
+    ref = L.forward(li.x_f32[:T])
+    check_routing(r, ref["logits"], ref["idx"], ref["gate"], li.shape.num_experts, ref["row_of"], ref["offsets_raw"])
+    assert rel_err(out, ref["out"]) <= TOL_BF16
+
+
+def test_mixtral_deterministic(mixtral):
+    li, layer, L = mixtral
+    x = x_device(li)
+    a = layer.forward(x).clone()
+    b = layer.forward(x)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ edge cases and the boundary
+def test_zero_router_gives_empty_experts_and_ties():
+    shape = testgen.LayerShape("zero-router", 200, 256, 256, 8, testgen.ACT_SWIGLU, "bf16")
+    li = testgen.make_inputs(shape)
+    li.w_router_f32 = np.zeros_like(li.w_router_f32)
+    li.w_router_bits = testgen.f32_to_bf16_bits(li.w_router_f32)
+    layer, out, r, ref, err = _full_check(li)
+    assert np.all(r["idx"] == [0, 1]) and np.all(r["gate"] == 0.5)
+    assert list(r["counts"]) == [200, 200] + [0] * 6
+
+
+def test_t0_is_noop_and_max_tokens():
+    shape = testgen.LayerShape("edge", 256, 256, 256, 4, testgen.ACT_SWIGLU, "bf16")
+    li = testgen.make_inputs(shape)
+    layer = make_layer(li, max_tokens=256)
+    out = torch.full((0, 256), 7.0, device="cuda")
+    layer.forward(x_device(li, 0), out)
+    _full_check(li, T=256, layer=layer)
+
+
+def test_forward_host_matches_device_forward():
+    shape = testgen.LayerShape("host", 300, 256, 256, 4, testgen.ACT_SWIGLU, "bf16")
+    li = testgen.make_inputs(shape)
+    layer = make_layer(li)
+    x = x_device(li)
+    dev = layer.forward(x).cpu()
+    xh = torch_from_bits(li.x_bits).pin_memory()
+    oh = torch.empty((300, 256), dtype=torch.float32).pin_memory()
+    layer.forward_host(xh, oh)
+    assert torch.equal(dev, oh)
+
+
+def test_bf16_output_dtype():
+    shape = testgen.LayerShape("bf16-out", 400, 256, 256, 4, testgen.ACT_SWIGLU, "bf16")
+    li = testgen.make_inputs(shape)
+    layer = make_layer(li, out_dtype="bf16")
+    out, r = run(layer, x_device(li))
+    ref = oracle.OracleLayer.from_inputs(li).forward(li.x_f32)["out"]
+    rms = math.sqrt(float(np.mean(ref ** 2)))
+    # fp32 tolerance plus one bf16 rounding of the result (half an ulp, 2^-8 relative)
+    bound = TOL_BF16 * rms + np.abs(ref) * 2.0 ** -8
+    assert np.all(np.abs(out - ref) <= bound)
+
+
+def test_error_paths():
+    from mixture_experts_gemm_gb300 import ColibriError, MoELayer
+    shape = testgen.LayerShape("err", 64, 256, 256, 4, testgen.ACT_SWIGLU, "bf16")
+    li = testgen.make_inputs(shape)
+    fresh = MoELayer(256, 256, 4, 64)
+    x = x_device(li)
+    with pytest.raises(ColibriError) as e:
+        fresh.forward(x)
+    assert e.value.code == -5   # weights not loaded
+    with pytest.raises(ColibriError) as e:
+        fresh.get_routing(4)
+    assert e.value.code == -5
+    layer = make_layer(li)
+    big = torch.zeros((65, 256), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ColibriError) as e:
+        layer.forward(big)
+    assert e.value.code == -1   # T > max_tokens
+    with pytest.raises(ColibriError) as e:
+        layer.forward(x.cpu())
+    assert e.value.code == -1   # host pointer where a device pointer is required
+    buf = torch.zeros((64 * 256 * 3,), dtype=torch.bfloat16, device="cuda")
+    xa = buf[: 64 * 256].view(64, 256)
+    with pytest.raises(ColibriError) as e:
+        layer.forward(xa, out=buf[64 * 128: 64 * 128 + 64 * 256 * 2].view(torch.float32).view(64, 256))
+    assert e.value.code == -1   # x and out overlap
+    with pytest.raises(ColibriError) as e:
+        MoELayer(256, 256, 4, 64, act="swiglu").load_weights(li.w_router_bits, [None] * 4, [None] * 4)
+    assert e.value.code == -3   # missing expert weights
+    with pytest.raises(ColibriError) as e:
+        MoELayer(250, 256, 4, 64)
+    assert e.value.code == -6   # d not a multiple of 8
+
+
+def test_stage_events_time_every_stage():
+    shape = testgen.LayerShape("events", 512, 512, 512, 8, testgen.ACT_SWIGLU, "bf16")
+    li = testgen.make_inputs(shape)
+    layer = make_layer(li)
+    n = layer.num_stages()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    layer.set_stage_events(ev)
+    layer.forward(x_device(li))
+    torch.cuda.synchronize()
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+    assert all(t > 0 for t in times)
+    layer.set_stage_events(None)
