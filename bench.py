@@ -1,0 +1,359 @@
+#!/usr/bin/env python3
+"""Throughput of the MoE layer forward on GB300: tokens/s on the Mixtral-8x7B-shaped prefill layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME] [--T T]
+
+One step = one colibri_moe_forward (router, gather, grouped up-GEMM, grouped down-GEMM, combine) over
+a batch of T tokens already resident in HBM.  Prints one JSON line (rank 0).  Under torchrun each
+rank runs the same workload on its own GPU (replicas, weak scaling, no data-path collective); the
+reported time is the max over ranks and the value counts every rank's tokens.
+
+--impl reference times the CPU oracle (fp64 C, OpenMP) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+METRIC = "MoE-layer tokens/s at Mixtral-8x7B shape; % of bf16 tensor peak / HBM BW"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGES = ["router", "gather", "gemm_up", "gemm_down", "combine"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="mixtral-prefill")
+    p.add_argument("--T", type=int, default=None, help="tokens per step (default: the workload's)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU work budget of the oracle baseline")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_desc(s, T):
+    act = "SwiGLU" if s.act == 1 else "ReLU+bias"
+    return (f"{s.name}: T={T} d_model={s.d_model} d_ff={s.d_ff} E={s.num_experts} top-2 {act} {s.dtype}"
+            + (" router-bias zipf" if s.zipf_router_bias else ""))
+
+
+def algorithmic(s, T, active_experts=None):
+    """FLOPs and bytes of one forward counting routed work only (no padding rows)."""
+    n_up = 2 if s.act == 1 else 1
+    es = 2 if s.dtype == "bf16" else 4
+    flops_up = 2.0 * (2 * T) * s.d_model * s.d_ff * n_up
+    flops_down = 2.0 * (2 * T) * s.d_model * s.d_ff
+    flops_router = 2.0 * T * s.num_experts * s.d_model
+    n_act = s.num_experts if active_experts is None else active_experts
+    w_bytes_expert = (n_up + 1) * s.d_model * s.d_ff * es
+    bytes_total = n_act * w_bytes_expert + T * s.d_model * es + T * s.d_model * 4 + s.num_experts * s.d_model * es
+    return dict(flops_up=flops_up, flops_down=flops_down, flops_router=flops_router,
+                flops=flops_up + flops_down + flops_router, bytes=bytes_total,
+                w_bytes_up=n_act * n_up * s.d_model * s.d_ff * es, w_bytes_expert=w_bytes_expert)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", *sel], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception as e:  # no nvidia-smi: report nothing rather than fail the bench
+            log("clock sampler unavailable:", e)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        loaded = [c for c in sm if c > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------- CPU oracle
+def oracle_rate(li, T, seconds, tokens_per_round=None, rounds=None, seed=0):
+    """Time the oracle on a sample of the workload's tokens: routing (logits + top-2) of the sampled
+    tokens and their two experts each.  Returns (tokens/s, tokens timed, wall seconds, threads)."""
+    import numpy as np
+    import oracle
+    L = oracle.OracleLayer.from_inputs(li)
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    rng = np.random.default_rng(seed)
+
+    def one(n):
+        toks = np.sort(rng.choice(T, size=n, replace=False)).astype(np.int32)
+        xs = li.x_f32[toks]
+        t0 = time.perf_counter()
+        logits = L.router_logits(xs)
+        idx, gate = L.top2(logits)
+        L.forward_rows(xs, idx, gate, np.arange(n, dtype=np.int32))
+        return time.perf_counter() - t0
+
+    if tokens_per_round is None:
+        probe = max(1, min(threads, T))
+        dt = one(probe)
+        per_tok = dt / probe
+        tokens_per_round = max(1, min(T, int(seconds / per_tok)))
+        rounds = 1
+    done, wall = 0, 0.0
+    for _ in range(rounds):
+        wall += one(tokens_per_round)
+        done += tokens_per_round
+    return done / wall, done, wall, min(threads, tokens_per_round)
+
+
+def run_reference(args, shape, T):
+    """--impl reference: the oracle as it stands, each step a bounded sample of the workload."""
+    import testgen
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    li = testgen.make_inputs(shape.with_T(T), want_bits=False)
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    # size each step from one probe so the whole run stays within ~2-3 minutes
+    rate, n, wall, _ = oracle_rate(li, T, 1.0)
+    per_step = max(1, min(T, int(rate * 120.0 / max(1, args.steps + args.warmup))))
+    for _ in range(args.warmup):
+        oracle_rate(li, T, 0, tokens_per_round=per_step, rounds=1, seed=1)
+    rate, n, wall, used = oracle_rate(li, T, 0, tokens_per_round=per_step, rounds=args.steps, seed=2)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(shape, T), "sample_tokens_per_step": per_step},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": f"{per_step} random tokens of {T} per step (routing + both experts, fp64)"},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------- GPU arm
+def main():
+    args = parse_args()
+    import testgen
+    shape = testgen.CONFIGS[args.workload]
+    T = args.T if args.T is not None else shape.T
+    if args.impl == "reference":
+        run_reference(args, shape, T)
+        return
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from moe_check import host_weights, x_device
+    import mixture_experts_gemm_gb300 as moe
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # inputs: the layer's weights and one batch of T tokens, generated on the host, copied to HBM
+    li = testgen.make_inputs(shape.with_T(T), want_f32=shape.dtype == "f32")
+    layer = moe.MoELayer(shape.d_model, shape.d_ff, shape.num_experts, T, dtype=shape.dtype,
+                         act="swiglu" if shape.act == testgen.ACT_SWIGLU else "relu_bias",
+                         has_router_bias=shape.zipf_router_bias, out_dtype="f32", device=local)
+    layer.load_weights(**host_weights(li))
+    x = x_device(li).to(dev)
+    out = torch.empty((T, shape.d_model), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    n_st = layer.num_stages()
+
+    for _ in range(max(3, args.warmup)):
+        layer.forward_ptr(x.data_ptr(), out.data_ptr(), T, sh)
+    torch.cuda.synchronize(dev)
+    routing = layer.get_routing(T)
+    counts = routing["counts"].cpu().numpy()
+    active = int((counts > 0).sum())
+
+    # per-step stage events, created before the timed region
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)] for _ in range(args.steps)]
+    arrs = []
+    for evs in ev_sets:
+        for e in evs:
+            e.record(stream)
+        import ctypes
+        arrs.append((ctypes.c_void_p * (n_st + 1))(*[e.cuda_event for e in evs]))
+    torch.cuda.synchronize(dev)
+    lib = moe.lib()
+    import ctypes
+
+    clocks = ClockSampler(local)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for k in range(args.steps):
+        lib.colibri_moe_set_stage_events(layer._h, ctypes.cast(arrs[k], ctypes.c_void_p), n_st + 1)
+        layer.forward_ptr(x.data_ptr(), out.data_ptr(), T, sh)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    lib.colibri_moe_set_stage_events(layer._h, None, 0)
+    ms_total = t_start.elapsed_time(t_end)
+    stage_ms = np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(n_st)] for evs in ev_sets])
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_per_step = ms_total / args.steps
+    value = world * T * args.steps / (ms_total / 1e3)
+
+    # end to end through the C ABI with host buffers (pinned): H2D of x, forward, D2H of out
+    e2e = None
+    if not args.no_e2e:
+        if shape.dtype == "bf16":
+            from moe_check import torch_from_bits
+            xh = torch_from_bits(li.x_bits).pin_memory()
+        else:
+            xh = torch.from_numpy(li.x_f32).pin_memory()
+        oh = torch.empty((T, shape.d_model), dtype=torch.float32).pin_memory()
+        for _ in range(3):
+            layer.forward_host(xh, oh, stream)
+        k_e2e = max(1, min(args.steps, 100))
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(k_e2e):
+            layer.forward_host(xh, oh, stream)
+        el = time.perf_counter() - t0
+        if world > 1:
+            tt = torch.tensor([el], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            el = float(tt.item())
+        e2e = {"value": world * T * k_e2e / el, "unit": UNIT,
+               "h2d_bytes_per_step": xh.numel() * xh.element_size(),
+               "d2h_bytes_per_step": oh.numel() * oh.element_size()}
+    clk = clocks.stop()
+    status = layer.device_status()
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    alg = algorithmic(shape, T, active)
+    peaks, peak_src = load_peaks()
+    mean_stage = stage_ms.mean(axis=0)
+    dominant = int(np.argmax(mean_stage))
+    dur = mean_stage[dominant] / 1e3
+    if shape.dtype == "bf16" and T >= 256 and dominant in (2, 3):
+        fl = alg["flops_up"] if dominant == 2 else alg["flops_down"]
+        ach = fl / dur / 1e12
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        roof = {"bound": "tensor", "kernel": STAGES[dominant], "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": None, "peak_source": f"{peak_src} bf16 burst"}
+    else:
+        # weight streaming: bytes of the distinct active experts' weights this stage reads
+        n_up = 2 if shape.act == 1 else 1
+        es = 2 if shape.dtype == "bf16" else 4
+        byts = {2: active * n_up * shape.d_model * shape.d_ff * es,
+                3: active * shape.d_model * shape.d_ff * es}.get(dominant, alg["bytes"])
+        ach = byts / dur / 1e9
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        roof = {"bound": "hbm", "kernel": STAGES[dominant], "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": ach / peak, "traffic": None, "peak_source": f"{peak_src} copy"}
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        li32 = li if li.x_f32 is not None and (li.w1_f32 and li.w1_f32[0] is not None) else \
+            testgen.make_inputs(shape.with_T(T), want_bits=False)
+        rate, n, wall, used = oracle_rate(li32, T, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": used, "kind": "oracle",
+               "sample": f"{n} random tokens of the {T}-token batch: fp64 routing + both experts, {wall:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": shape.dtype, "data": "synthetic",
+        "config": {"workload": workload_desc(shape, T), "tokens_per_step_per_gpu": T,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2: {alg['bytes'] / 1e9:.2f} GB of weights and activations per step",
+                   "active_experts": active},
+        "tflops": alg["flops"] / (ms_per_step / 1e3) / 1e12,
+        "roofline": roof,
+        "stages_us": {n: float(v * 1e3) for n, v in zip(STAGES, mean_stage)},
+        "e2e": e2e,
+        "gpu_launches": args.steps * n_st,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
