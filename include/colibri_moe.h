@@ -145,6 +145,26 @@ COLIBRI_API int colibri_moe_set_stage_events(colibri_moe_t* ctx, void* const* ev
  * gives up or an index check fails: *status = 0 means none did. */
 COLIBRI_API int colibri_moe_device_status(colibri_moe_t* ctx, int32_t* status);
 
+/* Routing without any allocation (no counterpart in the articles: an addition for callers that
+ * cannot allocate device memory -- code that runs inside a host framework whose memory pool owns
+ * the whole GPU, real-time loops where cudaMalloc's implicit synchronisation is not allowed, or
+ * deployments with a fixed device-memory budget set at start-up).  It computes, from device
+ * buffers on the CURRENT device, exactly what colibri_moe_get_routing reports after a forward of
+ * the same x and router weights: idx[T,2], gate[T,2], counts[E], offsets[E+1], row_of[T,2].
+ *   x [T, d_model] and w_router [E, d_model] in `dtype` (16-byte aligned), b_router [E] fp32 or NULL.
+ * It needs no context.  Its scratch (per-chunk histograms and the routing summary) is a fixed
+ * __device__ array of about 129 KB inside the library, present on every GPU that loads the library
+ * until the process exits; hence T <= 65536 (larger T returns COLIBRI_ERR_INVALID_ARG).  The first
+ * call on a device looks up the array's device address and sets kernel attributes (host-side
+ * set-up, no allocation); make that first call before any stream capture.  Every call on a device
+ * shares the one array, and each call clears the part that must start at zero: calls that overlap
+ * on the GPU (different streams, or concurrent host threads) race and give wrong results.
+ * Asynchronous on `stream`; it calls no cudaMalloc, cudaFree or allocating library routine. */
+COLIBRI_API int colibri_moe_route_noalloc(const void* x, const void* w_router, const float* b_router, int32_t T,
+                                          int32_t d_model, int32_t num_experts, int32_t dtype, int32_t* idx,
+                                          float* gate, int32_t* counts, int32_t* offsets, int32_t* row_of,
+                                          void* stream);
+
 /* Frees everything the context owns.  NULL-safe. */
 COLIBRI_API void colibri_moe_destroy(colibri_moe_t* ctx);
 

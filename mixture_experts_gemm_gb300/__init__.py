@@ -30,8 +30,8 @@ _ACTS = {"relu_bias": ACT_RELU_BIAS, "relu": ACT_RELU_BIAS, "swiglu": ACT_SWIGLU
 # every function include/colibri_moe.h declares
 EXPORTED = ("colibri_moe_create", "colibri_moe_load_weights", "colibri_moe_forward", "colibri_moe_forward_host",
             "colibri_moe_get_routing", "colibri_moe_debug_buffer", "colibri_moe_num_stages",
-            "colibri_moe_set_stage_events", "colibri_moe_device_status", "colibri_moe_destroy",
-            "colibri_moe_strerror")
+            "colibri_moe_set_stage_events", "colibri_moe_device_status", "colibri_moe_route_noalloc",
+            "colibri_moe_destroy", "colibri_moe_strerror")
 
 
 class ColibriError(RuntimeError):
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
             "colibri_moe_num_stages": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
             "colibri_moe_set_stage_events": ([vp, vp, i32], ctypes.c_int),
             "colibri_moe_device_status": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
+            "colibri_moe_route_noalloc": ([vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp], ctypes.c_int),
             "colibri_moe_destroy": ([vp], None),
             "colibri_moe_strerror": ([ctypes.c_int], ctypes.c_char_p),
         }
