@@ -79,6 +79,22 @@ def algorithmic(s, T, active_experts=None):
                 w_bytes_up=n_act * n_up * s.d_model * s.d_ff * es, w_bytes_expert=w_bytes_expert)
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank number over all ranks (the job takes as long as its slowest replica)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, tokens_per_rank_step: int, steps: int, seconds: float) -> float:
+    """Tokens/s of the whole job: every replica processes its own batch each step (weak scaling)."""
+    return world * tokens_per_rank_step * steps / seconds
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -262,14 +278,10 @@ def main():
     torch.cuda.synchronize(dev)
     barrier()
     lib.colibri_moe_set_stage_events(layer._h, None, 0)
-    ms_total = t_start.elapsed_time(t_end)
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     stage_ms = np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(n_st)] for evs in ev_sets])
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
     ms_per_step = ms_total / args.steps
-    value = world * T * args.steps / (ms_total / 1e3)
+    value = whole_job_rate(world, T, args.steps, ms_total / 1e3)
 
     # end to end through the C ABI with host buffers (pinned): H2D of x, forward, D2H of out
     e2e = None
@@ -287,12 +299,8 @@ def main():
         t0 = time.perf_counter()
         for _ in range(k_e2e):
             layer.forward_host(xh, oh, stream)
-        el = time.perf_counter() - t0
-        if world > 1:
-            tt = torch.tensor([el], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            el = float(tt.item())
-        e2e = {"value": world * T * k_e2e / el, "unit": UNIT,
+        el = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e = {"value": whole_job_rate(world, T, k_e2e, el), "unit": UNIT,
                "h2d_bytes_per_step": xh.numel() * xh.element_size(),
                "d2h_bytes_per_step": oh.numel() * oh.element_size()}
     clk = clocks.stop()
