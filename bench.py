@@ -253,17 +253,32 @@ def main():
     counts = routing["counts"].cpu().numpy()
     active = int((counts > 0).sum())
 
-    # per-step stage events, created before the timed region
-    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)] for _ in range(args.steps)]
-    arrs = []
-    for evs in ev_sets:
-        for e in evs:
-            e.record(stream)
-        import ctypes
-        arrs.append((ctypes.c_void_p * (n_st + 1))(*[e.cuda_event for e in evs]))
-    torch.cuda.synchronize(dev)
-    lib = moe.lib()
     import ctypes
+    lib = moe.lib()
+
+    def event_array(evs):
+        for e in evs:
+            if e is not None:
+                e.record(stream)  # makes torch create the underlying cudaEvent_t
+        return (ctypes.c_void_p * (n_st + 1))(*[None if e is None else e.cuda_event for e in evs])
+
+    # 1) stage breakdown: a short pass with an event at every stage boundary
+    n_prof = min(args.steps, 50)
+    prof_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)] for _ in range(n_prof)]
+    prof_arrs = [event_array(evs) for evs in prof_sets]
+    torch.cuda.synchronize(dev)
+    for k in range(n_prof):
+        lib.colibri_moe_set_stage_events(layer._h, ctypes.cast(prof_arrs[k], ctypes.c_void_p), n_st + 1)
+        layer.forward_ptr(x.data_ptr(), out.data_ptr(), T, sh)
+    torch.cuda.synchronize(dev)
+    stage_ms = np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(n_st)] for evs in prof_sets])
+    dominant = int(np.argmax(stage_ms.mean(axis=0)))
+
+    # 2) the timed region: K back-to-back forwards; events only around the dominant kernel
+    dom_sets = [[torch.cuda.Event(enable_timing=True) if i in (dominant, dominant + 1) else None
+                 for i in range(n_st + 1)] for _ in range(args.steps)]
+    dom_arrs = [event_array(evs) for evs in dom_sets]
+    torch.cuda.synchronize(dev)
 
     clocks = ClockSampler(local)
     t_start = torch.cuda.Event(enable_timing=True)
@@ -272,14 +287,14 @@ def main():
     torch.cuda.synchronize(dev)
     t_start.record(stream)
     for k in range(args.steps):
-        lib.colibri_moe_set_stage_events(layer._h, ctypes.cast(arrs[k], ctypes.c_void_p), n_st + 1)
+        lib.colibri_moe_set_stage_events(layer._h, ctypes.cast(dom_arrs[k], ctypes.c_void_p), n_st + 1)
         layer.forward_ptr(x.data_ptr(), out.data_ptr(), T, sh)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     lib.colibri_moe_set_stage_events(layer._h, None, 0)
     ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
-    stage_ms = np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(n_st)] for evs in ev_sets])
+    dom_ms = np.array([evs[dominant].elapsed_time(evs[dominant + 1]) for evs in dom_sets])
     ms_per_step = ms_total / args.steps
     value = whole_job_rate(world, T, args.steps, ms_total / 1e3)
 
@@ -314,8 +329,7 @@ def main():
     alg = algorithmic(shape, T, active)
     peaks, peak_src = load_peaks()
     mean_stage = stage_ms.mean(axis=0)
-    dominant = int(np.argmax(mean_stage))
-    dur = mean_stage[dominant] / 1e3
+    dur = float(dom_ms.mean()) / 1e3  # live, inside the timed region
     if shape.dtype == "bf16" and T >= 256 and dominant in (2, 3):
         fl = alg["flops_up"] if dominant == 2 else alg["flops_down"]
         ach = fl / dur / 1e12
@@ -352,6 +366,7 @@ def main():
         "tflops": alg["flops"] / (ms_per_step / 1e3) / 1e12,
         "roofline": roof,
         "stages_us": {n: float(v * 1e3) for n, v in zip(STAGES, mean_stage)},
+        "stages_note": "stage split from a separate 50-step pass with an event at every stage boundary",
         "e2e": e2e,
         "gpu_launches": args.steps * n_st,
         "clocks": clk,

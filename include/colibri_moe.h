@@ -137,7 +137,8 @@ COLIBRI_API int colibri_moe_debug_buffer(colibri_moe_t* ctx, int32_t which, void
 COLIBRI_API int colibri_moe_num_stages(const colibri_moe_t* ctx, int32_t* n_stages);
 
 /* Stage timing: with n == num_stages + 1 cudaEvent_t values (passed as void*), every later forward
- * records events[i] just before stage i and events[n-1] after the last stage, on its stream.
+ * records events[i] just before stage i and events[n-1] after the last stage, on its stream; NULL
+ * entries are skipped (record only the boundaries you need: each record sits between two kernels).
  * events == NULL (n == 0) turns it off.  The caller owns the events. */
 COLIBRI_API int colibri_moe_set_stage_events(colibri_moe_t* ctx, void* const* events, int32_t n);
 

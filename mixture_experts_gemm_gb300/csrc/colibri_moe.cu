@@ -6,6 +6,7 @@
 // forward path; m.nxbn.cn/news/48047 3.1: the maximum batch is fixed at initialisation).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -15,6 +16,17 @@
 #include "moe_internal.cuh"
 
 using namespace colibri;
+
+namespace colibri {
+// Programmatic dependent launch between the forward's kernels; COLIBRI_MOE_PDL=0 turns it off.
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* s = std::getenv("COLIBRI_MOE_PDL");
+    return !(s && s[0] == '0');
+  }();
+  return on;
+}
+}  // namespace colibri
 
 struct colibri_moe {
   colibri_moe_config_t cfg{};
@@ -55,6 +67,10 @@ struct colibri_moe {
   void* out_stage = nullptr;
 
   CUtensorMap tm_xp{}, tm_h{}, tm_w13{}, tm_w2{};
+  // decode path (T <= decode_max_t): 128-row weight boxes, token boxes of 16/32/48/64 rows
+  CUtensorMap tm_w13_dec{}, tm_w2_dec{}, tm_xp_dec[4]{}, tm_h_dec[4]{};
+  float* partial = nullptr;  // decode partial sums [splits][n_pad][E * rows]
+  int decode_max_t = 0;
   int32_t last_T = -1;
   std::vector<cudaEvent_t> events;
   uint64_t timeout_ns = 2000000000ull;
@@ -140,6 +156,15 @@ int check_config(const colibri_moe_config_t* c) {
   return COLIBRI_OK;
 }
 
+int env_decode_max_t() {
+  const char* s = std::getenv("COLIBRI_MOE_DECODE_MAX_T");
+  if (s) {
+    long v = std::strtol(s, nullptr, 10);
+    if (v >= 0 && v <= kDecodeMaxT) return static_cast<int>(v);
+  }
+  return kDecodeMaxT;
+}
+
 uint64_t env_timeout_ns() {
   const char* s = std::getenv("COLIBRI_MOE_WAIT_TIMEOUT_MS");
   if (s) {
@@ -213,7 +238,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
     // W_r columns staged per router pass: at most 96 KB of shared memory
     const int vec_span = 32 * (16 / static_cast<int>(c->esize));
     const int emax = E <= 4 ? 4 : (E <= 8 ? 8 : 16);
-    int dc = (96 * 1024) / (emax * static_cast<int>(c->esize));
+    int dc = kRouterMaxSmem / (emax * static_cast<int>(c->esize));
     dc = dc / vec_span * vec_span;
     c->dchunk = static_cast<int>(d) < dc ? static_cast<int>(d) : dc;
   }
@@ -233,6 +258,15 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   const size_t o_tok = carve(c->rows_alloc * 4);
   const size_t o_hist = carve(static_cast<size_t>(c->nchunks_max) * E * 4);
   const size_t o_sched = carve(sizeof(Sched));
+  // decode partial sums: bf16 layers whose batches can be decode-sized
+  c->decode_max_t = cfg->dtype == COLIBRI_DTYPE_BF16 ? env_decode_max_t() : 0;
+  if (c->decode_max_t > T) c->decode_max_t = static_cast<int>(T);
+  const int64_t npad_max = (c->decode_max_t + 15) / 16 * 16;
+  const int64_t part_floats = c->decode_max_t > 0
+                                  ? std::max<int64_t>(kDecodeSplitsUp * npad_max * E * c->n_up,
+                                                      kDecodeSplitsDown * npad_max * E * d)
+                                  : 0;
+  const size_t o_part = carve(part_floats * 4);
   const size_t o_xs = carve(T * d * c->esize);
   const size_t o_os = carve(T * d * c->out_esize);
   c->ws_bytes = off;
@@ -251,6 +285,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   c->tok_of_row = reinterpret_cast<int32_t*>(b + o_tok);
   c->hist = reinterpret_cast<int32_t*>(b + o_hist);
   c->sched = reinterpret_cast<Sched*>(b + o_sched);
+  c->partial = part_floats > 0 ? reinterpret_cast<float*>(b + o_part) : nullptr;
   c->x_stage = b + o_xs;
   c->out_stage = b + o_os;
   if (cudaMemset(c->ws, 0, c->ws_bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
@@ -258,9 +293,19 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
     colibri_moe_destroy(c);
     return COLIBRI_ERR_CUDA;
   }
+  if (prepare_router(cfg->dtype, cfg->num_experts) != cudaSuccess ||
+      (cfg->dtype == COLIBRI_DTYPE_BF16 && (prepare_tc_gemm() != cudaSuccess || prepare_decode_gemm() != cudaSuccess))) {
+    cudaGetLastError();
+    colibri_moe_destroy(c);
+    return COLIBRI_ERR_CUDA;
+  }
   if (cfg->dtype == COLIBRI_DTYPE_BF16) {
-    if (!make_tmap(&c->tm_xp, c->xp, d, c->rows_alloc, kRowTile) ||
-        !make_tmap(&c->tm_h, c->h, f, c->rows_alloc, kRowTile)) {
+    bool ok = make_tmap(&c->tm_xp, c->xp, d, c->rows_alloc, kRowTile) &&
+              make_tmap(&c->tm_h, c->h, f, c->rows_alloc, kRowTile);
+    for (int i = 0; ok && i < 4; ++i)
+      ok = make_tmap(&c->tm_xp_dec[i], c->xp, d, c->rows_alloc, 16 * (i + 1)) &&
+           make_tmap(&c->tm_h_dec[i], c->h, f, c->rows_alloc, 16 * (i + 1));
+    if (!ok) {
       colibri_moe_destroy(c);
       return COLIBRI_ERR_CUDA;
     }
@@ -354,7 +399,9 @@ int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_weights_t* w,
   if (c.dtype == COLIBRI_DTYPE_BF16) {
     const int bn = tc_gemm_block_n();
     if (!make_tmap(&ctx->tm_w13, ctx->w13, d, static_cast<uint64_t>(E) * ctx->n_up, bn) ||
-        !make_tmap(&ctx->tm_w2, ctx->w2, f, static_cast<uint64_t>(E) * d, bn))
+        !make_tmap(&ctx->tm_w2, ctx->w2, f, static_cast<uint64_t>(E) * d, bn) ||
+        !make_tmap(&ctx->tm_w13_dec, ctx->w13, d, static_cast<uint64_t>(E) * ctx->n_up, kRowTile) ||
+        !make_tmap(&ctx->tm_w2_dec, ctx->w2, f, static_cast<uint64_t>(E) * d, kRowTile))
       return COLIBRI_ERR_CUDA;
   }
   ctx->loaded = true;
@@ -368,7 +415,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   const bool swiglu = c.act == COLIBRI_ACT_SWIGLU;
   const bool timed = static_cast<int>(ctx->events.size()) == kNumStages + 1;
   auto mark = [&](int i) {
-    if (timed) cudaEventRecord(ctx->events[i], s);
+    if (timed && ctx->events[i]) cudaEventRecord(ctx->events[i], s);
   };
   const int nchunks = (T + kRouterChunk - 1) / kRouterChunk;
   int64_t max_mtiles = (2 * static_cast<int64_t>(T) + (kRowTile - 1) * E) / kRowTile;
@@ -382,6 +429,30 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   GatherArgs ga{x, ctx->idx, ctx->row_of, ctx->hist, T, d, E, ctx->rows_alloc, ctx->xp, ctx->tok_of_row, ctx->sched};
   if (launch_gather(c.dtype, ga, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   mark(2);
+  if (bf16 && T <= ctx->decode_max_t) {
+    // decode-sized batch: weight-streaming GEMMs with K splits, deterministic reductions
+    const int n_pad = (T + 15) / 16 * 16;
+    const int mi = n_pad / 16 - 1;
+    DecodeArgs up{ctx->sched, E, d, ctx->n_up, n_pad, kDecodeSplitsUp, ctx->num_sms, ctx->partial,
+                  ctx->timeout_ns, &ctx->sched->status};
+    if (launch_decode_gemm(ctx->tm_w13_dec, ctx->tm_xp_dec[mi], up, ctx->num_sms, s) != cudaSuccess)
+      return COLIBRI_ERR_CUDA;
+    DecodeActArgs act{ctx->sched, E, d, ctx->n_up, n_pad, kDecodeSplitsUp, ctx->num_sms, f, ctx->partial, ctx->b1,
+                      ctx->h};
+    if (launch_decode_act(swiglu, act, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+    mark(3);
+    DecodeArgs dn{ctx->sched, E, f, d, n_pad, kDecodeSplitsDown, ctx->num_sms, ctx->partial, ctx->timeout_ns,
+                  &ctx->sched->status};
+    if (launch_decode_gemm(ctx->tm_w2_dec, ctx->tm_h_dec[mi], dn, ctx->num_sms, s) != cudaSuccess)
+      return COLIBRI_ERR_CUDA;
+    mark(4);
+    DecodeCombineArgs cb{ctx->sched, E, f, n_pad, kDecodeSplitsDown, ctx->num_sms, d, T, ctx->partial, ctx->b2,
+                         ctx->idx, ctx->row_of, ctx->gate, out};
+    if (launch_decode_combine(c.out_dtype, cb, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+    mark(5);
+    ctx->last_T = T;
+    return COLIBRI_OK;
+  }
   if (bf16) {
     const int bn = tc_gemm_block_n();
     GemmArgs up{ctx->sched, E, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns,
@@ -515,8 +586,6 @@ int colibri_moe_set_stage_events(colibri_moe_t* ctx, void* const* events, int32_
     return COLIBRI_OK;
   }
   if (n != kNumStages + 1) return COLIBRI_ERR_INVALID_ARG;
-  for (int i = 0; i < n; ++i)
-    if (!events[i]) return COLIBRI_ERR_INVALID_ARG;
   ctx->events.assign(reinterpret_cast<cudaEvent_t const*>(events), reinterpret_cast<cudaEvent_t const*>(events) + n);
   return COLIBRI_OK;
 }

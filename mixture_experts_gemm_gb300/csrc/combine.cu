@@ -17,6 +17,8 @@ constexpr int kCombineThreads = 256;
 template <bool kBf16Out>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a) {
   const int nvec = a.d / 4;
+  pdl_trigger();
+  pdl_wait();
   for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
     const int r0 = a.row_of[2 * (size_t)t], r1 = a.row_of[2 * (size_t)t + 1];
     const float g0 = a.gate[2 * (size_t)t], g1 = a.gate[2 * (size_t)t + 1];
@@ -46,11 +48,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
 
 cudaError_t launch_combine(int out_dtype, const CombineArgs& a, int num_sms, cudaStream_t s) {
   const int grid = a.T < num_sms * 8 ? a.T : num_sms * 8;
-  if (out_dtype == 0)
-    combine_kernel<false><<<grid, kCombineThreads, 0, s>>>(a);
-  else
-    combine_kernel<true><<<grid, kCombineThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  if (out_dtype == 0) return pdl_launch(combine_kernel<false>, dim3(grid), dim3(kCombineThreads), 0, s, a);
+  return pdl_launch(combine_kernel<true>, dim3(grid), dim3(kCombineThreads), 0, s, a);
 }
 
 }  // namespace colibri

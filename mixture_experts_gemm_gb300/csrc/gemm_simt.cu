@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
   const Sched* sc = a.sched;
   const int n_tiles = (a.N + SBN - 1) / SBN;
   const int tile = blockIdx.x;
+  pdl_trigger();
+  pdl_wait();
   if (tile >= sc->mtile_start[a.E] * n_tiles) return;
   int e = 0;
   while (e + 1 < a.E && sc->mtile_start[e + 1] * n_tiles <= tile) ++e;
@@ -105,11 +107,10 @@ cudaError_t launch_simt_gemm(int epi, const SimtGemmArgs& a, int max_mtiles, cud
   const int grid = max_mtiles * n_tiles;
   if (grid <= 0) return cudaSuccess;
   switch (epi) {
-    case kEpiSwiGLU: simt_gemm_kernel<kEpiSwiGLU><<<grid, 256, 0, s>>>(a); break;
-    case kEpiReluBias: simt_gemm_kernel<kEpiReluBias><<<grid, 256, 0, s>>>(a); break;
-    default: simt_gemm_kernel<kEpiStoreF32><<<grid, 256, 0, s>>>(a); break;
+    case kEpiSwiGLU: return pdl_launch(simt_gemm_kernel<kEpiSwiGLU>, dim3(grid), dim3(256), 0, s, a);
+    case kEpiReluBias: return pdl_launch(simt_gemm_kernel<kEpiReluBias>, dim3(grid), dim3(256), 0, s, a);
+    default: return pdl_launch(simt_gemm_kernel<kEpiStoreF32>, dim3(grid), dim3(256), 0, s, a);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace colibri

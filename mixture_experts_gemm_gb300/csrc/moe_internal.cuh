@@ -6,12 +6,18 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace colibri {
 
 constexpr int kMaxE = 16;            // experts per layer (upper bound)
 constexpr int kRowTile = 128;        // expert row segments start on multiples of this (GEMM M tile)
 constexpr int kRouterChunk = 32;     // tokens per router CTA (4 per warp)
 constexpr int kRouterThreads = 256;
+constexpr int kRouterMaxSmem = 96 * 1024;  // W_r columns staged per router pass (dynamic smem)
+constexpr int kDecodeMaxT = 64;            // batches up to this many tokens take the decode path
+constexpr int kDecodeSplitsUp = 2;         // most K splits of the decode up projection
+constexpr int kDecodeSplitsDown = 8;       // most K splits of the decode down projection
 
 // Device status word bits (sticky until read by colibri_moe_device_status).
 enum : int32_t {
@@ -84,6 +90,41 @@ struct GemmArgs {
   int32_t* status;          // device status word (Sched::status)
 };
 
+// Decode (weight-streaming) GEMM: P[s][tok][row] partial sums over K split s.
+struct DecodeArgs {
+  const Sched* sched;
+  int E;
+  int K;                    // reduction length
+  int n_per_expert;         // weight rows per expert (multiple of 128)
+  int n_pad;                // token columns (16, 32, 48 or 64), >= every expert's count
+  int s_max;                // most K splits
+  int grid_ref;             // CTA count the split choice is computed for (same in every kernel)
+  float* partial;           // [s_max][n_pad][E * n_per_expert] fp32
+  uint64_t timeout_ns;
+  int32_t* status;
+};
+
+struct DecodeActArgs {
+  const Sched* sched;
+  int E, K, n_per_expert, n_pad, s_max, grid_ref;
+  int f;                    // H columns
+  const float* partial;
+  const float* bias;        // b1 [E, f] (ReLU) or nullptr
+  void* h;                  // H [rows, f] bf16
+};
+
+struct DecodeCombineArgs {
+  const Sched* sched;
+  int E, K, n_pad, s_max, grid_ref;
+  int d, T;
+  const float* partial;     // down-projection partials, rows = E * d
+  const float* bias;        // b2 [E, d] or nullptr
+  const int32_t* idx;
+  const int32_t* row_of;
+  const float* gate;
+  void* out;
+};
+
 // fp32 SIMT grouped GEMM operands (row-major, K contiguous)
 struct SimtGemmArgs {
   const Sched* sched;
@@ -95,6 +136,32 @@ struct SimtGemmArgs {
   float* out;               // [rows, N]
 };
 
+// Programmatic dependent launch: a kernel launched with pdl_launch may start (and run its prologue)
+// while the previous kernel on the stream drains; it must call pdl_wait() before touching anything
+// an earlier kernel wrote (pdl_wait returns once every prerequisite grid has completed and its
+// memory is visible; without the launch attribute it returns at once).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t pdl_launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // launchers (return cudaGetLastError() of the launch)
 cudaError_t launch_router(int dtype, const RouterArgs& a, int nchunks, cudaStream_t s);
 cudaError_t launch_gather(int dtype, const GatherArgs& a, cudaStream_t s);
@@ -103,6 +170,14 @@ cudaError_t launch_tc_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& t
                            int grid, cudaStream_t s);
 cudaError_t launch_simt_gemm(int epi, const SimtGemmArgs& a, int max_mtiles, cudaStream_t s);
 int router_smem_bytes(int dtype, int E, int dchunk);
+// One-time kernel attribute set-up (dynamic shared memory limits) for the current device.
+cudaError_t prepare_router(int dtype, int E);
+cudaError_t prepare_tc_gemm();
+cudaError_t prepare_decode_gemm();
+cudaError_t launch_decode_gemm(const CUtensorMap& tmW, const CUtensorMap& tmX, const DecodeArgs& a, int grid,
+                               cudaStream_t s);
+cudaError_t launch_decode_act(bool swiglu, const DecodeActArgs& a, cudaStream_t s);
+cudaError_t launch_decode_combine(int out_dtype, const DecodeCombineArgs& a, cudaStream_t s);
 int tc_gemm_block_n();
 int tc_gemm_threads();
 

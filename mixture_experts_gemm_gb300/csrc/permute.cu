@@ -16,9 +16,13 @@ namespace {
 constexpr int kGatherThreads = 256;
 
 template <int ESIZE>
-__global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherArgs a) {
+__global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherArgs a, int wpt) {
+  // wpt warps share one token row (small batches spread a row over several warps)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (kGatherThreads / 32) + warp;
+  const int gw = blockIdx.x * (kGatherThreads / 32) + warp;
+  const int t = gw / wpt, part = gw - t * wpt;
+  pdl_trigger();
+  pdl_wait();
   if (t >= a.T) return;
   const int chunk = t / kRouterChunk;
   int r[2];
@@ -29,7 +33,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherArgs a) {
   }
   const bool ok = r[0] >= 0 && r[0] < a.rows_alloc && r[1] >= 0 && r[1] < a.rows_alloc;
   __syncwarp();
-  if (lane == 0) {
+  if (lane == 0 && part == 0) {
     if (ok) {
       a.row_of[2 * (size_t)t] = r[0];
       a.row_of[2 * (size_t)t + 1] = r[1];
@@ -42,19 +46,20 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherArgs a) {
   if (!ok) return;
   const size_t row_bytes = (size_t)a.d * ESIZE;
   const int nvec = (int)(row_bytes / 16);
+  const int v0 = (nvec * part) / wpt, v1 = (nvec * (part + 1)) / wpt;
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(a.x) + (size_t)t * row_bytes);
   uint4* d0 = reinterpret_cast<uint4*>(static_cast<char*>(a.xp) + (size_t)r[0] * row_bytes);
   uint4* d1 = reinterpret_cast<uint4*>(static_cast<char*>(a.xp) + (size_t)r[1] * row_bytes);
-  int i = lane;
-  for (; i + 96 < nvec; i += 128) {
-    uint4 v0 = __ldg(src + i), v1 = __ldg(src + i + 32), v2 = __ldg(src + i + 64), v3 = __ldg(src + i + 96);
-    d0[i] = v0; d0[i + 32] = v1; d0[i + 64] = v2; d0[i + 96] = v3;
-    d1[i] = v0; d1[i + 32] = v1; d1[i + 64] = v2; d1[i + 96] = v3;
+  int i = v0 + lane;
+  for (; i + 96 < v1; i += 128) {
+    uint4 q0 = __ldg(src + i), q1 = __ldg(src + i + 32), q2 = __ldg(src + i + 64), q3 = __ldg(src + i + 96);
+    d0[i] = q0; d0[i + 32] = q1; d0[i + 64] = q2; d0[i + 96] = q3;
+    d1[i] = q0; d1[i + 32] = q1; d1[i + 64] = q2; d1[i + 96] = q3;
   }
-  for (; i < nvec; i += 32) {
-    uint4 v = __ldg(src + i);
-    d0[i] = v;
-    d1[i] = v;
+  for (; i < v1; i += 32) {
+    uint4 q = __ldg(src + i);
+    d0[i] = q;
+    d1[i] = q;
   }
 }
 
@@ -62,12 +67,10 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherArgs a) {
 
 cudaError_t launch_gather(int dtype, const GatherArgs& a, cudaStream_t s) {
   const int per = kGatherThreads / 32;
-  const int grid = (a.T + per - 1) / per;
-  if (dtype == 0)
-    gather_kernel<4><<<grid, kGatherThreads, 0, s>>>(a);
-  else
-    gather_kernel<2><<<grid, kGatherThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  const int wpt = a.T >= 1024 ? 1 : (a.T >= 256 ? 2 : (a.T >= 64 ? 4 : 8));
+  const int grid = (a.T * wpt + per - 1) / per;
+  if (dtype == 0) return pdl_launch(gather_kernel<4>, dim3(grid), dim3(kGatherThreads), 0, s, a, wpt);
+  return pdl_launch(gather_kernel<2>, dim3(grid), dim3(kGatherThreads), 0, s, a, wpt);
 }
 
 }  // namespace colibri

@@ -25,12 +25,15 @@ struct Vec<float> {
     float4 q = *reinterpret_cast<const float4*>(p);
     v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
   }
+  __device__ static void from_raw(const uint4& q, float (&v)[4]) {
+    v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y);
+    v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
+  }
 };
 template <>
 struct Vec<__nv_bfloat16> {
   static constexpr int N = 8;
-  __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
-    uint4 q = *reinterpret_cast<const uint4*>(p);
+  __device__ static void from_raw(const uint4& q, float (&v)[8]) {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -38,185 +41,91 @@ struct Vec<__nv_bfloat16> {
       v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
   }
+  __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
+    from_raw(*reinterpret_cast<const uint4*>(p), v);
+  }
 };
 
-template <typename Tin>
-__device__ __forceinline__ void load_global_vec(const Tin* p, float (&v)[Vec<Tin>::N]) {
-  Vec<Tin>::load(p, v);
-}
-
-// Block-wide exclusive scan of one int per thread (blockDim.x == kRouterThreads).  Returns the
-// exclusive prefix; *total receives the block sum.
-__device__ int block_exclusive_scan(int v, int* scratch /* >= 8 ints */, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int n = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += n;
-  }
-  if (lane == 31) scratch[warp] = inc;
-  __syncthreads();
-  int warp_prefix = 0, sum = 0;
-#pragma unroll
-  for (int w = 0; w < kRouterThreads / 32; ++w) {
-    int s = scratch[w];
-    if (w < warp) warp_prefix += s;
-    sum += s;
-  }
-  __syncthreads();
-  *total = sum;
-  return warp_prefix + inc - v;
-}
-
-// Runs in the last router CTA: counts, padded offsets, M-tile prefix, and first row of each
-// (chunk, expert) pair, written over the per-chunk counts.
+// Runs in the last router CTA: counts, padded offsets, M-tile prefix, and the first row of every
+// (chunk, expert) pair, written over the per-chunk counts.  All experts are scanned together (one
+// barrier), so the cost is a couple of memory round trips, not one per expert.
 __device__ void scan_offsets(const RouterArgs& a, int nchunks) {
-  __shared__ int s_scratch[8];
-  __shared__ int s_offsets[kMaxE + 1];
+  constexpr int NW = kRouterThreads / 32;
+  __shared__ int s_wsum[NW][kMaxE];
   const int E = a.E;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int per = (nchunks + kRouterThreads - 1) / kRouterThreads;
-  const int c0 = threadIdx.x * per;
-  const int c1 = min(c0 + per, nchunks);
-  int prefix[kMaxE];
+  const int c0 = min((int)threadIdx.x * per, nchunks), c1 = min(c0 + per, nchunks);
+  int local[kMaxE];
+#pragma unroll
+  for (int e = 0; e < kMaxE; ++e) local[e] = 0;
+  for (int c = c0; c < c1; ++c) {
+    int v[kMaxE];
+#pragma unroll
+    for (int e = 0; e < kMaxE; ++e) v[e] = e < E ? __ldcg(&a.hist[(size_t)c * E + e]) : 0;
+#pragma unroll
+    for (int e = 0; e < kMaxE; ++e) local[e] += v[e];
+  }
+  // inclusive warp scans of every expert's chunk counts, then warp totals through shared memory
+  int inc[kMaxE];
 #pragma unroll
   for (int e = 0; e < kMaxE; ++e) {
-    prefix[e] = 0;
-    if (e < E) {
-      int local = 0;
-      for (int c = c0; c < c1; ++c) local += __ldcg(&a.hist[c * E + e]);
-      int total;
-      prefix[e] = block_exclusive_scan(local, s_scratch, &total);
-      if (threadIdx.x == 0) a.sched->counts[e] = total;
+    inc[e] = local[e];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, inc[e], o);
+      if (lane >= o) inc[e] += n;
     }
   }
+  if (lane == 31) {
+#pragma unroll
+    for (int e = 0; e < kMaxE; ++e) s_wsum[warp][e] = inc[e];
+  }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int off = 0, mt = 0;
-    for (int e = 0; e < E; ++e) {
-      const int c = a.sched->counts[e];
-      s_offsets[e] = off;
-      a.sched->offsets[e] = off;
-      a.sched->mtile_start[e] = mt;
-      const int tiles = (c + kRowTile - 1) / kRowTile;
+  int off = 0, mt = 0;
+#pragma unroll
+  for (int e = 0; e < kMaxE; ++e) {
+    int pre = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const int v = s_wsum[w][e];
+      pre += w < warp ? v : 0;
+      tot += v;
+    }
+    if (e < E) {
+      if (threadIdx.x == 0) {
+        a.sched->counts[e] = tot;
+        a.sched->offsets[e] = off;
+        a.sched->mtile_start[e] = mt;
+      }
+      // first row of each of this thread's chunks for expert e, in chunk order
+      int run = off + pre + inc[e] - local[e];
+      if (c1 - c0 == 1) {
+        a.hist[(size_t)c0 * E + e] = run;
+      } else {
+        for (int c = c0; c < c1; ++c) {
+          const int n = __ldcg(&a.hist[(size_t)c * E + e]);
+          a.hist[(size_t)c * E + e] = run;
+          run += n;
+        }
+      }
+      const int tiles = (tot + kRowTile - 1) / kRowTile;
       off += tiles * kRowTile;
       mt += tiles;
     }
-    s_offsets[E] = off;
+  }
+  if (threadIdx.x == 0) {
     a.sched->offsets[E] = off;
     a.sched->mtile_start[E] = mt;
     a.sched->ticket = 0;  // ready for the next forward
   }
-  __syncthreads();
-#pragma unroll
-  for (int e = 0; e < kMaxE; ++e) {
-    if (e < E) {
-      int run = s_offsets[e] + prefix[e];
-      for (int c = c0; c < c1; ++c) {
-        const int n = __ldcg(&a.hist[c * E + e]);
-        a.hist[c * E + e] = run;
-        run += n;
-      }
-    }
-  }
 }
 
-template <typename Tin, int EMAX>
-__global__ void __launch_bounds__(kRouterThreads) router_top2_kernel(RouterArgs a) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  constexpr int VEC = Vec<Tin>::N;
-  Tin* wsm = reinterpret_cast<Tin*>(smem_raw);
-  __shared__ int s_idx[kRouterChunk][2];
+// After the chunk's top-2 is in s_idx (a __syncthreads() ago): in-chunk ranks, the chunk's expert
+// histogram, and -- in the CTA that finishes last -- the scan of all histograms.
+__device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[2], int valid, int chunk_t0) {
   __shared__ int s_last;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int chunk_t0 = blockIdx.x * kRouterChunk;
-  const int t0 = chunk_t0 + warp * 4;
-  const int T = a.T, d = a.d, E = a.E;
-  const Tin* __restrict__ x = static_cast<const Tin*>(a.x);
-  const Tin* __restrict__ w = static_cast<const Tin*>(a.w_router);
-
-  float acc[4][EMAX];
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-#pragma unroll
-    for (int e = 0; e < EMAX; ++e) acc[k][e] = 0.f;
-
-  for (int d0 = 0; d0 < d; d0 += a.dchunk) {
-    const int dc = min(a.dchunk, d - d0);
-    __syncthreads();
-    const int nvec = dc / VEC;
-    for (int i = threadIdx.x; i < E * nvec; i += kRouterThreads) {
-      const int e = i / nvec, jv = i - e * nvec;
-      *reinterpret_cast<uint4*>(wsm + (size_t)e * a.dchunk + jv * VEC) =
-          *reinterpret_cast<const uint4*>(w + (size_t)e * d + d0 + jv * VEC);
-    }
-    __syncthreads();
-    for (int j = lane * VEC; j < dc; j += 32 * VEC) {
-      float xv[4][VEC];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (t0 + k < T) {
-          load_global_vec<Tin>(x + (size_t)(t0 + k) * d + d0 + j, xv[k]);
-        } else {
-#pragma unroll
-          for (int v = 0; v < VEC; ++v) xv[k][v] = 0.f;
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < EMAX; ++e) {
-        if (e < E) {
-          float wv[VEC];
-          Vec<Tin>::load(wsm + (size_t)e * a.dchunk + j, wv);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) acc[k][e] = fmaf(xv[k][v], wv[v], acc[k][e]);
-        }
-      }
-    }
-  }
-
-  // warp all-reduce: every lane ends with the full dot products
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-#pragma unroll
-    for (int e = 0; e < EMAX; ++e)
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc[k][e] += __shfl_xor_sync(0xffffffffu, acc[k][e], o);
-
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    if (lane == k) {
-      const int t = t0 + k;
-      float L[EMAX];
-#pragma unroll
-      for (int e = 0; e < EMAX; ++e) L[e] = acc[k][e] + ((a.b_router != nullptr && e < E) ? a.b_router[e] : 0.f);
-      // first: highest logit, lowest index on ties (strict > keeps the earlier index)
-      int ia = 0;
-      float la = L[0];
-#pragma unroll
-      for (int e = 1; e < EMAX; ++e)
-        if (e < E && L[e] > la) { la = L[e]; ia = e; }
-      int ib = -1;
-      float lb = 0.f;
-#pragma unroll
-      for (int e = 0; e < EMAX; ++e)
-        if (e < E && e != ia && (ib < 0 || L[e] > lb)) { lb = L[e]; ib = e; }
-      s_idx[warp * 4 + k][0] = ia;
-      s_idx[warp * 4 + k][1] = ib;
-      if (t < T) {
-        const float ga = 1.0f / (1.0f + expf(lb - la));
-        a.idx[2 * (size_t)t] = ia;
-        a.idx[2 * (size_t)t + 1] = ib;
-        a.gate[2 * (size_t)t] = ga;
-        a.gate[2 * (size_t)t + 1] = 1.0f - ga;
-      }
-    }
-  }
-  __syncthreads();
-
-  const int valid = min(kRouterChunk, T - chunk_t0);
+  const int E = a.E;
   if (threadIdx.x < 2 * kRouterChunk) {
     const int tt = threadIdx.x >> 1, s = threadIdx.x & 1;
     if (tt < valid) {
@@ -241,19 +150,277 @@ __global__ void __launch_bounds__(kRouterThreads) router_top2_kernel(RouterArgs 
   }
 }
 
+// Top-2 of one token's logits (strict > keeps the lower index on ties) and its pair-softmax gates.
+template <int EMAX>
+__device__ __forceinline__ void top2_store(const RouterArgs& a, const float (&L)[EMAX], int t, int (&sidx)[2]) {
+  const int E = a.E;
+  int ia = 0;
+  float la = L[0];
+#pragma unroll
+  for (int e = 1; e < EMAX; ++e)
+    if (e < E && L[e] > la) { la = L[e]; ia = e; }
+  int ib = -1;
+  float lb = 0.f;
+#pragma unroll
+  for (int e = 0; e < EMAX; ++e)
+    if (e < E && e != ia && (ib < 0 || L[e] > lb)) { lb = L[e]; ib = e; }
+  sidx[0] = ia;
+  sidx[1] = ib;
+  if (t < a.T) {
+    const float ga = 1.0f / (1.0f + expf(lb - la));
+    a.idx[2 * (size_t)t] = ia;
+    a.idx[2 * (size_t)t + 1] = ib;
+    a.gate[2 * (size_t)t] = ga;
+    a.gate[2 * (size_t)t + 1] = 1.0f - ga;
+  }
+}
+
+// fp32 layers: FMA dot products with W_r staged in shared memory.
+template <typename Tin, int EMAX>
+__global__ void __launch_bounds__(kRouterThreads) router_top2_kernel(RouterArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  constexpr int VEC = Vec<Tin>::N;
+  constexpr int SPAN = 32 * VEC;                // columns one warp covers per iteration
+  constexpr int NW = kRouterThreads / 32;       // warps per CTA
+  Tin* wsm = reinterpret_cast<Tin*>(smem_raw);
+  __shared__ int s_idx[kRouterChunk][2];
+  __shared__ float s_part[NW][4][EMAX];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk_t0 = blockIdx.x * kRouterChunk;
+  const int T = a.T, d = a.d, E = a.E;
+  const int valid = min(kRouterChunk, T - chunk_t0);
+  // Warps = G token groups (4 tokens each, the groups this chunk needs, rounded up to a power of
+  // two) x S slices of the hidden dimension.  A full chunk gives G = 8, S = 1; a lone token gives
+  // G = 1 and all 8 warps share its row, so small batches are not one warp's serial latency.
+  const int need = (valid + 3) >> 2;
+  const int G = need <= 1 ? 1 : (need <= 2 ? 2 : (need <= 4 ? 4 : 8));
+  const int S = NW / G;
+  const int g = warp % G, sl = warp / G;
+  const int t0 = chunk_t0 + g * 4;
+  const Tin* __restrict__ x = static_cast<const Tin*>(a.x);
+  const Tin* __restrict__ w = static_cast<const Tin*>(a.w_router);
+  pdl_trigger();
+  pdl_wait();  // x may come from the previous kernel; the workspace from the previous forward
+
+  float acc[4][EMAX];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) acc[k][e] = 0.f;
+
+  for (int d0 = 0; d0 < d; d0 += a.dchunk) {
+    const int dc = min(a.dchunk, d - d0);
+    __syncthreads();
+    // stage W_r[:, d0 : d0 + dc]: eight independent 16-byte loads in flight per thread
+    const int nvec = dc / VEC, total = E * nvec;
+    for (int base = threadIdx.x; base < total; base += kRouterThreads * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * kRouterThreads;
+        if (i < total) {
+          const int e = i / nvec, jv = i - e * nvec;
+          v[u] = __ldg(reinterpret_cast<const uint4*>(w + (size_t)e * d + d0 + jv * VEC));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * kRouterThreads;
+        if (i < total) {
+          const int e = i / nvec, jv = i - e * nvec;
+          *reinterpret_cast<uint4*>(wsm + (size_t)e * a.dchunk + jv * VEC) = v[u];
+        }
+      }
+    }
+    __syncthreads();
+    const int n_it = (dc + SPAN - 1) / SPAN;
+    const int it0 = (n_it * sl) / S, it1 = (n_it * (sl + 1)) / S;
+    for (int it = it0; it < it1; it += 2) {
+      // both iterations' token vectors are requested before any is used
+      uint4 xr[2][4];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int j = (it + u) * SPAN + lane * VEC;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          xr[u][k] = make_uint4(0u, 0u, 0u, 0u);
+          if (it + u < it1 && j < dc && t0 + k < T)
+            xr[u][k] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + k) * d + d0 + j));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int j = (it + u) * SPAN + lane * VEC;
+        if (it + u < it1 && j < dc) {
+          float xv[4][VEC];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) Vec<Tin>::from_raw(xr[u][k], xv[k]);
+#pragma unroll
+          for (int e = 0; e < EMAX; ++e) {
+            if (e < E) {
+              float wv[VEC];
+              Vec<Tin>::load(wsm + (size_t)e * a.dchunk + j, wv);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) acc[k][e] = fmaf(xv[k][v], wv[v], acc[k][e]);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // warp all-reduce, then the S slices of each token group summed in slice order via shared memory
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[k][e] += __shfl_xor_sync(0xffffffffu, acc[k][e], o);
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) s_part[warp][k][e] = acc[k][e];
+  }
+  __syncthreads();
+
+  if (sl == 0 && lane < 4) {
+    const int k = lane;
+    const int t = t0 + k;
+    float L[EMAX];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+      float v = s_part[g][k][e];
+      for (int q = 1; q < S; ++q) v += s_part[g + q * G][k][e];
+      L[e] = v + ((a.b_router != nullptr && e < E) ? a.b_router[e] : 0.f);
+    }
+    top2_store<EMAX>(a, L, t, s_idx[g * 4 + k]);
+  }
+  __syncthreads();
+  finish_chunk(a, s_idx, valid, chunk_t0);
+}
+
+
+// bf16 layers: the logits GEMM on tensor cores with mma.sync m16n8k16 (bf16 x bf16 -> fp32).  Each
+// warp owns 16 tokens x (8 * NT) experts over one slice of the hidden dimension; A fragments come
+// straight from x in global memory (every 32-byte sector a warp touches is used whole), B fragments
+// from W_r through L1/L2.  Partial tiles of the slices are summed in slice order in shared memory.
+template <int NT>
+__global__ void __launch_bounds__(kRouterThreads) router_top2_mma_kernel(RouterArgs a) {
+  constexpr int NW = kRouterThreads / 32;
+  constexpr int EMAX = 8 * NT;
+  constexpr int UNR = 8;
+  __shared__ float s_part[NW][16][EMAX];
+  __shared__ int s_idx[kRouterChunk][2];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk_t0 = blockIdx.x * kRouterChunk;
+  const int T = a.T, d = a.d, E = a.E;
+  const int valid = min(kRouterChunk, T - chunk_t0);
+  const int H = valid > 16 ? 2 : 1;  // 16-token halves with work
+  const int S = NW / H;              // slices of the hidden dimension
+  const int h = warp % H, sl = warp / H;
+  const int g = lane >> 2, q = lane & 3;
+  const int r0 = chunk_t0 + 16 * h;
+  const bool v0 = r0 + g < T, v1 = r0 + g + 8 < T;
+  const uint32_t* x0 = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.x) +
+                                                          (size_t)(v0 ? r0 + g : 0) * d);
+  const uint32_t* x1 = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.x) +
+                                                          (size_t)(v1 ? r0 + g + 8 : 0) * d);
+  const uint32_t* wr[NT];
+  bool wv[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    wv[nt] = nt * 8 + g < E;
+    wr[nt] = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.w_router) +
+                                               (size_t)(wv[nt] ? nt * 8 + g : 0) * d);
+  }
+  const int nks = d / 16;
+  const int ks0 = (nks * sl) / S, ks1 = (nks * (sl + 1)) / S;
+  pdl_trigger();
+  pdl_wait();  // x may come from the previous kernel; the workspace from the previous forward
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+
+  for (int ks = ks0; ks < ks1; ks += UNR) {
+    uint32_t A[UNR][4], B[UNR][NT][2];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int c = (ks + u) * 8 + q;  // 32-bit word holding columns 2q, 2q+1 of this k-step
+      const bool in = ks + u < ks1;
+      A[u][0] = (in && v0) ? __ldg(x0 + c) : 0u;
+      A[u][1] = (in && v1) ? __ldg(x1 + c) : 0u;
+      A[u][2] = (in && v0) ? __ldg(x0 + c + 4) : 0u;
+      A[u][3] = (in && v1) ? __ldg(x1 + c + 4) : 0u;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        B[u][nt][0] = (in && wv[nt]) ? __ldg(wr[nt] + c) : 0u;
+        B[u][nt][1] = (in && wv[nt]) ? __ldg(wr[nt] + c + 4) : 0u;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      if (ks + u < ks1) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          asm volatile(
+              "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+              "{%0,%1,%2,%3};"
+              : "+f"(acc[nt][0]), "+f"(acc[nt][1]), "+f"(acc[nt][2]), "+f"(acc[nt][3])
+              : "r"(A[u][0]), "r"(A[u][1]), "r"(A[u][2]), "r"(A[u][3]), "r"(B[u][nt][0]), "r"(B[u][nt][1]));
+      }
+    }
+  }
+  // D fragment: acc[nt][0..1] = rows g, experts nt*8 + 2q, +1; acc[nt][2..3] = row g + 8
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    s_part[warp][g][nt * 8 + 2 * q] = acc[nt][0];
+    s_part[warp][g][nt * 8 + 2 * q + 1] = acc[nt][1];
+    s_part[warp][g + 8][nt * 8 + 2 * q] = acc[nt][2];
+    s_part[warp][g + 8][nt * 8 + 2 * q + 1] = acc[nt][3];
+  }
+  __syncthreads();
+  if (threadIdx.x < kRouterChunk) {
+    const int tt = threadIdx.x, hh = tt >> 4, r = tt & 15;
+    if (tt < valid) {
+      float L[EMAX];
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) {
+        float v = s_part[hh][r][e];
+        for (int s2 = 1; s2 < S; ++s2) v += s_part[hh + s2 * H][r][e];
+        L[e] = v + ((a.b_router != nullptr && e < E) ? a.b_router[e] : 0.f);
+      }
+      top2_store<EMAX>(a, L, chunk_t0 + tt, s_idx[tt]);
+    }
+  }
+  __syncthreads();
+  finish_chunk(a, s_idx, valid, chunk_t0);
+}
+
 template <typename Tin, int EMAX>
 cudaError_t launch_router_t(const RouterArgs& a, int nchunks, cudaStream_t s) {
   const int smem = EMAX * a.dchunk * (int)sizeof(Tin);
-  auto k = router_top2_kernel<Tin, EMAX>;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-  }
-  k<<<nchunks, kRouterThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return pdl_launch(router_top2_kernel<Tin, EMAX>, dim3(nchunks), dim3(kRouterThreads), smem, s, a);
+}
+
+template <typename Tin, int EMAX>
+cudaError_t prepare_router_t() {
+  return cudaFuncSetAttribute(router_top2_kernel<Tin, EMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kRouterMaxSmem);
 }
 
 }  // namespace
+
+cudaError_t prepare_router(int dtype, int E) {
+  if (dtype == 0) return E <= 4 ? prepare_router_t<float, 4>() : E <= 8 ? prepare_router_t<float, 8>()
+                                                                       : prepare_router_t<float, 16>();
+  return E <= 4 ? prepare_router_t<__nv_bfloat16, 4>() : E <= 8 ? prepare_router_t<__nv_bfloat16, 8>()
+                                                                 : prepare_router_t<__nv_bfloat16, 16>();
+}
 
 int router_smem_bytes(int dtype, int E, int dchunk) {
   const int emax = E <= 4 ? 4 : (E <= 8 ? 8 : 16);
@@ -265,6 +432,10 @@ cudaError_t launch_router(int dtype, const RouterArgs& a, int nchunks, cudaStrea
     if (a.E <= 4) return launch_router_t<float, 4>(a, nchunks, s);
     if (a.E <= 8) return launch_router_t<float, 8>(a, nchunks, s);
     return launch_router_t<float, 16>(a, nchunks, s);
+  }
+  if (a.d % 16 == 0) {
+    if (a.E <= 8) return pdl_launch(router_top2_mma_kernel<1>, dim3(nchunks), dim3(kRouterThreads), 0, s, a);
+    return pdl_launch(router_top2_mma_kernel<2>, dim3(nchunks), dim3(kRouterThreads), 0, s, a);
   }
   if (a.E <= 4) return launch_router_t<__nv_bfloat16, 4>(a, nchunks, s);
   if (a.E <= 8) return launch_router_t<__nv_bfloat16, 8>(a, nchunks, s);

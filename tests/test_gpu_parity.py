@@ -123,6 +123,26 @@ def test_small_bf16_relu_bias_with_router_bias():
     _full_check(li)
 
 
+@pytest.mark.parametrize("T", [1, 5, 16, 33, 64])
+def test_decode_path_matches_oracle_and_prefill_path(T, monkeypatch):
+    """Batches of <= 64 tokens take the weight-streaming decode kernels; the same inputs through the
+    prefill kernels (decode threshold 0) must agree, and both must match the oracle."""
+    shape = testgen.LayerShape("decode-small", T, 512, 384, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True)
+    li = testgen.make_inputs(shape)
+    _, out_d, r_d, ref, _ = _full_check(li)
+    monkeypatch.setenv("COLIBRI_MOE_DECODE_MAX_T", "0")
+    _, out_p, r_p, _, _ = _full_check(li)
+    for k in ("idx", "counts", "offsets", "row_of"):
+        assert np.array_equal(r_d[k], r_p[k]), k
+    assert rel_err(out_d, out_p) <= TOL_BF16
+
+
+def test_decode_path_relu_bias():
+    shape = testgen.LayerShape("decode-relu", 20, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")
+    li = testgen.make_inputs(shape)
+    _full_check(li)
+
+
 def test_1p3b_workload():
     li = testgen.make_inputs(testgen.CONFIGS["1.3b-8e"])
     _, _, _, _, err = _full_check(li)
