@@ -71,6 +71,8 @@ struct colibri_moe {
   CUtensorMap tm_w13_dec{}, tm_w2_dec{}, tm_xp_dec[4]{}, tm_h_dec[4]{};
   float* partial = nullptr;  // decode partial sums [splits][n_pad][E * rows]
   int decode_max_t = 0;
+  bool pair_gemm = false;    // prefill GEMMs on CTA pairs (256x256 tiles)
+  int pair_ctas = 0;         // co-resident CTAs of the pair kernel (persistent grid size)
   int32_t last_T = -1;
   std::vector<cudaEvent_t> events;
   uint64_t timeout_ns = 2000000000ull;
@@ -156,6 +158,11 @@ int check_config(const colibri_moe_config_t* c) {
   return COLIBRI_OK;
 }
 
+bool env_pair_gemm() {
+  const char* s = std::getenv("COLIBRI_MOE_GEMM");
+  return s && std::strcmp(s, "2sm") == 0;
+}
+
 int env_decode_max_t() {
   const char* s = std::getenv("COLIBRI_MOE_DECODE_MAX_T");
   if (s) {
@@ -228,6 +235,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   c->device = device;
   c->num_sms = sms;
   c->timeout_ns = env_timeout_ns();
+  c->pair_gemm = env_pair_gemm() && (sms % 2 == 0);
   const int64_t d = cfg->d_model, f = cfg->d_ff, E = cfg->num_experts, T = cfg->max_tokens;
   c->esize = cfg->dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
   c->out_esize = cfg->out_dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
@@ -294,10 +302,15 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
     return COLIBRI_ERR_CUDA;
   }
   if (prepare_router(cfg->dtype, cfg->num_experts) != cudaSuccess ||
-      (cfg->dtype == COLIBRI_DTYPE_BF16 && (prepare_tc_gemm() != cudaSuccess || prepare_decode_gemm() != cudaSuccess))) {
+      (cfg->dtype == COLIBRI_DTYPE_BF16 && (prepare_tc_gemm() != cudaSuccess || prepare_decode_gemm() != cudaSuccess ||
+                                             prepare_pair_gemm() != cudaSuccess))) {
     cudaGetLastError();
     colibri_moe_destroy(c);
     return COLIBRI_ERR_CUDA;
+  }
+  if (c->pair_gemm) {
+    c->pair_ctas = pair_gemm_max_ctas();
+    if (c->pair_ctas < 2) c->pair_gemm = false;
   }
   if (cfg->dtype == COLIBRI_DTYPE_BF16) {
     bool ok = make_tmap(&c->tm_xp, c->xp, d, c->rows_alloc, kRowTile) &&
@@ -453,7 +466,24 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     ctx->last_T = T;
     return COLIBRI_OK;
   }
-  if (bf16) {
+  if (bf16 && ctx->pair_gemm) {
+    // CTA pairs: 256-row tiles made of two 128-row tiles of one expert sharing the weight tile
+    const int bn = tc_gemm_block_n();
+    const int64_t max_pairs = (max_mtiles + E + 1) / 2;
+    GemmArgs up{ctx->sched, E, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns,
+                &ctx->sched->status};
+    int64_t ctas = 2 * max_pairs * up.n_tiles;
+    int grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
+    if (launch_pair_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, ctx->tm_xp, ctx->tm_w13_dec, up, grid, s) !=
+        cudaSuccess)
+      return COLIBRI_ERR_CUDA;
+    mark(3);
+    GemmArgs dn{ctx->sched, E, f, d, d / bn, ctx->y, d, ctx->b2, d, ctx->timeout_ns, &ctx->sched->status};
+    ctas = 2 * max_pairs * dn.n_tiles;
+    grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
+    if (launch_pair_gemm(kEpiStoreF32, ctx->tm_h, ctx->tm_w2_dec, dn, grid, s) != cudaSuccess)
+      return COLIBRI_ERR_CUDA;
+  } else if (bf16) {
     const int bn = tc_gemm_block_n();
     GemmArgs up{ctx->sched, E, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns,
                  &ctx->sched->status};

@@ -1,0 +1,378 @@
+// Grouped expert GEMM on CTA pairs (tcgen05 cta_group::2): 256x256 output tiles.
+//
+// Same computation as gemm_tcgen05.cu (the Compute stage of zskr.cn/news/2272131, "Colibri: a
+// lightweight C MoE inference engine for edge devices", 2.1: one GEMM per expert over its
+// contiguous rows, activation fused in the epilogue as in m.nxbn.cn/news/48047 2.1), mapped onto a
+// cluster of two CTAs on neighbouring SMs:
+//
+//   - each CTA loads its own 128-row A tile (its own M rows) and one 128-row half of the 256-row B
+//     tile, so each SM stages 32 KB per 64-wide K step instead of 48 KB;
+//   - the leader CTA (rank 0) issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16), which reads A and
+//     B from both CTAs' shared memory and accumulates each CTA's 128 rows in that CTA's TMEM;
+//   - both CTAs' TMA loads complete on the leader's `full` barrier; the leader's commits multicast to
+//     both CTAs' `empty` and `tmem_full` barriers; both epilogues arrive on the leader's `tmem_empty`.
+//
+// A pair computes two 128-row M tiles of one expert that share the weight tile; when an expert has
+// an odd number of M tiles, the second CTA of its last pair computes rows past the expert's segment
+// (read as they are or as zeros past the buffer) and stores nothing.  Waits are bounded as in the
+// single-CTA kernel; TMEM is allocated and freed collectively by one warp of each CTA.
+#include "tcgen05_ptx.cuh"
+
+namespace colibri {
+namespace {
+
+using namespace ptx;
+
+constexpr int PBM = 128, PBN = 256, PBK = 64, PUMMA_K = 16;
+constexpr int PSTAGES = 6;
+constexpr int PA_BYTES = PBM * PBK * 2;         // 16 KB: this CTA's A rows
+constexpr int PB_BYTES = (PBN / 2) * PBK * 2;   // 16 KB: this CTA's half of B
+constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
+constexpr int PNUM_THREADS = 192;
+constexpr uint32_t PTMEM_COLS = 512;
+constexpr int PNUM_BARS = 2 * PSTAGES + 5;
+constexpr int PSMEM_BYTES = 1024 + PSTAGES * PSTAGE_BYTES + PNUM_BARS * 8 + 16 + 4 * (4 * kMaxE + 4);
+static_assert(PSMEM_BYTES <= 227 * 1024, "pair GEMM shared memory");
+
+struct PairCoord {
+  int e, pm, n;
+};
+
+__device__ __forceinline__ PairCoord decode_pair(int p, const int* pstart, int E, int n_tiles) {
+  int e = 0;
+  while (e + 1 < E && pstart[e + 1] * n_tiles <= p) ++e;
+  const int local = p - pstart[e] * n_tiles;
+  const int pme = pstart[e + 1] - pstart[e];
+  PairCoord c;
+  c.e = e;
+  c.n = local / pme;
+  c.pm = local - c.n * pme;
+  return c;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(PNUM_THREADS, 1)
+    tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const GemmArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + PSTAGES * PA_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + PSTAGES * PB_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + PNUM_BARS);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_counts = reinterpret_cast<int*>(tmem_slot + 4);
+  int* s_offsets = s_counts + kMaxE;
+  int* s_mstart = s_offsets + kMaxE + 1;
+  int* s_pstart = s_mstart + kMaxE + 1;
+
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + PSTAGES);
+  const uint32_t tfull0 = smem_u32(bars + 2 * PSTAGES);
+  const uint32_t tempty0 = smem_u32(bars + 2 * PSTAGES + 2);
+  const uint32_t drain = smem_u32(bars + 2 * PSTAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = a.E;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  pdl_trigger();
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < PSTAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);   // leader's: one arrive (with both CTAs' bytes) per phase
+      mbar_init(empty0 + 8 * s, 1);  // each CTA's: one multicast commit per phase
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull0 + 8 * i, 1);
+      mbar_init(tempty0 + 8 * i, 8);  // leader's: 4 epilogue warps of each CTA
+    }
+    mbar_init(drain, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), PTMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  pdl_wait();  // the routing summary and the A operand come from earlier kernels
+  if (threadIdx.x < kMaxE) s_counts[threadIdx.x] = threadIdx.x < E ? a.sched->counts[threadIdx.x] : 0;
+  if (threadIdx.x < kMaxE + 1) {
+    s_offsets[threadIdx.x] = threadIdx.x <= E ? a.sched->offsets[threadIdx.x] : 0;
+    s_mstart[threadIdx.x] = threadIdx.x <= E ? a.sched->mtile_start[threadIdx.x] : 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      s_pstart[e] = acc;
+      acc += (s_mstart[e + 1] - s_mstart[e] + 1) / 2;
+    }
+    s_pstart[E] = acc;
+  }
+  tc_fence_before();
+  cluster_sync();  // barrier inits and TMEM addresses visible across the pair
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total = s_pstart[E] * a.n_tiles;
+  const int num_kb = (a.K + PBK - 1) / PBK;
+  const int pair_id = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_phase = 0;
+      bool ok = true;
+      for (int p = pair_id; ok && p < total; p += n_pairs) {
+        const PairCoord c = decode_pair(p, s_pstart, E, a.n_tiles);
+        const int a_row = s_offsets[c.e] + (2 * c.pm + static_cast<int>(rank)) * PBM;
+        const int b_row = c.e * a.n_per_expert + c.n * PBN + static_cast<int>(rank) * (PBN / 2);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, s_abort, a.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_leader = mapa_shared(full0 + 8 * stage, 0);
+          if (leader) {
+            mbar_arrive_expect_tx(full0 + 8 * stage, 2 * PSTAGE_BYTES);
+            armed |= 1u << stage;
+            armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          }
+          tma_load_2d_pair(smem_u32(sA + stage * PA_BYTES), &tmA, full_leader, kb * PBK, a_row);
+          tma_load_2d_pair(smem_u32(sB + stage * PB_BYTES), &tmB, full_leader, kb * PBK, b_row);
+          if (++stage == PSTAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        if (!*s_abort) atomicOr(a.status, kStatusTimeoutProducer);
+        *s_abort = 1;
+      }
+      // the leader's full barriers complete only when both CTAs' copies have landed
+      for (int s = 0; s < PSTAGES; ++s)
+        if (armed & (1u << s)) {
+          volatile int never = 0;
+          mbar_wait(full0 + 8 * s, (armed_phase >> s) & 1u, &never, a.timeout_ns);
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------------ MMA issuer (leader only)
+      constexpr uint32_t idesc = make_idesc_bf16(2 * PBM, PBN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int p = pair_id; ok && p < total; p += n_pairs) {
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, s_abort, a.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PBN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, s_abort, a.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * PA_BYTES);
+          const uint32_t b_addr = smem_u32(sB + stage * PB_BYTES);
+#pragma unroll
+          for (int k = 0; k < PBK / PUMMA_K; ++k)
+            umma_bf16_pair(d_tmem, sw128_desc(a_addr + k * PUMMA_K * 2), sw128_desc(b_addr + k * PUMMA_K * 2), idesc,
+                           (kb | k) != 0 ? 1u : 0u);
+          umma_commit_pair(empty0 + 8 * stage, 0x3);
+          if (++stage == PSTAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(tfull0 + 8 * acc, 0x3);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        if (!*s_abort) atomicOr(a.status, kStatusTimeoutMma);
+        *s_abort = 1;
+      }
+      umma_commit_pair(drain, 0x1);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never, a.timeout_ns);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue (warps 2..5, both CTAs)
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int p = pair_id; p < total; p += n_pairs) {
+      const PairCoord c = decode_pair(p, s_pstart, E, a.n_tiles);
+      bool ok = mbar_wait(tfull0 + 8 * acc, acc_phase, s_abort, a.timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0 && !*s_abort) atomicOr(a.status, kStatusTimeoutEpilogue);
+        if (lane == 0) *s_abort = 1;
+        break;
+      }
+      tc_fence_after();
+      const int row = s_offsets[c.e] + (2 * c.pm + static_cast<int>(rank)) * PBM + q * 32 + lane;
+      const bool valid = row < s_offsets[c.e] + s_counts[c.e];
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * PBN);
+      if constexpr (EPI == kEpiSwiGLU) {
+        // columns [0,128) = gate (B half of the leader), [128,256) = up (B half of the peer)
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(row) * a.ldo + c.n * (PBN / 2);
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t g[32], u[32];
+          tmem_ld32_sync(tbase + ch * 32, g);
+          tmem_ld32_sync(tbase + 128 + ch * 32, u);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+            const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+            pk[i] = pack_bf16((g0 / (1.0f + expf(-g0))) * u0, (g1 / (1.0f + expf(-g1))) * u1);
+          }
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+      } else if constexpr (EPI == kEpiReluBias) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(row) * a.ldo + c.n * PBN;
+        const float* bias = a.bias + static_cast<size_t>(c.e) * a.out_cols + c.n * PBN;
+#pragma unroll 1
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t v[32];
+          tmem_ld32_sync(tbase + ch * 32, v);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16(fmaxf(__uint_as_float(v[2 * i]) + bias[ch * 32 + 2 * i], 0.f),
+                              fmaxf(__uint_as_float(v[2 * i + 1]) + bias[ch * 32 + 2 * i + 1], 0.f));
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+          }
+        }
+      } else {
+        float* out = static_cast<float*>(a.out) + static_cast<size_t>(row) * a.ldo + c.n * PBN;
+        const float* bias = a.bias ? a.bias + static_cast<size_t>(c.e) * a.out_cols + c.n * PBN : nullptr;
+#pragma unroll 1
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t v[32];
+          tmem_ld32_sync(tbase + ch * 32, v);
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(out + ch * 32);
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+              float4 o = make_float4(__uint_as_float(v[4 * w]), __uint_as_float(v[4 * w + 1]),
+                                     __uint_as_float(v[4 * w + 2]), __uint_as_float(v[4 * w + 3]));
+              if (bias) {
+                o.x += bias[ch * 32 + 4 * w];
+                o.y += bias[ch * 32 + 4 * w + 1];
+                o.z += bias[ch * 32 + 4 * w + 2];
+                o.w += bias[ch * 32 + 4 * w + 3];
+              }
+              dst[w] = o;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(mapa_shared(tempty0 + 8 * acc, 0));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();  // no CTA leaves while its peer may still signal its barriers
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, PTMEM_COLS);
+  }
+}
+
+template <int EPI>
+cudaError_t launch_pair_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
+                          cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(PNUM_THREADS);
+  cfg.dynamicSmemBytes = PSMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<EPI>, tmA, tmB, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t prepare_pair_gemm() {
+  cudaError_t e = cudaFuncSetAttribute(tc_pair_gemm_kernel<kEpiSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       PSMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tc_pair_gemm_kernel<kEpiReluBias>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PSMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tc_pair_gemm_kernel<kEpiStoreF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PSMEM_BYTES);
+  return e;
+}
+
+// Most CTA pairs of this kernel that can be resident at once on the current device (0 on error).
+int pair_gemm_max_ctas() {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(PNUM_THREADS);
+  cfg.dynamicSmemBytes = PSMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, tc_pair_gemm_kernel<kEpiStoreF32>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return 2 * clusters;
+}
+
+// grid: an even number of CTAs (one pair per two SMs)
+cudaError_t launch_pair_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
+                             cudaStream_t s) {
+  grid &= ~1;
+  if (grid <= 0) return cudaSuccess;
+  switch (epi) {
+    case kEpiSwiGLU: return launch_pair_t<kEpiSwiGLU>(tmA, tmB, a, grid, s);
+    case kEpiReluBias: return launch_pair_t<kEpiReluBias>(tmA, tmB, a, grid, s);
+    default: return launch_pair_t<kEpiStoreF32>(tmA, tmB, a, grid, s);
+  }
+}
+
+}  // namespace colibri

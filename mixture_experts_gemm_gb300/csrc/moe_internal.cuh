@@ -174,6 +174,10 @@ int router_smem_bytes(int dtype, int E, int dchunk);
 cudaError_t prepare_router(int dtype, int E);
 cudaError_t prepare_tc_gemm();
 cudaError_t prepare_decode_gemm();
+cudaError_t prepare_pair_gemm();
+int pair_gemm_max_ctas();
+cudaError_t launch_pair_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
+                             cudaStream_t s);
 cudaError_t launch_decode_gemm(const CUtensorMap& tmW, const CUtensorMap& tmX, const DecodeArgs& a, int grid,
                                cudaStream_t s);
 cudaError_t launch_decode_act(bool swiglu, const DecodeActArgs& a, cudaStream_t s);

@@ -143,6 +143,27 @@ def test_decode_path_relu_bias():
     _full_check(li)
 
 
+@pytest.mark.parametrize("case", ["int-relu", "swiglu-odd-tiles", "skewed"])
+def test_pair_gemm_kernel(case, monkeypatch):
+    """The CTA-pair (cta_group::2) grouped GEMM, selected with COLIBRI_MOE_GEMM=2sm: exact-integer
+    layer bit for bit, experts with an odd number of 128-row tiles, and a skewed router."""
+    monkeypatch.setenv("COLIBRI_MOE_GEMM", "2sm")
+    if case == "int-relu":
+        shape = testgen.LayerShape("pair-int", 300, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")
+        li, h, y = _integer_inputs(shape, 300, lo=-1, hi=2, wlo=-1, whi=2, seed=3)
+        layer = make_layer(li)
+        out, r = run(layer, x_device(li))
+        assert np.array_equal(out, y.astype(np.float64))
+        assert layer.device_status() == 0
+    elif case == "swiglu-odd-tiles":
+        shape = testgen.LayerShape("pair-swiglu", 700, 512, 384, 4, testgen.ACT_SWIGLU, "bf16")
+        _full_check(testgen.make_inputs(shape))
+    else:
+        shape = testgen.LayerShape("pair-skewed", 1500, 512, 256, 16, testgen.ACT_SWIGLU, "bf16",
+                                   zipf_router_bias=True)
+        _full_check(testgen.make_inputs(shape))
+
+
 def test_1p3b_workload():
     li = testgen.make_inputs(testgen.CONFIGS["1.3b-8e"])
     _, _, _, _, err = _full_check(li)
