@@ -158,9 +158,10 @@ int check_config(const colibri_moe_config_t* c) {
   return COLIBRI_OK;
 }
 
+// Prefill GEMMs run on CTA pairs (cta_group::2) unless COLIBRI_MOE_GEMM=1sm selects the single-CTA kernel.
 bool env_pair_gemm() {
   const char* s = std::getenv("COLIBRI_MOE_GEMM");
-  return s && std::strcmp(s, "2sm") == 0;
+  return !(s && std::strcmp(s, "1sm") == 0);
 }
 
 int env_decode_max_t() {

@@ -280,10 +280,10 @@ __global__ void __launch_bounds__(256) decode_act_kernel(DecodeActArgs a) {
       g.x += pg.x; g.y += pg.y; g.z += pg.z; g.w += pg.w;
       u.x += pu.x; u.y += pu.y; u.z += pu.z; u.w += pu.w;
     }
-    h[0] = (g.x / (1.0f + expf(-g.x))) * u.x;
-    h[1] = (g.y / (1.0f + expf(-g.y))) * u.y;
-    h[2] = (g.z / (1.0f + expf(-g.z))) * u.z;
-    h[3] = (g.w / (1.0f + expf(-g.w))) * u.w;
+    h[0] = silu_fast(g.x) * u.x;
+    h[1] = silu_fast(g.y) * u.y;
+    h[2] = silu_fast(g.z) * u.z;
+    h[3] = silu_fast(g.w) * u.w;
   } else {
     const size_t grow = static_cast<size_t>(e) * a.n_per_expert + c;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -240,8 +240,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < 16; ++i) {
             const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
             const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-            const float h0 = (g0 / (1.0f + expf(-g0))) * u0;
-            const float h1 = (g1 / (1.0f + expf(-g1))) * u1;
+            const float h0 = silu_fast(g0) * u0;
+            const float h1 = silu_fast(g1) * u1;
             p[i] = pack_bf16(h0, h1);
           }
           if (valid) {

@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(PNUM_THREADS, 1)
           for (int i = 0; i < 16; ++i) {
             const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
             const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-            pk[i] = pack_bf16((g0 / (1.0f + expf(-g0))) * u0, (g1 / (1.0f + expf(-g1))) * u1);
+            pk[i] = pack_bf16(silu_fast(g0) * u0, silu_fast(g1) * u1);
           }
           if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);

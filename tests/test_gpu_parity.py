@@ -145,7 +145,7 @@ def test_decode_path_relu_bias():
 
 @pytest.mark.parametrize("case", ["int-relu", "swiglu-odd-tiles", "skewed"])
 def test_pair_gemm_kernel(case, monkeypatch):
-    """The CTA-pair (cta_group::2) grouped GEMM, selected with COLIBRI_MOE_GEMM=2sm: exact-integer
+    """The CTA-pair (cta_group::2) grouped GEMM (the default; COLIBRI_MOE_GEMM=2sm): exact-integer
     layer bit for bit, experts with an odd number of 128-row tiles, and a skewed router."""
     monkeypatch.setenv("COLIBRI_MOE_GEMM", "2sm")
     if case == "int-relu":
@@ -162,6 +162,25 @@ def test_pair_gemm_kernel(case, monkeypatch):
         shape = testgen.LayerShape("pair-skewed", 1500, 512, 256, 16, testgen.ACT_SWIGLU, "bf16",
                                    zipf_router_bias=True)
         _full_check(testgen.make_inputs(shape))
+
+
+@pytest.mark.parametrize("case", ["int-relu", "swiglu", "skewed"])
+def test_single_cta_gemm_kernel(case, monkeypatch):
+    """The single-CTA grouped GEMM (COLIBRI_MOE_GEMM=1sm) on the same cases as the pair kernel."""
+    monkeypatch.setenv("COLIBRI_MOE_GEMM", "1sm")
+    if case == "int-relu":
+        shape = testgen.LayerShape("one-int", 300, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")
+        li, h, y = _integer_inputs(shape, 300, lo=-1, hi=2, wlo=-1, whi=2, seed=4)
+        layer = make_layer(li)
+        out, r = run(layer, x_device(li))
+        assert np.array_equal(out, y.astype(np.float64))
+        assert layer.device_status() == 0
+    elif case == "swiglu":
+        _full_check(testgen.make_inputs(testgen.LayerShape("one-swiglu", 700, 512, 384, 4, testgen.ACT_SWIGLU,
+                                                           "bf16")))
+    else:
+        _full_check(testgen.make_inputs(testgen.LayerShape("one-skewed", 1500, 512, 256, 16, testgen.ACT_SWIGLU,
+                                                           "bf16", zipf_router_bias=True)))
 
 
 def test_1p3b_workload():
