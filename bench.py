@@ -29,6 +29,9 @@ METRIC = "MoE-layer tokens/s at Mixtral-8x7B shape; % of bf16 tensor peak / HBM 
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 STAGES = ["router", "gather", "gemm_up", "gemm_down", "combine"]
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture of the kernel as it now
+# stands (profiles/gemm_pair_mixtral_prefill.md); None where no capture of the current kernel exists.
+NCU_TRAFFIC = {("mixtral-prefill", 8192, "gemm_up", "2sm"): 3.836e9, ("mixtral-prefill", 8192, "gemm_down", "2sm"): 3.466e9}
 
 
 def log(*a):
@@ -333,9 +336,14 @@ def main():
     if shape.dtype == "bf16" and T >= 256 and dominant in (2, 3):
         fl = alg["flops_up"] if dominant == 2 else alg["flops_down"]
         ach = fl / dur / 1e12
-        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        # timed inside a seconds-long loop of steps: the sustained (power-capped) peak applies
+        peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        gemm = "1sm" if os.environ.get("COLIBRI_MOE_GEMM") == "1sm" else "2sm"
         roof = {"bound": "tensor", "kernel": STAGES[dominant], "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                "frac": ach / peak, "traffic": None, "peak_source": f"{peak_src} bf16 burst"}
+                "frac": ach / peak, "traffic": NCU_TRAFFIC.get((shape.name, T, STAGES[dominant], gemm)),
+                "peak_source": f"{peak_src} bf16 sustained", "frac_of_burst": ach / burst,
+                "algorithmic_flops_per_launch": fl}
     else:
         # weight streaming: bytes of the distinct active experts' weights this stage reads
         n_up = 2 if shape.act == 1 else 1
@@ -345,7 +353,9 @@ def main():
         ach = byts / dur / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         roof = {"bound": "hbm", "kernel": STAGES[dominant], "achieved": ach, "peak": peak, "unit": "GB/s",
-                "frac": ach / peak, "traffic": None, "peak_source": f"{peak_src} copy"}
+                "frac": ach / peak, "traffic": NCU_TRAFFIC.get((shape.name, T, STAGES[dominant], "decode")),
+                "peak_source": f"{peak_src} copy", "algorithmic_bytes_per_launch": byts,
+                "step_frac_of_hbm": alg["bytes"] / (ms_per_step / 1e3) / 1e9 / peak}
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
