@@ -18,7 +18,7 @@ takes ``v`` as the variance):
 x ~ N(0, 1); weights ~ N(0, 1/fan_in); biases ~ N(0, 0.01); router weights
 ~ N(0, 1/d).  Seed 0 throughout.  Tensor ids: x = 0, W_r = 1, b_r = 2, and for
 expert e: 16 + 8e + {0: W1 (ReLU) or W_gate (SwiGLU), 1: W_up, 2: W2/W_down,
-3: b1, 4: b2}.
+3: b1, 4: b2}; the optional shared expert: 8 + {0..4} in the same order.
 """
 from __future__ import annotations
 
@@ -50,10 +50,12 @@ class LayerShape:
     dtype: str               # "f32" or "bf16"
     zipf_router_bias: bool = False
     top_k: int = 2
+    gate_mode: int = 0       # 0 softmax over the selected experts, 1 full softmax (unnormalised)
+    shared_expert: bool = False
 
     def with_T(self, T: int) -> "LayerShape":
         return LayerShape(self.name, T, self.d_model, self.d_ff, self.num_experts, self.act,
-                          self.dtype, self.zipf_router_bias, self.top_k)
+                          self.dtype, self.zipf_router_bias, self.top_k, self.gate_mode, self.shared_expert)
 
 
 CONFIGS = {
@@ -66,6 +68,7 @@ CONFIGS = {
 DECODE_TOKENS = (1, 4, 16, 32)
 
 TID_X, TID_WR, TID_BR = 0, 1, 2
+TID_SHARED = 8  # shared expert: 8 W1/W_gate, 9 W_up, 10 W2/W_down, 11 b1, 12 b2
 
 
 def tid_expert(e: int, which: int) -> int:
@@ -161,6 +164,15 @@ class LayerInputs:
     w2_bits: List[np.ndarray] = field(default_factory=list)
     b1: List[np.ndarray] = field(default_factory=list)
     b2: List[np.ndarray] = field(default_factory=list)
+    # shared expert (same shapes as one routed expert)
+    ws1_f32: Optional[np.ndarray] = None
+    ws3_f32: Optional[np.ndarray] = None
+    ws2_f32: Optional[np.ndarray] = None
+    ws1_bits: Optional[np.ndarray] = None
+    ws3_bits: Optional[np.ndarray] = None
+    ws2_bits: Optional[np.ndarray] = None
+    bs1: Optional[np.ndarray] = None
+    bs2: Optional[np.ndarray] = None
 
 
 def _draw(seed, tid, shape, std, is_bf16, want_f32, want_bits):
@@ -196,6 +208,14 @@ def make_weights(shape: LayerShape, seed: int = 0, want_f32: bool = True, want_b
         if shape.act == ACT_RELU_BIAS:
             li.b1.append(normal_f32(seed, tid_expert(e, 3), (f,), 0.1))
             li.b2.append(normal_f32(seed, tid_expert(e, 4), (d,), 0.1))
+    if shape.shared_expert:
+        li.ws1_f32, li.ws1_bits = _draw(seed, TID_SHARED + 0, (f, d), math.sqrt(1.0 / d), bf, want_f32, want_bits)
+        if shape.act == ACT_SWIGLU:
+            li.ws3_f32, li.ws3_bits = _draw(seed, TID_SHARED + 1, (f, d), math.sqrt(1.0 / d), bf, want_f32, want_bits)
+        li.ws2_f32, li.ws2_bits = _draw(seed, TID_SHARED + 2, (d, f), math.sqrt(1.0 / f), bf, want_f32, want_bits)
+        if shape.act == ACT_RELU_BIAS:
+            li.bs1 = normal_f32(seed, TID_SHARED + 3, (f,), 0.1)
+            li.bs2 = normal_f32(seed, TID_SHARED + 4, (d,), 0.1)
     return li
 
 

@@ -18,7 +18,8 @@ import testgen
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
-def _layer(d, f, E, act, rng, router=None, b_router=None, identical=False, integer=False):
+def _layer(d, f, E, act, rng, router=None, b_router=None, identical=False, integer=False, top_k=2, gate_mode=0,
+           shared=False):
     def draw(shape, scale):
         if integer:
             return rng.integers(-2, 3, size=shape).astype(np.float32)
@@ -36,19 +37,33 @@ def _layer(d, f, E, act, rng, router=None, b_router=None, identical=False, integ
         w3 = None if w3 is None else w3 * E
         b1 = None if b1 is None else b1 * E
         b2 = None if b2 is None else b2 * E
-    return oracle.OracleLayer(d, f, E, act, wr, w1, w2, w3=w3, b_router=b_router, b1=b1, b2=b2)
+    sh = None
+    if shared:
+        sh = dict(w1=draw((f, d), 1 / math.sqrt(d)), w2=draw((d, f), 1 / math.sqrt(f)),
+                  w3=draw((f, d), 1 / math.sqrt(d)) if act == oracle.ACT_SWIGLU else None,
+                  b1=draw((f,), 0.1) if act == oracle.ACT_RELU_BIAS else None,
+                  b2=draw((d,), 0.1) if act == oracle.ACT_RELU_BIAS else None)
+    return oracle.OracleLayer(d, f, E, act, wr, w1, w2, w3=w3, b_router=b_router, b1=b1, b2=b2, top_k=top_k,
+                              gate_mode=gate_mode, shared=sh)
 
 
 def _numpy_ffn(layer, e, x):
-    """Expert FFN written with numpy matmuls (an independent routine)."""
+    """Expert FFN written with numpy matmuls (an independent routine); e = "shared" for the shared expert."""
     x = x.astype(np.float64)
-    W1 = layer._w1[e].astype(np.float64)
-    W2 = layer._w2[e].astype(np.float64)
+    if e == "shared":
+        sh = layer._shared
+        W1, W2, W3, B1, B2 = sh["w1"], sh["w2"], sh.get("w3"), sh.get("b1"), sh.get("b2")
+    else:
+        W1, W2 = layer._w1[e], layer._w2[e]
+        W3 = None if layer._w3 is None else layer._w3[e]
+        B1 = None if layer._b1 is None else layer._b1[e]
+        B2 = None if layer._b2 is None else layer._b2[e]
+    W1, W2 = W1.astype(np.float64), W2.astype(np.float64)
     if layer.act == oracle.ACT_RELU_BIAS:
-        h = np.maximum(x @ W1.T + layer._b1[e], 0.0)
-        return h @ W2.T + layer._b2[e]
+        h = np.maximum(x @ W1.T + B1, 0.0)
+        return h @ W2.T + B2
     g = x @ W1.T
-    u = x @ layer._w3[e].astype(np.float64).T
+    u = x @ W3.astype(np.float64).T
     silu = g * 0.5 * (1.0 + np.tanh(0.5 * g))  # z * sigmoid(z) through tanh: a different formula
     return (silu * u) @ W2.T
 
@@ -121,7 +136,7 @@ def test_top2_equals_bruteforce_on_random_and_tied_logits(E):
     logits = np.concatenate([rng.standard_normal((200, E)),
                              rng.integers(-2, 3, size=(400, E)).astype(np.float64),   # many ties
                              np.zeros((3, E))])
-    idx, gate = L.top2(logits)
+    idx, gate = L.topk(logits)
     for t in range(logits.shape[0]):
         assert tuple(idx[t]) == _brute_top2(logits[t]), (t, logits[t], idx[t])
 
@@ -140,11 +155,11 @@ def test_top2_special_cases():
     wr[2] = wr[5] = 1.0
     Ld = _layer(d, 8, E, oracle.ACT_SWIGLU, rng, router=wr)
     xp = np.abs(rng.standard_normal((10, d))).astype(np.float32)
-    idx, gate = Ld.top2(Ld.router_logits(xp))
+    idx, gate = Ld.topk(Ld.router_logits(xp))
     assert np.all(idx == [2, 5]) and np.all(gate == 0.5)
     # two experts: idx is a permutation of {0, 1}
     L2 = _layer(d, 8, 2, oracle.ACT_SWIGLU, rng)
-    idx, _ = L2.top2(L2.router_logits(x))
+    idx, _ = L2.topk(L2.router_logits(x))
     assert np.all(np.sort(idx, axis=1) == [0, 1])
 
 
@@ -153,7 +168,7 @@ def test_gates_are_softmax_over_the_selected_pair():
     E = 8
     L = _layer(8, 8, E, oracle.ACT_SWIGLU, rng)
     logits = rng.standard_normal((300, E)) * 3
-    idx, gate = L.top2(logits)
+    idx, gate = L.topk(logits)
     p = np.exp(logits - logits.max(axis=1, keepdims=True))
     p /= p.sum(axis=1, keepdims=True)                        # full softmax over experts
     pa = np.take_along_axis(p, idx[:, :1], 1)[:, 0]
@@ -178,7 +193,7 @@ def test_printed_gate_pairs():
         logits[0, a] = 1.0
         logits[0, b] = 1.0 - math.log(ga / gb)   # the logit gap a pair-softmax gives these gates
         L = _layer(8, 8, E, oracle.ACT_SWIGLU, np.random.default_rng(0))
-        idx, gate = L.top2(logits)
+        idx, gate = L.topk(logits)
         assert tuple(idx[0]) == (a, b)
         np.testing.assert_allclose(gate[0], [ga, gb], rtol=0, atol=1e-12)
 
@@ -270,3 +285,87 @@ def test_oracle_on_generated_tiny_workload():
     r = L.forward(li.x_f32)
     assert r["out"].shape == (64, 256) and np.isfinite(r["out"]).all()
     assert r["counts"].sum() == 128 and np.all(r["gate"][:, 0] >= 0.5)
+
+
+# ------------------------------------------------------------------ top-k, gate modes, shared expert
+def _brute_topk(Lrow, k):
+    """Lexicographic maximum over ordered k-tuples of distinct experts of (L_e1..L_ek, -e1..-ek)."""
+    E = len(Lrow)
+    return max((tuple(Lrow[e] for e in p) + tuple(-e for e in p), p)
+               for p in itertools.permutations(range(E), k))[1]
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 4])
+@pytest.mark.parametrize("E", [4, 8])
+def test_topk_equals_bruteforce(k, E):
+    rng = np.random.default_rng(100 * k + E)
+    L = _layer(8, 8, E, oracle.ACT_SWIGLU, rng, top_k=k)
+    logits = np.concatenate([rng.standard_normal((60, E)), rng.integers(-1, 2, size=(120, E)).astype(np.float64),
+                             np.zeros((2, E))])
+    idx, gate = L.topk(logits)
+    assert idx.shape == (logits.shape[0], k)
+    for t in range(logits.shape[0]):
+        assert tuple(idx[t]) == _brute_topk(logits[t], k), (t, logits[t], idx[t])
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 4])
+def test_gates_softmax_over_selected_and_full_softmax(k):
+    rng = np.random.default_rng(200 + k)
+    E = 8
+    logits = rng.standard_normal((200, E)) * 2
+    Lp = _layer(8, 8, E, oracle.ACT_SWIGLU, rng, top_k=k, gate_mode=oracle.GATE_PAIR_SOFTMAX)
+    Lf = _layer(8, 8, E, oracle.ACT_SWIGLU, rng, top_k=k, gate_mode=oracle.GATE_FULL_SOFTMAX)
+    idx, gp = Lp.topk(logits)
+    idx2, gf = Lf.topk(logits)
+    assert np.array_equal(idx, idx2)                     # the mode changes gates, not the selection
+    sel = np.take_along_axis(logits, idx, 1)
+    z = np.exp(sel - sel.max(axis=1, keepdims=True))
+    np.testing.assert_allclose(gp, z / z.sum(axis=1, keepdims=True), rtol=1e-12, atol=1e-15)
+    full = np.exp(logits - logits.max(axis=1, keepdims=True))
+    full /= full.sum(axis=1, keepdims=True)
+    np.testing.assert_allclose(gf, np.take_along_axis(full, idx, 1), rtol=1e-12, atol=1e-15)
+    assert np.all(np.abs(gp.sum(axis=1) - 1) < 1e-14)
+    if k < E:
+        assert np.all(gf.sum(axis=1) < 1.0)
+    assert np.all(np.diff(gp, axis=1) <= 0) and np.all(np.diff(gf, axis=1) <= 0)   # descending
+    if k == 1:
+        assert np.all(gp == 1.0)
+
+
+def test_dispatch_three_slots_bruteforce():
+    rng = np.random.default_rng(7)
+    T, E, k = 50, 6, 3
+    L = _layer(8, 8, E, oracle.ACT_SWIGLU, rng, top_k=k)
+    idx = np.array([rng.choice(E, k, replace=False) for _ in range(T)], dtype=np.int32)
+    counts, offs, row_of, tok = L.dispatch(idx)
+    slots = sorted((int(idx[t, s]), t, s) for t in range(T) for s in range(k))
+    for row, (e, t, s) in enumerate(slots):
+        assert row_of[t, s] == row and tok[row] == t
+    assert counts.sum() == k * T
+
+
+@pytest.mark.parametrize("act", [oracle.ACT_RELU_BIAS, oracle.ACT_SWIGLU])
+@pytest.mark.parametrize("k,mode", [(1, 0), (3, 0), (4, 1), (2, 1)])
+def test_output_is_gated_sum_plus_shared_expert(act, k, mode):
+    rng = np.random.default_rng(300 + 10 * k + mode + act)
+    d, f, E = 32, 48, 6
+    L = _layer(d, f, E, act, rng, top_k=k, gate_mode=mode, shared=True)
+    x = rng.standard_normal((20, d)).astype(np.float32)
+    r = L.forward(x)
+    assert r["idx"].shape == (20, k)
+    for t in range(20):
+        ref = _numpy_ffn(L, "shared", x[t:t + 1])[0]
+        for s in range(k):
+            ref = ref + r["gate"][t, s] * _numpy_ffn(L, r["idx"][t, s], x[t:t + 1])[0]
+        np.testing.assert_allclose(r["out"][t], ref, rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(L.shared_ffn(x[0]), _numpy_ffn(L, "shared", x[:1])[0], rtol=1e-11, atol=1e-12)
+
+
+def test_shared_expert_with_zero_weights_changes_nothing():
+    rng = np.random.default_rng(400)
+    d, f, E = 32, 40, 4
+    base = _layer(d, f, E, oracle.ACT_SWIGLU, rng)
+    zero = dict(w1=np.zeros((f, d)), w3=np.zeros((f, d)), w2=np.zeros((d, f)))
+    with_sh = oracle.OracleLayer(d, f, E, oracle.ACT_SWIGLU, base._wr, base._w1, base._w2, w3=base._w3, shared=zero)
+    x = rng.standard_normal((10, d)).astype(np.float32)
+    assert np.array_equal(with_sh.forward(x)["out"], base.forward(x)["out"])
