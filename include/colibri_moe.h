@@ -2,7 +2,7 @@
  * colibri_moe.h -- C ABI of a GB300 (sm_103a) Mixture-of-Experts layer forward.
  *
  * One call of colibri_moe_forward runs, on the caller's CUDA stream:
- *   1. router: logits L = x W_r^T (+ b_r), top-2 experts per token, gates
+ *   1. router: logits L = x W_r^T (+ b_r), top-k experts per token (k = 1..4), gates
  *      (zskr.cn/news/2272131 "Colibri: a lightweight C MoE inference engine for
  *      edge devices" 3.2; hnwysp.cn/news/30485 3.1);
  *   2. dispatch: per-expert counts, offsets, tokens gathered into
@@ -14,11 +14,15 @@
  *
  * Math of the layer (all row-major, nn.Linear [out, in] weight layout):
  *   L[t,e]   = sum_j x[t,j] W_r[e,j] (+ b_r[e])
- *   (a, b)   = the two experts ranked first by (L descending, expert index ascending)
- *   g_a      = 1 / (1 + exp(L[t,b] - L[t,a])),  g_b = 1 - g_a   (softmax over the pair)
+ *   e_1..e_k = the k experts ranked first by (L descending, expert index ascending)
+ *   gates    = softmax of L over e_1..e_k (default; k = 2: g_1 = 1/(1+exp(L_e2 - L_e1)), g_2 = 1 - g_1),
+ *              or the softmax over all E experts evaluated at e_1..e_k (COLIBRI_GATE_SOFTMAX_ALL)
  *   SwiGLU:  y_e(x) = W2_e (silu(W1_e x) * (W3_e x))      W1 = W_gate, W3 = W_up, W2 = W_down
  *   ReLU:    y_e(x) = W2_e max(W1_e x + b1_e, 0) + b2_e
- *   out[t]   = g_a y_a(x_t) + g_b y_b(x_t)                (fp32 sum; no residual add)
+ *   out[t]   = sum_j g_j y_{e_j}(x_t) (+ y_shared(x_t))   (fp32 sum in slot order; no residual add)
+ * (the two gate modes: news.rkmt.cn/news/2271114 5.2 "linear top-2" (Mixtral) vs "softmax top-2"
+ * (DeepSeek), the latter being the weights hnwysp.cn 3.1's code returns; top_k: hnwysp.cn 3.1;
+ * shared expert: news.rkmt.cn 5.2, Qwen2-MoE's always-on expert.)
  *
  * Conventions (m.nxbn.cn 3.3 and 5.1: int status codes, 0 = success;
  * zskr.cn 5.3: one context per thread; hnwysp.cn 2.1: no allocation on the
@@ -66,20 +70,26 @@ extern "C" {
 #define COLIBRI_ACT_RELU_BIAS 0 /* y = W2 max(W1 x + b1, 0) + b2 (b1, b2 required)       */
 #define COLIBRI_ACT_SWIGLU 1    /* y = W2 (silu(W1 x) * (W3 x)), no biases                 */
 
+#define COLIBRI_GATE_SOFTMAX_SELECTED 0 /* softmax over the k selected logits (sums to 1)          */
+#define COLIBRI_GATE_SOFTMAX_ALL 1      /* softmax over all experts, at the selected ones (sum < 1) */
+
 #define COLIBRI_MAX_EXPERTS 16
+#define COLIBRI_MAX_TOP_K 4
 
 typedef struct colibri_moe colibri_moe_t; /* opaque */
 
 typedef struct {
   int32_t d_model;         /* d: hidden size.  Multiple of 8; bf16 also needs d % 256 == 0        */
   int32_t d_ff;            /* f: expert inner size.  bf16 SwiGLU: f % 128 == 0; bf16 ReLU: f % 256 */
-  int32_t num_experts;     /* E, 2..16                                                              */
-  int32_t top_k;           /* must be 2                                                             */
+  int32_t num_experts;     /* E, 2..16 routed experts                                               */
+  int32_t top_k;           /* k, 1..4 and <= E                                                      */
   int32_t max_tokens;      /* largest T any forward will be given (> 0); sizes the workspace        */
   int32_t dtype;           /* COLIBRI_DTYPE_*: dtype of x and of all weights                         */
   int32_t act;             /* COLIBRI_ACT_*                                                          */
   int32_t has_router_bias; /* 0/1: b_r present                                                       */
   int32_t out_dtype;       /* COLIBRI_DTYPE_*: dtype of out (the combine itself is fp32)             */
+  int32_t gate_mode;       /* COLIBRI_GATE_*                                                         */
+  int32_t has_shared_expert; /* 0/1: an always-on expert of the same shape, added with weight 1      */
 } colibri_moe_config_t;
 
 /* Per-tensor pointers, nn.Linear [out, in] row-major, dtype = config.dtype for weights and fp32 for
@@ -93,6 +103,11 @@ typedef struct {
   const void* const* w2;     /* E x [d, f]: W2 / W_down                            */
   const float* const* b1;    /* E x [f] fp32: ReLU only (required), else NULL      */
   const float* const* b2;    /* E x [d] fp32: ReLU only (required), else NULL      */
+  const void* ws1;           /* shared expert [f, d] (W1 / W_gate); NULL without one */
+  const void* ws3;           /* shared expert [f, d] W_up (SwiGLU)                    */
+  const void* ws2;           /* shared expert [d, f] (W2 / W_down)                    */
+  const float* bs1;          /* shared expert [f] fp32 (ReLU)                         */
+  const float* bs2;          /* shared expert [d] fp32 (ReLU)                         */
 } colibri_moe_weights_t;
 
 /* Validates the config, selects `device`, and allocates the workspace for max_tokens tokens
@@ -117,9 +132,10 @@ COLIBRI_API int colibri_moe_forward(colibri_moe_t* ctx, const void* x, void* out
 COLIBRI_API int colibri_moe_forward_host(colibri_moe_t* ctx, const void* x_host, void* out_host, int32_t T, void* stream);
 
 /* Routing of the most recent forward, copied into caller DEVICE buffers on `stream` (any may be
- * NULL): idx[T,2] int32 (slot 0 = higher logit), gate[T,2] fp32, counts[E] int32,
- * offsets[E+1] int32 (row where each expert's segment starts; segments padded to 128 rows),
- * row_of[T,2] int32 (row of token t's slot s; row_of - offsets[e] is t's rank among e's tokens). */
+ * NULL): idx[T,k] int32 (slot 0 = highest logit), gate[T,k] fp32, counts[E] int32 (routed
+ * experts), offsets[E+1] int32 (row where each routed expert's segment starts; segments padded to
+ * 128 rows; offsets[E] is where the shared expert's rows start when there is one), row_of[T,k]
+ * int32 (row of token t's slot s; row_of - offsets[e] is t's rank among e's tokens). */
 COLIBRI_API int colibri_moe_get_routing(colibri_moe_t* ctx, int32_t* idx, float* gate, int32_t* counts, int32_t* offsets,
                             int32_t* row_of, void* stream);
 

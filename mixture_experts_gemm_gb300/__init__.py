@@ -24,6 +24,9 @@ __all__ = ["MoELayer", "ColibriError", "lib", "LIB_PATH", "DTYPE_F32", "DTYPE_BF
 
 DTYPE_F32, DTYPE_BF16 = 0, 1
 ACT_RELU_BIAS, ACT_SWIGLU = 0, 1
+GATE_SOFTMAX_SELECTED, GATE_SOFTMAX_ALL = 0, 1
+_GATES = {"selected": GATE_SOFTMAX_SELECTED, "pair": GATE_SOFTMAX_SELECTED, "all": GATE_SOFTMAX_ALL,
+          "full": GATE_SOFTMAX_ALL}
 _DTYPES = {"f32": DTYPE_F32, "fp32": DTYPE_F32, "float32": DTYPE_F32, "bf16": DTYPE_BF16, "bfloat16": DTYPE_BF16}
 _ACTS = {"relu_bias": ACT_RELU_BIAS, "relu": ACT_RELU_BIAS, "swiglu": ACT_SWIGLU}
 
@@ -43,13 +46,15 @@ class ColibriError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("num_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("act", ctypes.c_int32), ("has_router_bias", ctypes.c_int32), ("out_dtype", ctypes.c_int32)]
+                ("act", ctypes.c_int32), ("has_router_bias", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+                ("gate_mode", ctypes.c_int32), ("has_shared_expert", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
     _fields_ = [("w_router", ctypes.c_void_p), ("b_router", ctypes.c_void_p), ("w1", ctypes.c_void_p),
                 ("w3", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("b1", ctypes.c_void_p),
-                ("b2", ctypes.c_void_p)]
+                ("b2", ctypes.c_void_p), ("ws1", ctypes.c_void_p), ("ws3", ctypes.c_void_p),
+                ("ws2", ctypes.c_void_p), ("bs1", ctypes.c_void_p), ("bs2", ctypes.c_void_p)]
 
 
 _lib = None
@@ -126,11 +131,13 @@ class MoELayer:
     """One MoE layer instance (a ``colibri_moe_t`` context) on one GPU."""
 
     def __init__(self, d_model: int, d_ff: int, num_experts: int, max_tokens: int, dtype="bf16", act="swiglu",
-                 has_router_bias: bool = False, out_dtype="f32", device: int = 0):
-        self.cfg = Config(d_model, d_ff, num_experts, 2, max_tokens,
+                 has_router_bias: bool = False, out_dtype="f32", device: int = 0, top_k: int = 2,
+                 gate_mode="selected", shared_expert: bool = False):
+        self.cfg = Config(d_model, d_ff, num_experts, top_k, max_tokens,
                           _DTYPES[dtype] if isinstance(dtype, str) else int(dtype),
                           _ACTS[act] if isinstance(act, str) else int(act), int(bool(has_router_bias)),
-                          _DTYPES[out_dtype] if isinstance(out_dtype, str) else int(out_dtype))
+                          _DTYPES[out_dtype] if isinstance(out_dtype, str) else int(out_dtype),
+                          _GATES[gate_mode] if isinstance(gate_mode, str) else int(gate_mode), int(bool(shared_expert)))
         self.device = device
         self._h = ctypes.c_void_p()
         _check(lib().colibri_moe_create(ctypes.byref(self.cfg), device, ctypes.byref(self._h)), "colibri_moe_create")
@@ -162,8 +169,10 @@ class MoELayer:
 
     # -------------------------------------------------------------- calls
     def load_weights(self, w_router, w1: Sequence, w2: Sequence, w3: Optional[Sequence] = None, b_router=None,
-                     b1: Optional[Sequence] = None, b2: Optional[Sequence] = None, stream=None):
-        """Copy weights (host or device, dtype per config; biases fp32) into the device arena."""
+                     b1: Optional[Sequence] = None, b2: Optional[Sequence] = None, shared: Optional[dict] = None,
+                     stream=None):
+        """Copy weights (host or device, dtype per config; biases fp32) into the device arena.
+        shared: the shared expert's tensors, dict(w1=..., w3=..., w2=..., b1=..., b2=...)."""
         E = self.cfg.num_experts
 
         def parr(lst):
@@ -175,7 +184,9 @@ class MoELayer:
             self._keep.append(arr)
             return ctypes.cast(arr, ctypes.c_void_p).value
 
-        w = Weights(_ptr(w_router), _ptr(b_router), parr(w1), parr(w3), parr(w2), parr(b1), parr(b2))
+        sh = shared or {}
+        w = Weights(_ptr(w_router), _ptr(b_router), parr(w1), parr(w3), parr(w2), parr(b1), parr(b2),
+                    _ptr(sh.get("w1")), _ptr(sh.get("w3")), _ptr(sh.get("w2")), _ptr(sh.get("b1")), _ptr(sh.get("b2")))
         s = _stream_handle(stream) if stream is not None else None
         try:
             _check(lib().colibri_moe_load_weights(self._h, ctypes.byref(w), s), "colibri_moe_load_weights")
@@ -207,12 +218,12 @@ class MoELayer:
         """Routing of the last forward (T tokens) as CUDA tensors."""
         import torch
         dev = torch.device("cuda", self.device)
-        E = self.cfg.num_experts
-        r = dict(idx=torch.empty((T, 2), dtype=torch.int32, device=dev),
-                 gate=torch.empty((T, 2), dtype=torch.float32, device=dev),
+        E, k = self.cfg.num_experts, self.cfg.top_k
+        r = dict(idx=torch.empty((T, k), dtype=torch.int32, device=dev),
+                 gate=torch.empty((T, k), dtype=torch.float32, device=dev),
                  counts=torch.empty(E, dtype=torch.int32, device=dev),
                  offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
-                 row_of=torch.empty((T, 2), dtype=torch.int32, device=dev))
+                 row_of=torch.empty((T, k), dtype=torch.int32, device=dev))
         _check(lib().colibri_moe_get_routing(self._h, _ptr(r["idx"]), _ptr(r["gate"]), _ptr(r["counts"]),
                                              _ptr(r["offsets"]), _ptr(r["row_of"]), _stream_handle(stream)),
                "colibri_moe_get_routing")

@@ -38,6 +38,9 @@ struct colibri_moe {
   size_t esize = 0;         // bytes per element of x and weights
   size_t out_esize = 0;
   int n_up = 0;             // weight rows per expert of the up projection (2f SwiGLU bf16, f otherwise)
+  int k = 2;                // routed experts per token
+  int S = 2;                // rows per token: k routed (+1 shared)
+  int Ex = 0;               // scheduled experts: E routed (+1 shared, index E)
 
   // weight arena (one allocation, every block 256-byte aligned)
   void* warena = nullptr;
@@ -140,7 +143,11 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 
 int check_config(const colibri_moe_config_t* c) {
   if (!c) return COLIBRI_ERR_INVALID_ARG;
-  if (c->top_k != 2 || c->num_experts < 2 || c->num_experts > COLIBRI_MAX_EXPERTS) return COLIBRI_ERR_INVALID_ARG;
+  if (c->num_experts < 2 || c->num_experts > COLIBRI_MAX_EXPERTS) return COLIBRI_ERR_INVALID_ARG;
+  if (c->top_k < 1 || c->top_k > COLIBRI_MAX_TOP_K || c->top_k > c->num_experts) return COLIBRI_ERR_INVALID_ARG;
+  if ((c->gate_mode != COLIBRI_GATE_SOFTMAX_SELECTED && c->gate_mode != COLIBRI_GATE_SOFTMAX_ALL) ||
+      (c->has_shared_expert != 0 && c->has_shared_expert != 1))
+    return COLIBRI_ERR_INVALID_ARG;
   if (c->d_model <= 0 || c->d_ff <= 0 || c->max_tokens <= 0 || c->max_tokens > (1 << 24))
     return COLIBRI_ERR_INVALID_ARG;
   if ((c->dtype != COLIBRI_DTYPE_F32 && c->dtype != COLIBRI_DTYPE_BF16) ||
@@ -241,7 +248,11 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   c->esize = cfg->dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
   c->out_esize = cfg->out_dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
   c->n_up = (cfg->dtype == COLIBRI_DTYPE_BF16 && cfg->act == COLIBRI_ACT_SWIGLU) ? 2 * cfg->d_ff : cfg->d_ff;
-  c->rows_alloc = ((2 * T + (kRowTile - 1) * E) + kRowTile - 1) / kRowTile * kRowTile;
+  c->k = cfg->top_k;
+  c->S = cfg->top_k + cfg->has_shared_expert;
+  c->Ex = static_cast<int>(E) + cfg->has_shared_expert;
+  const int64_t S = c->S, Ex = c->Ex;
+  c->rows_alloc = ((S * T + (kRowTile - 1) * Ex) + kRowTile - 1) / kRowTile * kRowTile;
   c->nchunks_max = static_cast<int>((T + kRouterChunk - 1) / kRouterChunk);
   {
     // W_r columns staged per router pass: at most 96 KB of shared memory
@@ -261,19 +272,19 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   const size_t o_xp = carve(c->rows_alloc * d * c->esize);
   const size_t o_h = carve(c->rows_alloc * f * h_es);
   const size_t o_y = carve(c->rows_alloc * d * 4);
-  const size_t o_idx = carve(2 * T * 4);
-  const size_t o_gate = carve(2 * T * 4);
-  const size_t o_row = carve(2 * T * 4);
+  const size_t o_idx = carve(S * T * 4);
+  const size_t o_gate = carve(S * T * 4);
+  const size_t o_row = carve(S * T * 4);
   const size_t o_tok = carve(c->rows_alloc * 4);
-  const size_t o_hist = carve(static_cast<size_t>(c->nchunks_max) * E * 4);
+  const size_t o_hist = carve(static_cast<size_t>(c->nchunks_max) * Ex * 4);
   const size_t o_sched = carve(sizeof(Sched));
   // decode partial sums: bf16 layers whose batches can be decode-sized
   c->decode_max_t = cfg->dtype == COLIBRI_DTYPE_BF16 ? env_decode_max_t() : 0;
   if (c->decode_max_t > T) c->decode_max_t = static_cast<int>(T);
   const int64_t npad_max = (c->decode_max_t + 15) / 16 * 16;
   const int64_t part_floats = c->decode_max_t > 0
-                                  ? std::max<int64_t>(kDecodeSplitsUp * npad_max * E * c->n_up,
-                                                      kDecodeSplitsDown * npad_max * E * d)
+                                  ? std::max<int64_t>(kDecodeSplitsUp * npad_max * Ex * c->n_up,
+                                                      kDecodeSplitsDown * npad_max * Ex * d)
                                   : 0;
   const size_t o_part = carve(part_floats * 4);
   const size_t o_xs = carve(T * d * c->esize);
@@ -331,8 +342,9 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
 int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_weights_t* w, void* stream) {
   if (!ctx || !w) return COLIBRI_ERR_INVALID_ARG;
   const colibri_moe_config_t& c = ctx->cfg;
-  const int E = c.num_experts;
+  const int E = c.num_experts, Ex = ctx->Ex;
   const bool swiglu = c.act == COLIBRI_ACT_SWIGLU;
+  const bool shared = c.has_shared_expert != 0;
   // presence checks: every tensor the activation needs, and none it does not use
   if (!w->w_router || !w->w1 || !w->w2) return COLIBRI_ERR_BAD_WEIGHTS;
   if ((c.has_router_bias != 0) != (w->b_router != nullptr)) return COLIBRI_ERR_BAD_WEIGHTS;
@@ -342,6 +354,12 @@ int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_weights_t* w,
     if (!w->w1[e] || !w->w2[e]) return COLIBRI_ERR_BAD_WEIGHTS;
     if (swiglu && !w->w3[e]) return COLIBRI_ERR_BAD_WEIGHTS;
     if (!swiglu && (!w->b1[e] || !w->b2[e])) return COLIBRI_ERR_BAD_WEIGHTS;
+  }
+  if (shared) {
+    if (!w->ws1 || !w->ws2 || (swiglu && (!w->ws3 || w->bs1 || w->bs2)) || (!swiglu && (w->ws3 || !w->bs1 || !w->bs2)))
+      return COLIBRI_ERR_BAD_WEIGHTS;
+  } else if (w->ws1 || w->ws3 || w->ws2 || w->bs1 || w->bs2) {
+    return COLIBRI_ERR_BAD_WEIGHTS;
   }
   DeviceGuard g(ctx->device);
   if (!g.ok) return COLIBRI_ERR_CUDA;
@@ -355,11 +373,11 @@ int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_weights_t* w,
   };
   const size_t o_wr = carve(E * d * es);
   const size_t o_br = carve(E * 4);
-  const size_t o_w13 = carve(E * static_cast<size_t>(ctx->n_up) * d * es);
-  const size_t o_w3 = (swiglu && c.dtype == COLIBRI_DTYPE_F32) ? carve(E * f * d * es) : 0;
-  const size_t o_w2 = carve(E * d * f * es);
-  const size_t o_b1 = carve(E * f * 4);
-  const size_t o_b2 = carve(E * d * 4);
+  const size_t o_w13 = carve(Ex * static_cast<size_t>(ctx->n_up) * d * es);
+  const size_t o_w3 = (swiglu && c.dtype == COLIBRI_DTYPE_F32) ? carve(Ex * f * d * es) : 0;
+  const size_t o_w2 = carve(Ex * d * f * es);
+  const size_t o_b1 = carve(Ex * f * 4);
+  const size_t o_b2 = carve(Ex * d * 4);
   if (ctx->warena && ctx->warena_bytes != off) {
     cudaFree(ctx->warena);
     ctx->warena = nullptr;
@@ -385,25 +403,29 @@ int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_weights_t* w,
   if (ok && ctx->b_router)
     ok = cudaMemcpyAsync(ctx->b_router, w->b_router, E * 4, cudaMemcpyDefault, s) == cudaSuccess;
   const size_t mat = f * d * es;  // bytes of one [f, d] matrix
-  for (int e = 0; ok && e < E; ++e) {
+  // arena expert e < E: routed expert e; e == E: the shared expert
+  for (int e = 0; ok && e < Ex; ++e) {
+    const bool sh = e == E;
+    const void* W1 = sh ? w->ws1 : w->w1[e];
+    const void* W3 = sh ? w->ws3 : (swiglu ? w->w3[e] : nullptr);
+    const void* W2 = sh ? w->ws2 : w->w2[e];
+    const float* B1 = sh ? w->bs1 : (swiglu ? nullptr : w->b1[e]);
+    const float* B2 = sh ? w->bs2 : (swiglu ? nullptr : w->b2[e]);
     char* w13e = static_cast<char*>(ctx->w13) + static_cast<size_t>(e) * ctx->n_up * d * es;
     if (swiglu && c.dtype == COLIBRI_DTYPE_BF16) {
       // gate rows [128j, 128j+128) -> arena rows [256j, 256j+128); up rows -> [256j+128, 256j+256)
       const size_t blk = 128 * d * es;
-      ok = cudaMemcpy2DAsync(w13e, 2 * blk, w->w1[e], blk, blk, f / 128, cudaMemcpyDefault, s) == cudaSuccess &&
-           cudaMemcpy2DAsync(w13e + blk, 2 * blk, w->w3[e], blk, blk, f / 128, cudaMemcpyDefault, s) == cudaSuccess;
+      ok = cudaMemcpy2DAsync(w13e, 2 * blk, W1, blk, blk, f / 128, cudaMemcpyDefault, s) == cudaSuccess &&
+           cudaMemcpy2DAsync(w13e + blk, 2 * blk, W3, blk, blk, f / 128, cudaMemcpyDefault, s) == cudaSuccess;
     } else {
-      ok = cudaMemcpyAsync(w13e, w->w1[e], mat, cudaMemcpyDefault, s) == cudaSuccess;
+      ok = cudaMemcpyAsync(w13e, W1, mat, cudaMemcpyDefault, s) == cudaSuccess;
       if (ok && ctx->w3)
-        ok = cudaMemcpyAsync(static_cast<char*>(ctx->w3) + e * mat, w->w3[e], mat, cudaMemcpyDefault, s) ==
-             cudaSuccess;
+        ok = cudaMemcpyAsync(static_cast<char*>(ctx->w3) + e * mat, W3, mat, cudaMemcpyDefault, s) == cudaSuccess;
     }
-    if (ok)
-      ok = cudaMemcpyAsync(static_cast<char*>(ctx->w2) + e * mat, w->w2[e], mat, cudaMemcpyDefault, s) ==
-           cudaSuccess;
+    if (ok) ok = cudaMemcpyAsync(static_cast<char*>(ctx->w2) + e * mat, W2, mat, cudaMemcpyDefault, s) == cudaSuccess;
     if (ok && !swiglu)
-      ok = cudaMemcpyAsync(ctx->b1 + e * f, w->b1[e], f * 4, cudaMemcpyDefault, s) == cudaSuccess &&
-           cudaMemcpyAsync(ctx->b2 + e * d, w->b2[e], d * 4, cudaMemcpyDefault, s) == cudaSuccess;
+      ok = cudaMemcpyAsync(ctx->b1 + e * f, B1, f * 4, cudaMemcpyDefault, s) == cudaSuccess &&
+           cudaMemcpyAsync(ctx->b2 + e * d, B2, d * 4, cudaMemcpyDefault, s) == cudaSuccess;
   }
   if (ok) ok = cudaStreamSynchronize(s) == cudaSuccess;
   if (!ok) {
@@ -412,10 +434,10 @@ int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_weights_t* w,
   }
   if (c.dtype == COLIBRI_DTYPE_BF16) {
     const int bn = tc_gemm_block_n();
-    if (!make_tmap(&ctx->tm_w13, ctx->w13, d, static_cast<uint64_t>(E) * ctx->n_up, bn) ||
-        !make_tmap(&ctx->tm_w2, ctx->w2, f, static_cast<uint64_t>(E) * d, bn) ||
-        !make_tmap(&ctx->tm_w13_dec, ctx->w13, d, static_cast<uint64_t>(E) * ctx->n_up, kRowTile) ||
-        !make_tmap(&ctx->tm_w2_dec, ctx->w2, f, static_cast<uint64_t>(E) * d, kRowTile))
+    if (!make_tmap(&ctx->tm_w13, ctx->w13, d, static_cast<uint64_t>(Ex) * ctx->n_up, bn) ||
+        !make_tmap(&ctx->tm_w2, ctx->w2, f, static_cast<uint64_t>(Ex) * d, bn) ||
+        !make_tmap(&ctx->tm_w13_dec, ctx->w13, d, static_cast<uint64_t>(Ex) * ctx->n_up, kRowTile) ||
+        !make_tmap(&ctx->tm_w2_dec, ctx->w2, f, static_cast<uint64_t>(Ex) * d, kRowTile))
       return COLIBRI_ERR_CUDA;
   }
   ctx->loaded = true;
@@ -424,7 +446,7 @@ int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_weights_t* w,
 
 static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t T, cudaStream_t s) {
   const colibri_moe_config_t& c = ctx->cfg;
-  const int E = c.num_experts, d = c.d_model, f = c.d_ff;
+  const int E = ctx->Ex, d = c.d_model, f = c.d_ff;  // scheduled experts (routed + shared)
   const bool bf16 = c.dtype == COLIBRI_DTYPE_BF16;
   const bool swiglu = c.act == COLIBRI_ACT_SWIGLU;
   const bool timed = static_cast<int>(ctx->events.size()) == kNumStages + 1;
@@ -432,15 +454,16 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     if (timed && ctx->events[i]) cudaEventRecord(ctx->events[i], s);
   };
   const int nchunks = (T + kRouterChunk - 1) / kRouterChunk;
-  int64_t max_mtiles = (2 * static_cast<int64_t>(T) + (kRowTile - 1) * E) / kRowTile;
+  int64_t max_mtiles = (ctx->S * static_cast<int64_t>(T) + (kRowTile - 1) * E) / kRowTile;
   if (max_mtiles > ctx->rows_alloc / kRowTile) max_mtiles = ctx->rows_alloc / kRowTile;
 
   mark(0);
-  RouterArgs ra{x, ctx->w_router, ctx->b_router, T, d, E, ctx->dchunk, ctx->idx, ctx->gate, ctx->row_of,
-                ctx->hist, ctx->sched};
+  RouterArgs ra{x, ctx->w_router, ctx->b_router, T, d, c.num_experts, ctx->dchunk, ctx->idx, ctx->gate,
+                ctx->row_of, ctx->hist, ctx->sched, ctx->k, c.gate_mode, c.has_shared_expert, ctx->S, ctx->Ex};
   if (launch_router(c.dtype, ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   mark(1);
-  GatherArgs ga{x, ctx->idx, ctx->row_of, ctx->hist, T, d, E, ctx->rows_alloc, ctx->xp, ctx->tok_of_row, ctx->sched};
+  GatherArgs ga{x, ctx->idx, ctx->row_of, ctx->hist, T, d, E, ctx->S, ctx->rows_alloc, ctx->xp, ctx->tok_of_row,
+                ctx->sched};
   if (launch_gather(c.dtype, ga, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   mark(2);
   if (bf16 && T <= ctx->decode_max_t) {
@@ -461,7 +484,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
       return COLIBRI_ERR_CUDA;
     mark(4);
     DecodeCombineArgs cb{ctx->sched, E, f, n_pad, kDecodeSplitsDown, ctx->num_sms, d, T, ctx->partial, ctx->b2,
-                         ctx->idx, ctx->row_of, ctx->gate, out};
+                         ctx->idx, ctx->row_of, ctx->gate, out, ctx->S};
     if (launch_decode_combine(c.out_dtype, cb, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
     mark(5);
     ctx->last_T = T;
@@ -508,7 +531,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     if (launch_simt_gemm(kEpiStoreF32, dn, static_cast<int>(max_mtiles), s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   }
   mark(4);
-  CombineArgs ca{ctx->y, ctx->row_of, ctx->gate, T, d, out};
+  CombineArgs ca{ctx->y, ctx->row_of, ctx->gate, T, d, out, ctx->S};
   if (launch_combine(c.out_dtype, ca, ctx->num_sms, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   mark(5);
   ctx->last_T = T;
@@ -567,11 +590,15 @@ int colibri_moe_get_routing(colibri_moe_t* ctx, int32_t* idx, float* gate, int32
   if (!g.ok) return COLIBRI_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t T = static_cast<size_t>(ctx->last_T), E = ctx->cfg.num_experts;
+  const size_t k = ctx->k, S = ctx->S;
   bool ok = true;
-  if (idx && T) ok = ok && cudaMemcpyAsync(idx, ctx->idx, 2 * T * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
-  if (gate && T) ok = ok && cudaMemcpyAsync(gate, ctx->gate, 2 * T * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
-  if (row_of && T)
-    ok = ok && cudaMemcpyAsync(row_of, ctx->row_of, 2 * T * 4, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+  // the routed slots [T, k] of the internal [T, S] arrays (slot k is the shared expert)
+  auto copy_slots = [&](void* dst, const void* src) {
+    return cudaMemcpy2DAsync(dst, k * 4, src, S * 4, k * 4, T, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+  };
+  if (idx && T) ok = ok && copy_slots(idx, ctx->idx);
+  if (gate && T) ok = ok && copy_slots(gate, ctx->gate);
+  if (row_of && T) ok = ok && copy_slots(row_of, ctx->row_of);
   if (T == 0) {
     if (counts) ok = ok && cudaMemsetAsync(counts, 0, E * 4, s) == cudaSuccess;
     if (offsets) ok = ok && cudaMemsetAsync(offsets, 0, (E + 1) * 4, s) == cudaSuccess;

@@ -1,9 +1,10 @@
-// Gate-weighted combine: out[t] = g[t,0] * Y[row_of[t,0]] + g[t,1] * Y[row_of[t,1]] in fp32.
+// Gate-weighted combine: out[t] = sum over the token's slots s of g[t,s] * Y[row_of[t,s]] in fp32
+// (k routed experts, then the shared expert with gate 1 when the layer has one).
 //
 // m.nxbn.cn/news/48047 3.3 ("output aggregation": expert outputs summed with their gating
 // scores); hnwysp.cn/news/30485 2.2 (a token's two expert outputs weighted like [0.6, 0.4]).
-// Slot 0 is multiplied and added first, each product rounded to fp32, then the sum rounded once
-// (fp32 addition of two terms is commutative, so the result does not depend on slot order).
+// Slots are accumulated in order, each product and each partial sum rounded to fp32 (for two slots
+// the result is g0*y0 + g1*y1 rounded once, independent of order).
 //
 // HBM-bound: per token 2 * d * 4 bytes read, d * sizeof(out) written; float4 loads, coalesced
 // 16-byte (fp32) or 8-byte (bf16) stores; one CTA per token row, grid-strided.
@@ -19,18 +20,29 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
   const int nvec = a.d / 4;
   pdl_trigger();
   pdl_wait();
+  const int S = a.S;
   for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
-    const int r0 = a.row_of[2 * (size_t)t], r1 = a.row_of[2 * (size_t)t + 1];
-    const float g0 = a.gate[2 * (size_t)t], g1 = a.gate[2 * (size_t)t + 1];
-    const float4* y0 = reinterpret_cast<const float4*>(a.y + (size_t)r0 * a.d);
-    const float4* y1 = reinterpret_cast<const float4*>(a.y + (size_t)r1 * a.d);
+    int r[kMaxSlots];
+    float g[kMaxSlots];
+#pragma unroll
+    for (int s = 0; s < kMaxSlots; ++s) {
+      r[s] = s < S ? a.row_of[(size_t)S * t + s] : 0;
+      g[s] = s < S ? a.gate[(size_t)S * t + s] : 0.f;
+    }
     for (int i = threadIdx.x; i < nvec; i += kCombineThreads) {
-      const float4 u = __ldcs(y0 + i), v = __ldcs(y1 + i);
-      float4 o;
-      o.x = __fadd_rn(__fmul_rn(g0, u.x), __fmul_rn(g1, v.x));
-      o.y = __fadd_rn(__fmul_rn(g0, u.y), __fmul_rn(g1, v.y));
-      o.z = __fadd_rn(__fmul_rn(g0, u.z), __fmul_rn(g1, v.z));
-      o.w = __fadd_rn(__fmul_rn(g0, u.w), __fmul_rn(g1, v.w));
+      // slot order: o = g0*y0, then o += g_s*y_s; each product and each sum rounded once in fp32
+      const float4 u = __ldcs(reinterpret_cast<const float4*>(a.y + (size_t)r[0] * a.d) + i);
+      float4 o = make_float4(__fmul_rn(g[0], u.x), __fmul_rn(g[0], u.y), __fmul_rn(g[0], u.z), __fmul_rn(g[0], u.w));
+#pragma unroll
+      for (int s = 1; s < kMaxSlots; ++s) {
+        if (s < S) {
+          const float4 v = __ldcs(reinterpret_cast<const float4*>(a.y + (size_t)r[s] * a.d) + i);
+          o.x = __fadd_rn(o.x, __fmul_rn(g[s], v.x));
+          o.y = __fadd_rn(o.y, __fmul_rn(g[s], v.y));
+          o.z = __fadd_rn(o.z, __fmul_rn(g[s], v.z));
+          o.w = __fadd_rn(o.w, __fmul_rn(g[s], v.w));
+        }
+      }
       if constexpr (kBf16Out) {
         __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
         uint2 p;

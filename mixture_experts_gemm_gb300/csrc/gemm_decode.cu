@@ -305,7 +305,8 @@ __global__ void __launch_bounds__(256) decode_act_kernel(DecodeActArgs a) {
                             static_cast<size_t>(a.sched->offsets[e] + tok) * f + c) = o;
 }
 
-// Down projection + combine: out[t, c] = g0 * (sum_s P[s][slot0][e0 rows] (+ b2)) + g1 * (... e1 ...).
+// Down projection + combine: out[t, c] = sum over the token's slots k, in order, of
+// g_k * (sum over K splits of P[split][row slot][e_k rows] (+ b2)).
 template <bool kBf16Out>
 __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeCombineArgs a) {
   __shared__ int s_act[kMaxE];
@@ -322,11 +323,13 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeCombineArgs a
   const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (c >= a.d) return;
   const size_t rows_total = static_cast<size_t>(a.E) * a.d;
-  float y[2][4];
+  const int Sl = a.S;
+  float o[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int e = a.idx[2 * t + k];
-    const int slot = a.row_of[2 * t + k] - a.sched->offsets[e];
+  for (int k = 0; k < kMaxSlots; ++k) {
+    if (k >= Sl) break;
+    const int e = a.idx[Sl * t + k];
+    const int slot = a.row_of[Sl * t + k] - a.sched->offsets[e];
     const size_t grow = static_cast<size_t>(e) * a.d + c;
     // all splits' partials requested before the (split-ordered) sum
     float4 p[kDecodeSplitsDown];
@@ -345,12 +348,11 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeCombineArgs a
       const float* b = a.bias + grow;
       v.x += b[0]; v.y += b[1]; v.z += b[2]; v.w += b[3];
     }
-    y[k][0] = v.x; y[k][1] = v.y; y[k][2] = v.z; y[k][3] = v.w;
-  }
-  const float g0 = a.gate[2 * t], g1 = a.gate[2 * t + 1];
-  float o[4];
+    const float gk = a.gate[Sl * t + k];
+    const float y[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) o[i] = __fadd_rn(__fmul_rn(g0, y[0][i]), __fmul_rn(g1, y[1][i]));
+    for (int i = 0; i < 4; ++i) o[i] = k == 0 ? __fmul_rn(gk, y[i]) : __fadd_rn(o[i], __fmul_rn(gk, y[i]));
+  }
   if constexpr (kBf16Out) {
     uint2 p;
     p.x = pack_bf16(o[0], o[1]);

@@ -10,7 +10,10 @@
 
 namespace colibri {
 
-constexpr int kMaxE = 16;            // experts per layer (upper bound)
+constexpr int kMaxRouted = 16;       // routed experts per layer (upper bound)
+constexpr int kMaxE = kMaxRouted + 1;  // scheduled experts: routed + the optional shared expert
+constexpr int kMaxTopK = 4;
+constexpr int kMaxSlots = kMaxTopK + 1;  // rows per token: its k routed experts + the shared expert
 constexpr int kRowTile = 128;        // expert row segments start on multiples of this (GEMM M tile)
 constexpr int kRouterChunk = 32;     // tokens per router CTA (4 per warp)
 constexpr int kRouterThreads = 256;
@@ -41,21 +44,27 @@ struct RouterArgs {
   const void* x;           // [T, d] dtype
   const void* w_router;    // [E, d] dtype
   const float* b_router;   // [E] or nullptr
-  int T, d, E;
+  int T, d, E;             // E = routed experts
   int dchunk;              // columns of W_r staged in shared memory per pass
-  int32_t* idx;            // [T, 2]
-  float* gate;             // [T, 2]
-  int32_t* rank;           // [T, 2] rank inside the router chunk; rewritten to the row by gather
-  int32_t* hist;           // [nchunks, E] counts per chunk, rewritten to first row per (chunk, expert)
+  int32_t* idx;            // [T, S]
+  float* gate;             // [T, S]
+  int32_t* rank;           // [T, S] rank inside the router chunk; rewritten to the row by gather
+  int32_t* hist;           // [nchunks, Ex] counts per chunk, rewritten to first row per (chunk, expert)
   Sched* sched;
+  int k;                   // routed experts per token (1..4)
+  int gate_mode;           // 0 softmax over the selected experts, 1 full softmax
+  int shared;              // 1: slot k of every token is the shared expert (index E, gate 1)
+  int S;                   // slots per token = k + shared
+  int Ex;                  // scheduled experts = E + shared
 };
 
 struct GatherArgs {
   const void* x;           // [T, d]
-  const int32_t* idx;      // [T, 2]
-  int32_t* row_of;         // [T, 2] in: rank in chunk, out: row
-  const int32_t* chunk_base;  // [nchunks, E]
-  int T, d, E;
+  const int32_t* idx;      // [T, S]
+  int32_t* row_of;         // [T, S] in: rank in chunk, out: row
+  const int32_t* chunk_base;  // [nchunks, Ex]
+  int T, d, E;             // E = scheduled experts (Ex)
+  int S;
   int64_t rows_alloc;
   void* xp;                // [rows_alloc, d]
   int32_t* token_of_row;   // [rows_alloc]
@@ -64,10 +73,11 @@ struct GatherArgs {
 
 struct CombineArgs {
   const float* y;          // [rows, d] fp32
-  const int32_t* row_of;   // [T, 2]
-  const float* gate;       // [T, 2]
+  const int32_t* row_of;   // [T, S]
+  const float* gate;       // [T, S]
   int T, d;
   void* out;               // [T, d] fp32 or bf16
+  int S;
 };
 
 enum GemmEpilogue : int {
@@ -119,10 +129,11 @@ struct DecodeCombineArgs {
   int d, T;
   const float* partial;     // down-projection partials, rows = E * d
   const float* bias;        // b2 [E, d] or nullptr
-  const int32_t* idx;
-  const int32_t* row_of;
-  const float* gate;
+  const int32_t* idx;       // [T, S]
+  const int32_t* row_of;    // [T, S]
+  const float* gate;        // [T, S]
   void* out;
+  int S;
 };
 
 // fp32 SIMT grouped GEMM operands (row-major, K contiguous)

@@ -25,20 +25,25 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherArgs a, in
   pdl_wait();
   if (t >= a.T) return;
   const int chunk = t / kRouterChunk;
-  int r[2];
+  const int S = a.S;
+  int r[kMaxSlots];
+  bool ok = true;
 #pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    const int e = a.idx[2 * (size_t)t + s];
-    r[s] = a.chunk_base[(size_t)chunk * a.E + e] + a.row_of[2 * (size_t)t + s];
+  for (int s = 0; s < kMaxSlots; ++s) {
+    r[s] = 0;
+    if (s < S) {
+      const int e = a.idx[(size_t)S * t + s];
+      r[s] = a.chunk_base[(size_t)chunk * a.E + e] + a.row_of[(size_t)S * t + s];
+      ok = ok && r[s] >= 0 && r[s] < a.rows_alloc;
+    }
   }
-  const bool ok = r[0] >= 0 && r[0] < a.rows_alloc && r[1] >= 0 && r[1] < a.rows_alloc;
   __syncwarp();
   if (lane == 0 && part == 0) {
     if (ok) {
-      a.row_of[2 * (size_t)t] = r[0];
-      a.row_of[2 * (size_t)t + 1] = r[1];
-      a.token_of_row[r[0]] = t;
-      a.token_of_row[r[1]] = t;
+      for (int s = 0; s < S; ++s) {
+        a.row_of[(size_t)S * t + s] = r[s];
+        a.token_of_row[r[s]] = t;
+      }
     } else {
       atomicOr(&a.sched->status, kStatusBadRow);
     }
@@ -48,18 +53,28 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherArgs a, in
   const int nvec = (int)(row_bytes / 16);
   const int v0 = (nvec * part) / wpt, v1 = (nvec * (part + 1)) / wpt;
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(a.x) + (size_t)t * row_bytes);
-  uint4* d0 = reinterpret_cast<uint4*>(static_cast<char*>(a.xp) + (size_t)r[0] * row_bytes);
-  uint4* d1 = reinterpret_cast<uint4*>(static_cast<char*>(a.xp) + (size_t)r[1] * row_bytes);
-  int i = v0 + lane;
-  for (; i + 96 < v1; i += 128) {
-    uint4 q0 = __ldg(src + i), q1 = __ldg(src + i + 32), q2 = __ldg(src + i + 64), q3 = __ldg(src + i + 96);
-    d0[i] = q0; d0[i + 32] = q1; d0[i + 64] = q2; d0[i + 96] = q3;
-    d1[i] = q0; d1[i + 32] = q1; d1[i + 64] = q2; d1[i + 96] = q3;
-  }
-  for (; i < v1; i += 32) {
-    uint4 q = __ldg(src + i);
-    d0[i] = q;
-    d1[i] = q;
+  char* xp = static_cast<char*>(a.xp);
+  if (S == 2) {
+    uint4* d0 = reinterpret_cast<uint4*>(xp + (size_t)r[0] * row_bytes);
+    uint4* d1 = reinterpret_cast<uint4*>(xp + (size_t)r[1] * row_bytes);
+    int i = v0 + lane;
+    for (; i + 96 < v1; i += 128) {
+      uint4 q0 = __ldg(src + i), q1 = __ldg(src + i + 32), q2 = __ldg(src + i + 64), q3 = __ldg(src + i + 96);
+      d0[i] = q0; d0[i + 32] = q1; d0[i + 64] = q2; d0[i + 96] = q3;
+      d1[i] = q0; d1[i + 32] = q1; d1[i + 64] = q2; d1[i + 96] = q3;
+    }
+    for (; i < v1; i += 32) {
+      uint4 q = __ldg(src + i);
+      d0[i] = q;
+      d1[i] = q;
+    }
+  } else {
+    for (int i = v0 + lane; i < v1; i += 32) {
+      const uint4 q = __ldg(src + i);
+#pragma unroll
+      for (int s = 0; s < kMaxSlots; ++s)
+        if (s < S) reinterpret_cast<uint4*>(xp + (size_t)r[s] * row_bytes)[i] = q;
+    }
   }
 }
 

@@ -77,7 +77,7 @@ extern "C" int colibri_moe_route_noalloc(const void* x, const void* w_router, co
                                          float* gate, int32_t* counts, int32_t* offsets, int32_t* row_of,
                                          void* stream) {
   if (T < 0 || T > kNoAllocMaxTokens) return COLIBRI_ERR_INVALID_ARG;
-  if (num_experts < 2 || num_experts > kMaxE || d_model <= 0) return COLIBRI_ERR_INVALID_ARG;
+  if (num_experts < 2 || num_experts > kMaxRouted || d_model <= 0) return COLIBRI_ERR_INVALID_ARG;
   if (dtype != COLIBRI_DTYPE_F32 && dtype != COLIBRI_DTYPE_BF16) return COLIBRI_ERR_INVALID_ARG;
   if (d_model % 8) return COLIBRI_ERR_UNSUPPORTED;
   if (!counts || !offsets || (T > 0 && (!x || !w_router || !idx || !gate || !row_of))) return COLIBRI_ERR_INVALID_ARG;
@@ -119,7 +119,7 @@ extern "C" int colibri_moe_route_noalloc(const void* x, const void* w_router, co
   int dchunk = kRouterMaxSmem / (emax * esize) / vec_span * vec_span;
   if (d_model < dchunk) dchunk = d_model;
   const int nchunks = (T + kRouterChunk - 1) / kRouterChunk;
-  RouterArgs ra{x, w_router, b_router, T, d_model, E, dchunk, idx, gate, row_of, hist, sched};
+  RouterArgs ra{x, w_router, b_router, T, d_model, E, dchunk, idx, gate, row_of, hist, sched, 2, 0, 0, 2, E};
   if (launch_router(dtype, ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   const int threads = 256;
   route_rows_kernel<<<(2 * T + threads - 1) / threads, threads, 0, s>>>(idx, row_of, hist, sched, T, E, counts,

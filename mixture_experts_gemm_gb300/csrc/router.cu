@@ -52,7 +52,7 @@ struct Vec<__nv_bfloat16> {
 __device__ void scan_offsets(const RouterArgs& a, int nchunks) {
   constexpr int NW = kRouterThreads / 32;
   __shared__ int s_wsum[NW][kMaxE];
-  const int E = a.E;
+  const int E = a.Ex;  // scheduled experts: routed (+ shared)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int per = (nchunks + kRouterThreads - 1) / kRouterThreads;
   const int c0 = min((int)threadIdx.x * per, nchunks), c1 = min(c0 + per, nchunks);
@@ -121,24 +121,27 @@ __device__ void scan_offsets(const RouterArgs& a, int nchunks) {
   }
 }
 
-// After the chunk's top-2 is in s_idx (a __syncthreads() ago): in-chunk ranks, the chunk's expert
-// histogram, and -- in the CTA that finishes last -- the scan of all histograms.
-__device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[2], int valid, int chunk_t0) {
+// After the chunk's routing is in s_idx (a __syncthreads() ago): in-chunk ranks, the chunk's expert
+// histogram, and -- in the CTA that finishes last -- the scan of all histograms.  S slots per token
+// (k routed experts, then the shared expert when present); a token names each expert at most once.
+__device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[kMaxSlots], int valid, int chunk_t0) {
   __shared__ int s_last;
-  const int E = a.E;
-  if (threadIdx.x < 2 * kRouterChunk) {
-    const int tt = threadIdx.x >> 1, s = threadIdx.x & 1;
+  const int Ex = a.Ex, S = a.S;
+  if (threadIdx.x < S * kRouterChunk) {
+    const int tt = threadIdx.x / S, s = threadIdx.x - tt * S;
     if (tt < valid) {
       const int e = s_idx[tt][s];
       int r = 0;
-      for (int u = 0; u < tt; ++u) r += (s_idx[u][0] == e) + (s_idx[u][1] == e);
-      a.rank[2 * (size_t)(chunk_t0 + tt) + s] = r;
+      for (int u = 0; u < tt; ++u)
+        for (int q = 0; q < S; ++q) r += (s_idx[u][q] == e);
+      a.rank[(size_t)S * (chunk_t0 + tt) + s] = r;
     }
   }
-  if (threadIdx.x < E) {
+  if (threadIdx.x < Ex) {
     int c = 0;
-    for (int u = 0; u < valid; ++u) c += (s_idx[u][0] == (int)threadIdx.x) + (s_idx[u][1] == (int)threadIdx.x);
-    a.hist[(size_t)blockIdx.x * E + threadIdx.x] = c;
+    for (int u = 0; u < valid; ++u)
+      for (int q = 0; q < S; ++q) c += (s_idx[u][q] == (int)threadIdx.x);
+    a.hist[(size_t)blockIdx.x * Ex + threadIdx.x] = c;
   }
   __threadfence();
   __syncthreads();
@@ -150,28 +153,63 @@ __device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[2], int val
   }
 }
 
-// Top-2 of one token's logits (strict > keeps the lower index on ties) and its pair-softmax gates.
+// Top-k of one token's logits (strict > keeps the lower index on ties) and its gates:
+// softmax over the selected experts (k = 2: g_a = 1 / (1 + e^{L_b - L_a}), g_b = 1 - g_a), or the
+// full softmax over all experts at the selected ones (gate_mode 1).  The shared expert, when
+// present, takes slot k with gate 1.
 template <int EMAX>
-__device__ __forceinline__ void top2_store(const RouterArgs& a, const float (&L)[EMAX], int t, int (&sidx)[2]) {
-  const int E = a.E;
-  int ia = 0;
-  float la = L[0];
+__device__ __forceinline__ void topk_store(const RouterArgs& a, const float (&L)[EMAX], int t, int* sidx) {
+  const int E = a.E, k = a.k;
+  int sel[kMaxTopK];
+  float ls[kMaxTopK];
+  uint32_t used = 0;
 #pragma unroll
-  for (int e = 1; e < EMAX; ++e)
-    if (e < E && L[e] > la) { la = L[e]; ia = e; }
-  int ib = -1;
-  float lb = 0.f;
+  for (int j = 0; j < kMaxTopK; ++j) {
+    int best = -1;
+    float lbest = 0.f;
+    if (j < k) {
 #pragma unroll
-  for (int e = 0; e < EMAX; ++e)
-    if (e < E && e != ia && (ib < 0 || L[e] > lb)) { lb = L[e]; ib = e; }
-  sidx[0] = ia;
-  sidx[1] = ib;
+      for (int e = 0; e < EMAX; ++e)
+        if (e < E && !((used >> e) & 1u) && (best < 0 || L[e] > lbest)) { lbest = L[e]; best = e; }
+      used |= 1u << best;
+    }
+    sel[j] = best;
+    ls[j] = lbest;
+  }
+  float g[kMaxTopK];
+  if (a.gate_mode == 0 && k == 2) {
+    g[0] = 1.0f / (1.0f + expf(ls[1] - ls[0]));
+    g[1] = 1.0f - g[0];
+  } else {
+    float den = 0.f;
+    if (a.gate_mode == 0) {
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j)
+        if (j < k) den += expf(ls[j] - ls[0]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e)
+        if (e < E) den += expf(L[e] - ls[0]);
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) g[j] = j < k ? expf(ls[j] - ls[0]) / den : 0.f;
+  }
+  const int S = a.S;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (j < k) sidx[j] = sel[j];
+  if (a.shared) sidx[k] = E;
   if (t < a.T) {
-    const float ga = 1.0f / (1.0f + expf(lb - la));
-    a.idx[2 * (size_t)t] = ia;
-    a.idx[2 * (size_t)t + 1] = ib;
-    a.gate[2 * (size_t)t] = ga;
-    a.gate[2 * (size_t)t + 1] = 1.0f - ga;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) {
+        a.idx[(size_t)S * t + j] = sel[j];
+        a.gate[(size_t)S * t + j] = g[j];
+      }
+    if (a.shared) {
+      a.idx[(size_t)S * t + k] = E;
+      a.gate[(size_t)S * t + k] = 1.0f;
+    }
   }
 }
 
@@ -183,7 +221,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_top2_kernel(RouterArgs 
   constexpr int SPAN = 32 * VEC;                // columns one warp covers per iteration
   constexpr int NW = kRouterThreads / 32;       // warps per CTA
   Tin* wsm = reinterpret_cast<Tin*>(smem_raw);
-  __shared__ int s_idx[kRouterChunk][2];
+  __shared__ int s_idx[kRouterChunk][kMaxSlots];
   __shared__ float s_part[NW][4][EMAX];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -297,7 +335,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_top2_kernel(RouterArgs 
       for (int q = 1; q < S; ++q) v += s_part[g + q * G][k][e];
       L[e] = v + ((a.b_router != nullptr && e < E) ? a.b_router[e] : 0.f);
     }
-    top2_store<EMAX>(a, L, t, s_idx[g * 4 + k]);
+    topk_store<EMAX>(a, L, t, s_idx[g * 4 + k]);
   }
   __syncthreads();
   finish_chunk(a, s_idx, valid, chunk_t0);
@@ -314,7 +352,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_top2_mma_kernel(RouterA
   constexpr int EMAX = 8 * NT;
   constexpr int UNR = 8;
   __shared__ float s_part[NW][16][EMAX];
-  __shared__ int s_idx[kRouterChunk][2];
+  __shared__ int s_idx[kRouterChunk][kMaxSlots];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk_t0 = blockIdx.x * kRouterChunk;
@@ -394,7 +432,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_top2_mma_kernel(RouterA
         for (int s2 = 1; s2 < S; ++s2) v += s_part[hh + s2 * H][r][e];
         L[e] = v + ((a.b_router != nullptr && e < E) ? a.b_router[e] : 0.f);
       }
-      top2_store<EMAX>(a, L, chunk_t0 + tt, s_idx[tt]);
+      topk_store<EMAX>(a, L, chunk_t0 + tt, s_idx[tt]);
     }
   }
   __syncthreads();

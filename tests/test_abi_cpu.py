@@ -48,7 +48,8 @@ def _cfg(m, **kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(top_k=1), -1), (dict(num_experts=1), -1), (dict(num_experts=17), -1), (dict(max_tokens=0), -1),
+    (dict(top_k=0), -1), (dict(top_k=5), -1), (dict(num_experts=2, top_k=3), -1), (dict(gate_mode=2), -1),
+    (dict(has_shared_expert=2), -1), (dict(num_experts=1), -1), (dict(num_experts=17), -1), (dict(max_tokens=0), -1),
     (dict(d_model=0), -1), (dict(dtype=5), -1), (dict(act=9), -1), (dict(out_dtype=3), -1),
     (dict(has_router_bias=2), -1), (dict(d_model=260), -6), (dict(d_ff=200), -6),
     (dict(act=0, d_ff=384), -6), (dict(dtype=0, d_model=12), -6),

@@ -37,7 +37,8 @@ def _full_check(li, T=None, tol=None, out_dtype="f32", layer=None):
     out, r = run(layer, x)
     L = oracle.OracleLayer.from_inputs(li)
     ref = L.forward(li.x_f32[:T])
-    check_routing(r, ref["logits"], ref["idx"], ref["gate"], s.num_experts, ref["row_of"], ref["offsets_raw"])
+    check_routing(r, ref["logits"], ref["idx"], ref["gate"], s.num_experts, ref["row_of"], ref["offsets_raw"],
+                  gate_mode=s.gate_mode)
     tol = tol if tol is not None else (TOL_F32 if s.dtype == "f32" else TOL_BF16)
     err = rel_err(out, ref["out"])
     assert err <= tol, f"max|err|/RMS = {err:.3e} > {tol}"
@@ -181,6 +182,37 @@ def test_single_cta_gemm_kernel(case, monkeypatch):
     else:
         _full_check(testgen.make_inputs(testgen.LayerShape("one-skewed", 1500, 512, 256, 16, testgen.ACT_SWIGLU,
                                                            "bf16", zipf_router_bias=True)))
+
+
+@pytest.mark.parametrize("T", [40, 700])
+@pytest.mark.parametrize("k,mode,shared", [(1, 0, False), (3, 0, False), (4, 1, False), (2, 1, False),
+                                           (2, 0, True), (4, 0, True), (1, 1, True)])
+def test_routing_variants_and_shared_expert_bf16(T, k, mode, shared):
+    """top-k 1..4, both gate modes, the shared expert: prefill (T=700) and decode (T=40) kernels."""
+    shape = testgen.LayerShape(f"var-k{k}-m{mode}-s{int(shared)}", T, 512, 384, 8, testgen.ACT_SWIGLU, "bf16",
+                               zipf_router_bias=True, top_k=k, gate_mode=mode, shared_expert=shared)
+    layer, out, r, ref, err = _full_check(testgen.make_inputs(shape))
+    if shared:
+        # the shared expert's segment holds every token, after the routed segments
+        off = r["offsets"]
+        tok = layer.debug_tensor(3).cpu().numpy()
+        assert np.array_equal(tok[off[-1]:off[-1] + T], np.arange(T))
+
+
+@pytest.mark.parametrize("k,mode,shared", [(1, 0, True), (3, 1, True), (4, 0, False)])
+def test_routing_variants_fp32(k, mode, shared):
+    shape = testgen.LayerShape("var-f32", 64, 256, 512, 4, testgen.ACT_RELU_BIAS, "f32", top_k=k, gate_mode=mode,
+                               shared_expert=shared)
+    _full_check(testgen.make_inputs(shape))
+
+
+def test_shared_expert_relu_bias_bf16_and_pair_kernel(monkeypatch):
+    shape = testgen.LayerShape("shared-relu", 600, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16", top_k=2,
+                               shared_expert=True)
+    li = testgen.make_inputs(shape)
+    _full_check(li)
+    monkeypatch.setenv("COLIBRI_MOE_GEMM", "1sm")
+    _full_check(li)
 
 
 def test_1p3b_workload():
