@@ -49,6 +49,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU work budget of the oracle baseline")
+    p.add_argument("--top-k", type=int, default=None, help="routed experts per token (default: the workload's, 2)")
+    p.add_argument("--gate-mode", type=int, default=None, help="0 softmax over the selected experts, 1 full softmax")
+    p.add_argument("--shared-expert", action="store_true", help="add an always-on shared expert")
     return p.parse_args()
 
 
@@ -63,18 +66,21 @@ def load_peaks():
 
 def workload_desc(s, T):
     act = "SwiGLU" if s.act == 1 else "ReLU+bias"
-    return (f"{s.name}: T={T} d_model={s.d_model} d_ff={s.d_ff} E={s.num_experts} top-2 {act} {s.dtype}"
-            + (" router-bias zipf" if s.zipf_router_bias else ""))
+    return (f"{s.name}: T={T} d_model={s.d_model} d_ff={s.d_ff} E={s.num_experts} top-{s.top_k} {act} {s.dtype}"
+            + (" router-bias zipf" if s.zipf_router_bias else "")
+            + (" full-softmax gates" if s.gate_mode == 1 else "")
+            + (" +1 shared expert" if s.shared_expert else ""))
 
 
 def algorithmic(s, T, active_experts=None):
     """FLOPs and bytes of one forward counting routed work only (no padding rows)."""
     n_up = 2 if s.act == 1 else 1
     es = 2 if s.dtype == "bf16" else 4
-    flops_up = 2.0 * (2 * T) * s.d_model * s.d_ff * n_up
-    flops_down = 2.0 * (2 * T) * s.d_model * s.d_ff
+    rows = (s.top_k + int(s.shared_expert)) * T          # routed rows (+ the shared expert's)
+    flops_up = 2.0 * rows * s.d_model * s.d_ff * n_up
+    flops_down = 2.0 * rows * s.d_model * s.d_ff
     flops_router = 2.0 * T * s.num_experts * s.d_model
-    n_act = s.num_experts if active_experts is None else active_experts
+    n_act = (s.num_experts if active_experts is None else active_experts) + int(s.shared_expert)
     w_bytes_expert = (n_up + 1) * s.d_model * s.d_ff * es
     bytes_total = n_act * w_bytes_expert + T * s.d_model * es + T * s.d_model * 4 + s.num_experts * s.d_model * es
     return dict(flops_up=flops_up, flops_down=flops_down, flops_router=flops_router,
@@ -212,8 +218,13 @@ def run_reference(args, shape, T):
 # ---------------------------------------------------------------------------------------- GPU arm
 def main():
     args = parse_args()
+    import dataclasses
     import testgen
     shape = testgen.CONFIGS[args.workload]
+    if args.top_k is not None or args.gate_mode is not None or args.shared_expert:
+        shape = dataclasses.replace(shape, top_k=args.top_k or shape.top_k,
+                                    gate_mode=shape.gate_mode if args.gate_mode is None else args.gate_mode,
+                                    shared_expert=args.shared_expert or shape.shared_expert)
     T = args.T if args.T is not None else shape.T
     if args.impl == "reference":
         run_reference(args, shape, T)
@@ -241,7 +252,8 @@ def main():
     li = testgen.make_inputs(shape.with_T(T), want_f32=shape.dtype == "f32")
     layer = moe.MoELayer(shape.d_model, shape.d_ff, shape.num_experts, T, dtype=shape.dtype,
                          act="swiglu" if shape.act == testgen.ACT_SWIGLU else "relu_bias",
-                         has_router_bias=shape.zipf_router_bias, out_dtype="f32", device=local)
+                         has_router_bias=shape.zipf_router_bias, out_dtype="f32", device=local, top_k=shape.top_k,
+                         gate_mode=shape.gate_mode, shared_expert=shape.shared_expert)
     layer.load_weights(**host_weights(li))
     x = x_device(li).to(dev)
     out = torch.empty((T, shape.d_model), dtype=torch.float32, device=dev)
@@ -348,8 +360,9 @@ def main():
         # weight streaming: bytes of the distinct active experts' weights this stage reads
         n_up = 2 if shape.act == 1 else 1
         es = 2 if shape.dtype == "bf16" else 4
-        byts = {2: active * n_up * shape.d_model * shape.d_ff * es,
-                3: active * shape.d_model * shape.d_ff * es}.get(dominant, alg["bytes"])
+        n_w = active + int(shape.shared_expert)
+        byts = {2: n_w * n_up * shape.d_model * shape.d_ff * es,
+                3: n_w * shape.d_model * shape.d_ff * es}.get(dominant, alg["bytes"])
         ach = byts / dur / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         roof = {"bound": "hbm", "kernel": STAGES[dominant], "achieved": ach, "peak": peak, "unit": "GB/s",
