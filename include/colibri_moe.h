@@ -170,7 +170,7 @@ COLIBRI_API int colibri_moe_device_status(colibri_moe_t* ctx, int32_t* status);
  * the same x and router weights: idx[T,2], gate[T,2], counts[E], offsets[E+1], row_of[T,2].
  *   x [T, d_model] and w_router [E, d_model] in `dtype` (16-byte aligned), b_router [E] fp32 or NULL.
  * It needs no context.  Its scratch (per-chunk histograms and the routing summary) is a fixed
- * __device__ array of about 129 KB inside the library, present on every GPU that loads the library
+ * __device__ array of about 137 KB inside the library, present on every GPU that loads the library
  * until the process exits; hence T <= 65536 (larger T returns COLIBRI_ERR_INVALID_ARG).  The first
  * call on a device looks up the array's device address and sets kernel attributes (host-side
  * set-up, no allocation); make that first call before any stream capture.  Every call on a device
