@@ -47,77 +47,66 @@ struct Vec<__nv_bfloat16> {
 };
 
 // Runs in the last router CTA: counts, padded offsets, M-tile prefix, and the first row of every
-// (chunk, expert) pair, written over the per-chunk counts.  All experts are scanned together (one
-// barrier), so the cost is a couple of memory round trips, not one per expert.
+// (chunk, expert) pair, written over the per-chunk counts.  Warp w scans experts w, w + 8, w + 16;
+// lane l of a warp owns a contiguous range of chunks, so one warp-wide scan gives every chunk's place
+// in chunk order.  Thread 0 then turns the expert totals into padded segment offsets.
 __device__ void scan_offsets(const RouterArgs& a, int nchunks) {
   constexpr int NW = kRouterThreads / 32;
-  __shared__ int s_wsum[NW][kMaxE];
+  constexpr int PER_WARP = (kMaxE + NW - 1) / NW;  // experts per warp
+  __shared__ int s_tot[kMaxE];
+  __shared__ int s_off[kMaxE + 1];
   const int E = a.Ex;  // scheduled experts: routed (+ shared)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int per = (nchunks + kRouterThreads - 1) / kRouterThreads;
-  const int c0 = min((int)threadIdx.x * per, nchunks), c1 = min(c0 + per, nchunks);
-  int local[kMaxE];
+  const int per = (nchunks + 31) / 32;
+  const int c0 = min(lane * per, nchunks), c1 = min(c0 + per, nchunks);
+  int excl[PER_WARP];
 #pragma unroll
-  for (int e = 0; e < kMaxE; ++e) local[e] = 0;
-  for (int c = c0; c < c1; ++c) {
-    int v[kMaxE];
+  for (int i = 0; i < PER_WARP; ++i) {
+    const int e = warp + i * NW;
+    excl[i] = 0;
+    if (e < E) {
+      int local = 0;
+      for (int c = c0; c < c1; ++c) local += __ldcg(&a.hist[(size_t)c * E + e]);
+      int inc = local;
 #pragma unroll
-    for (int e = 0; e < kMaxE; ++e) v[e] = e < E ? __ldcg(&a.hist[(size_t)c * E + e]) : 0;
-#pragma unroll
-    for (int e = 0; e < kMaxE; ++e) local[e] += v[e];
-  }
-  // inclusive warp scans of every expert's chunk counts, then warp totals through shared memory
-  int inc[kMaxE];
-#pragma unroll
-  for (int e = 0; e < kMaxE; ++e) {
-    inc[e] = local[e];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, inc[e], o);
-      if (lane >= o) inc[e] += n;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += n;
+      }
+      excl[i] = inc - local;
+      if (lane == 31) s_tot[e] = inc;
     }
-  }
-  if (lane == 31) {
-#pragma unroll
-    for (int e = 0; e < kMaxE; ++e) s_wsum[warp][e] = inc[e];
   }
   __syncthreads();
-  int off = 0, mt = 0;
-#pragma unroll
-  for (int e = 0; e < kMaxE; ++e) {
-    int pre = 0, tot = 0;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const int v = s_wsum[w][e];
-      pre += w < warp ? v : 0;
-      tot += v;
-    }
-    if (e < E) {
-      if (threadIdx.x == 0) {
-        a.sched->counts[e] = tot;
-        a.sched->offsets[e] = off;
-        a.sched->mtile_start[e] = mt;
-      }
-      // first row of each of this thread's chunks for expert e, in chunk order
-      int run = off + pre + inc[e] - local[e];
-      if (c1 - c0 == 1) {
-        a.hist[(size_t)c0 * E + e] = run;
-      } else {
-        for (int c = c0; c < c1; ++c) {
-          const int n = __ldcg(&a.hist[(size_t)c * E + e]);
-          a.hist[(size_t)c * E + e] = run;
-          run += n;
-        }
-      }
+  if (threadIdx.x == 0) {
+    int off = 0, mt = 0;
+    for (int e = 0; e < E; ++e) {
+      const int tot = s_tot[e];
+      s_off[e] = off;
+      a.sched->counts[e] = tot;
+      a.sched->offsets[e] = off;
+      a.sched->mtile_start[e] = mt;
       const int tiles = (tot + kRowTile - 1) / kRowTile;
       off += tiles * kRowTile;
       mt += tiles;
     }
-  }
-  if (threadIdx.x == 0) {
+    s_off[E] = off;
     a.sched->offsets[E] = off;
     a.sched->mtile_start[E] = mt;
     a.sched->ticket = 0;  // ready for the next forward
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < PER_WARP; ++i) {
+    const int e = warp + i * NW;
+    if (e < E) {
+      int run = s_off[e] + excl[i];
+      for (int c = c0; c < c1; ++c) {
+        const int n = __ldcg(&a.hist[(size_t)c * E + e]);
+        a.hist[(size_t)c * E + e] = run;
+        run += n;
+      }
+    }
   }
 }
 
@@ -347,10 +336,10 @@ __global__ void __launch_bounds__(kRouterThreads) router_top2_kernel(RouterArgs 
 // straight from x in global memory (every 32-byte sector a warp touches is used whole), B fragments
 // from W_r through L1/L2.  Partial tiles of the slices are summed in slice order in shared memory.
 template <int NT>
-__global__ void __launch_bounds__(kRouterThreads) router_top2_mma_kernel(RouterArgs a) {
+__global__ void __launch_bounds__(kRouterThreads, 2) router_top2_mma_kernel(RouterArgs a) {
   constexpr int NW = kRouterThreads / 32;
   constexpr int EMAX = 8 * NT;
-  constexpr int UNR = 8;
+  constexpr int UNR = NT == 1 ? 8 : 4;  // 32-column blocks in flight per warp
   __shared__ float s_part[NW][16][EMAX];
   __shared__ int s_idx[kRouterChunk][kMaxSlots];
 
@@ -376,40 +365,58 @@ __global__ void __launch_bounds__(kRouterThreads) router_top2_mma_kernel(RouterA
     wr[nt] = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.w_router) +
                                                (size_t)(wv[nt] ? nt * 8 + g : 0) * d);
   }
-  const int nks = d / 16;
-  const int ks0 = (nks * sl) / S, ks1 = (nks * (sl + 1)) / S;
+  // k is summed over, so any permutation of it applied to A and B alike gives the same product.  Per
+  // 32-column block, lane (g, q) loads columns 8q..8q+7 of its rows as one 16-byte vector and uses
+  // them as logical k {2q, 2q+1, 2q+8, 2q+9} of two consecutive k-steps: one load instruction per row
+  // per two MMAs, each instruction reading 64 contiguous bytes of 8 rows.
+  const int nblk = d / 32;
+  const int kb0 = (nblk * sl) / S, kb1 = (nblk * (sl + 1)) / S;
   pdl_trigger();
   pdl_wait();  // x may come from the previous kernel; the workspace from the previous forward
+  // one bulk L2 prefetch per token row of this warp's column range: only the first round of fragment
+  // loads below waits on HBM, the later rounds hit L2
+  if (lane < 16 && kb1 > kb0) {
+    const int row = r0 + lane;
+    if (row < T) {
+      const char* p = reinterpret_cast<const char*>(static_cast<const __nv_bfloat16*>(a.x) + (size_t)row * d +
+                                                    (size_t)kb0 * 32);
+      const uint32_t bytes = static_cast<uint32_t>(kb1 - kb0) * 64u;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+    }
+  }
   float acc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 
-  for (int ks = ks0; ks < ks1; ks += UNR) {
-    uint32_t A[UNR][4], B[UNR][NT][2];
+  for (int kb = kb0; kb < kb1; kb += UNR) {
+    uint4 A0[UNR], A1[UNR], B[UNR][NT];
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
-      const int c = (ks + u) * 8 + q;  // 32-bit word holding columns 2q, 2q+1 of this k-step
-      const bool in = ks + u < ks1;
-      A[u][0] = (in && v0) ? __ldg(x0 + c) : 0u;
-      A[u][1] = (in && v1) ? __ldg(x1 + c) : 0u;
-      A[u][2] = (in && v0) ? __ldg(x0 + c + 4) : 0u;
-      A[u][3] = (in && v1) ? __ldg(x1 + c + 4) : 0u;
+      const int vi = 4 * (kb + u) + q;  // 16-byte vector holding columns 32*(kb+u) + 8q .. +7
+      const bool in = kb + u < kb1;
+      A0[u] = (in && v0) ? __ldg(reinterpret_cast<const uint4*>(x0) + vi) : make_uint4(0u, 0u, 0u, 0u);
+      A1[u] = (in && v1) ? __ldg(reinterpret_cast<const uint4*>(x1) + vi) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        B[u][nt][0] = (in && wv[nt]) ? __ldg(wr[nt] + c) : 0u;
-        B[u][nt][1] = (in && wv[nt]) ? __ldg(wr[nt] + c + 4) : 0u;
-      }
+      for (int nt = 0; nt < NT; ++nt)
+        B[u][nt] = (in && wv[nt]) ? __ldg(reinterpret_cast<const uint4*>(wr[nt]) + vi) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
-      if (ks + u < ks1) {
+      if (kb + u < kb1) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt) {
+          // k-step 0 of the block: words x/y; k-step 1: words z/w
           asm volatile(
               "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
               "{%0,%1,%2,%3};"
               : "+f"(acc[nt][0]), "+f"(acc[nt][1]), "+f"(acc[nt][2]), "+f"(acc[nt][3])
-              : "r"(A[u][0]), "r"(A[u][1]), "r"(A[u][2]), "r"(A[u][3]), "r"(B[u][nt][0]), "r"(B[u][nt][1]));
+              : "r"(A0[u].x), "r"(A1[u].x), "r"(A0[u].y), "r"(A1[u].y), "r"(B[u][nt].x), "r"(B[u][nt].y));
+          asm volatile(
+              "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+              "{%0,%1,%2,%3};"
+              : "+f"(acc[nt][0]), "+f"(acc[nt][1]), "+f"(acc[nt][2]), "+f"(acc[nt][3])
+              : "r"(A0[u].z), "r"(A1[u].z), "r"(A0[u].w), "r"(A1[u].w), "r"(B[u][nt].z), "r"(B[u][nt].w));
+        }
       }
     }
   }
@@ -471,7 +478,7 @@ cudaError_t launch_router(int dtype, const RouterArgs& a, int nchunks, cudaStrea
     if (a.E <= 8) return launch_router_t<float, 8>(a, nchunks, s);
     return launch_router_t<float, 16>(a, nchunks, s);
   }
-  if (a.d % 16 == 0) {
+  if (a.d % 32 == 0) {
     if (a.E <= 8) return pdl_launch(router_top2_mma_kernel<1>, dim3(nchunks), dim3(kRouterThreads), 0, s, a);
     return pdl_launch(router_top2_mma_kernel<2>, dim3(nchunks), dim3(kRouterThreads), 0, s, a);
   }
