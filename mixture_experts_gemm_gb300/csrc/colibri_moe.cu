@@ -64,6 +64,7 @@ struct colibri_moe {
   float* gate = nullptr;
   int32_t* row_of = nullptr;
   int32_t* tok_of_row = nullptr;
+  float* gate_of_row = nullptr;
   int32_t* hist = nullptr;
   Sched* sched = nullptr;
   void* x_stage = nullptr;
@@ -75,6 +76,7 @@ struct colibri_moe {
   float* partial = nullptr;  // decode partial sums [splits][n_pad][E * rows]
   int decode_max_t = 0;
   bool pair_gemm = false;    // prefill GEMMs on CTA pairs (256x256 tiles)
+  bool fuse_combine = true;  // two-slot fp32 layers: gate-weighted combine inside the down GEMM
   int pair_ctas = 0;         // co-resident CTAs of the pair kernel (persistent grid size)
   int32_t last_T = -1;
   std::vector<cudaEvent_t> events;
@@ -166,6 +168,11 @@ int check_config(const colibri_moe_config_t* c) {
 }
 
 // Prefill GEMMs run on CTA pairs (cta_group::2) unless COLIBRI_MOE_GEMM=1sm selects the single-CTA kernel.
+bool env_fuse_combine() {
+  const char* s = std::getenv("COLIBRI_MOE_FUSED_COMBINE");
+  return !(s && s[0] == '0');
+}
+
 bool env_pair_gemm() {
   const char* s = std::getenv("COLIBRI_MOE_GEMM");
   return !(s && std::strcmp(s, "1sm") == 0);
@@ -244,6 +251,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   c->num_sms = sms;
   c->timeout_ns = env_timeout_ns();
   c->pair_gemm = env_pair_gemm() && (sms % 2 == 0);
+  c->fuse_combine = env_fuse_combine();
   const int64_t d = cfg->d_model, f = cfg->d_ff, E = cfg->num_experts, T = cfg->max_tokens;
   c->esize = cfg->dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
   c->out_esize = cfg->out_dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
@@ -276,6 +284,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   const size_t o_gate = carve(S * T * 4);
   const size_t o_row = carve(S * T * 4);
   const size_t o_tok = carve(c->rows_alloc * 4);
+  const size_t o_gor = carve(c->rows_alloc * 4);
   const size_t o_hist = carve(static_cast<size_t>(c->nchunks_max) * Ex * 4);
   const size_t o_sched = carve(sizeof(Sched));
   // decode partial sums: bf16 layers whose batches can be decode-sized
@@ -303,6 +312,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   c->gate = reinterpret_cast<float*>(b + o_gate);
   c->row_of = reinterpret_cast<int32_t*>(b + o_row);
   c->tok_of_row = reinterpret_cast<int32_t*>(b + o_tok);
+  c->gate_of_row = reinterpret_cast<float*>(b + o_gor);
   c->hist = reinterpret_cast<int32_t*>(b + o_hist);
   c->sched = reinterpret_cast<Sched*>(b + o_sched);
   c->partial = part_floats > 0 ? reinterpret_cast<float*>(b + o_part) : nullptr;
@@ -457,16 +467,21 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   int64_t max_mtiles = (ctx->S * static_cast<int64_t>(T) + (kRowTile - 1) * E) / kRowTile;
   if (max_mtiles > ctx->rows_alloc / kRowTile) max_mtiles = ctx->rows_alloc / kRowTile;
 
+  // Two slots with an fp32 output on the prefill path: the down GEMM adds g * y straight into out
+  // (cleared by the router); two fp32 additions onto zero give the same value in either order.
+  const bool decode = bf16 && T <= ctx->decode_max_t;
+  const bool fuse = bf16 && !decode && ctx->fuse_combine && ctx->S == 2 && c.out_dtype == COLIBRI_DTYPE_F32;
   mark(0);
   RouterArgs ra{x, ctx->w_router, ctx->b_router, T, d, c.num_experts, ctx->dchunk, ctx->idx, ctx->gate,
-                ctx->row_of, ctx->hist, ctx->sched, ctx->k, c.gate_mode, c.has_shared_expert, ctx->S, ctx->Ex};
+                ctx->row_of, ctx->hist, ctx->sched, ctx->k, c.gate_mode, c.has_shared_expert, ctx->S, ctx->Ex,
+                fuse ? static_cast<float*>(out) : nullptr};
   if (launch_router(c.dtype, ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   mark(1);
   GatherArgs ga{x, ctx->idx, ctx->row_of, ctx->hist, T, d, E, ctx->S, ctx->rows_alloc, ctx->xp, ctx->tok_of_row,
-                ctx->sched};
+                ctx->sched, ctx->gate, fuse ? ctx->gate_of_row : nullptr};
   if (launch_gather(c.dtype, ga, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   mark(2);
-  if (bf16 && T <= ctx->decode_max_t) {
+  if (decode) {
     // decode-sized batch: weight-streaming GEMMs with K splits, deterministic reductions
     const int n_pad = (T + 15) / 16 * 16;
     const int mi = n_pad / 16 - 1;
@@ -502,24 +517,27 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
         cudaSuccess)
       return COLIBRI_ERR_CUDA;
     mark(3);
-    GemmArgs dn{ctx->sched, E, f, d, d / bn, ctx->y, d, ctx->b2, d, ctx->timeout_ns, &ctx->sched->status};
+    GemmArgs dn{ctx->sched, E, f, d, d / bn, fuse ? out : ctx->y, d, ctx->b2, d, ctx->timeout_ns,
+                &ctx->sched->status, ctx->tok_of_row, ctx->gate_of_row};
     ctas = 2 * max_pairs * dn.n_tiles;
     grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
-    if (launch_pair_gemm(kEpiStoreF32, ctx->tm_h, ctx->tm_w2_dec, dn, grid, s) != cudaSuccess)
+    if (launch_pair_gemm(fuse ? kEpiCombineF32 : kEpiStoreF32, ctx->tm_h, ctx->tm_w2_dec, dn, grid, s) != cudaSuccess)
       return COLIBRI_ERR_CUDA;
   } else if (bf16) {
     const int bn = tc_gemm_block_n();
     GemmArgs up{ctx->sched, E, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns,
-                 &ctx->sched->status};
+                &ctx->sched->status};
     int64_t tiles = max_mtiles * up.n_tiles;
     int grid = static_cast<int>(tiles < ctx->num_sms ? tiles : ctx->num_sms);
     if (launch_tc_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, ctx->tm_xp, ctx->tm_w13, up, grid, s) != cudaSuccess)
       return COLIBRI_ERR_CUDA;
     mark(3);
-    GemmArgs dn{ctx->sched, E, f, d, d / bn, ctx->y, d, ctx->b2, d, ctx->timeout_ns, &ctx->sched->status};
+    GemmArgs dn{ctx->sched, E, f, d, d / bn, fuse ? out : ctx->y, d, ctx->b2, d, ctx->timeout_ns,
+                &ctx->sched->status, ctx->tok_of_row, ctx->gate_of_row};
     tiles = max_mtiles * dn.n_tiles;
     grid = static_cast<int>(tiles < ctx->num_sms ? tiles : ctx->num_sms);
-    if (launch_tc_gemm(kEpiStoreF32, ctx->tm_h, ctx->tm_w2, dn, grid, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+    if (launch_tc_gemm(fuse ? kEpiCombineF32 : kEpiStoreF32, ctx->tm_h, ctx->tm_w2, dn, grid, s) != cudaSuccess)
+      return COLIBRI_ERR_CUDA;
   } else {
     SimtGemmArgs up{ctx->sched, E, d, f, static_cast<const float*>(ctx->xp), static_cast<const float*>(ctx->w13),
                     static_cast<const float*>(ctx->w3), ctx->b1, static_cast<float*>(ctx->h)};
@@ -531,8 +549,10 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     if (launch_simt_gemm(kEpiStoreF32, dn, static_cast<int>(max_mtiles), s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   }
   mark(4);
-  CombineArgs ca{ctx->y, ctx->row_of, ctx->gate, T, d, out, ctx->S};
-  if (launch_combine(c.out_dtype, ca, ctx->num_sms, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  if (!fuse) {
+    CombineArgs ca{ctx->y, ctx->row_of, ctx->gate, T, d, out, ctx->S};
+    if (launch_combine(c.out_dtype, ca, ctx->num_sms, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  }
   mark(5);
   ctx->last_T = T;
   return COLIBRI_OK;

@@ -270,6 +270,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int w = 0; w < 4; ++w) dst[w] = make_uint4(p[4 * w], p[4 * w + 1], p[4 * w + 2], p[4 * w + 3]);
           }
         }
+      } else if constexpr (EPI == kEpiCombineF32) {
+        // out[token] += gate * (acc (+ b2)): with two slots and a zeroed output the two reductions give
+        // RN(g0*y0 + g1*y1) in either order, the value the separate combine computes
+        const int tok = valid ? a.token_of_row[row] : 0;
+        const float gr = valid ? a.gate_of_row[row] : 0.f;
+        float* out = static_cast<float*>(a.out) + static_cast<size_t>(tok) * a.ldo + c.n * BN;
+        const float* bias = a.bias ? a.bias + static_cast<size_t>(c.e) * a.out_cols + c.n * BN : nullptr;
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32_sync(tbase + ch * 32, v);
+          if (valid) {
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+              float y[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                y[i] = __uint_as_float(v[4 * w + i]);
+                if (bias) y[i] += bias[ch * 32 + 4 * w + i];
+                y[i] = __fmul_rn(gr, y[i]);
+              }
+              red_add_v4(out + ch * 32 + 4 * w, y[0], y[1], y[2], y[3]);
+            }
+          }
+        }
       } else {
         float* out = static_cast<float*>(a.out) + static_cast<size_t>(row) * a.ldo + c.n * BN;
         const float* bias = a.bias ? a.bias + static_cast<size_t>(c.e) * a.out_cols + c.n * BN : nullptr;
@@ -328,6 +353,9 @@ cudaError_t prepare_tc_gemm() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(tc_grouped_gemm_kernel<kEpiStoreF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tc_grouped_gemm_kernel<kEpiCombineF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES);
   return e;
 }
 
@@ -340,6 +368,7 @@ cudaError_t launch_tc_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& t
   switch (epi) {
     case kEpiSwiGLU: return launch_t<kEpiSwiGLU>(tmA, tmB, a, grid, s);
     case kEpiReluBias: return launch_t<kEpiReluBias>(tmA, tmB, a, grid, s);
+    case kEpiCombineF32: return launch_t<kEpiCombineF32>(tmA, tmB, a, grid, s);
     default: return launch_t<kEpiStoreF32>(tmA, tmB, a, grid, s);
   }
 }

@@ -56,6 +56,7 @@ struct RouterArgs {
   int shared;              // 1: slot k of every token is the shared expert (index E, gate 1)
   int S;                   // slots per token = k + shared
   int Ex;                  // scheduled experts = E + shared
+  float* zero_out;         // fused combine: out [T, d] fp32 rows of this CTA's tokens cleared, else nullptr
 };
 
 struct GatherArgs {
@@ -69,6 +70,8 @@ struct GatherArgs {
   void* xp;                // [rows_alloc, d]
   int32_t* token_of_row;   // [rows_alloc]
   Sched* sched;
+  const float* gate;       // [T, S]
+  float* gate_of_row;      // [rows_alloc] or nullptr
 };
 
 struct CombineArgs {
@@ -84,6 +87,7 @@ enum GemmEpilogue : int {
   kEpiSwiGLU = 0,    // up projection, gate/up interleaved -> H = silu(g) * u
   kEpiReluBias = 1,  // up projection -> H = max(acc + b1, 0)
   kEpiStoreF32 = 2,  // down projection -> Y = acc (+ b2)
+  kEpiCombineF32 = 3,  // down projection fused with the combine: out[token] += gate * (acc (+ b2))
 };
 
 struct GemmArgs {
@@ -98,6 +102,8 @@ struct GemmArgs {
   int out_cols;             // output columns per expert (f for up, d for down)
   uint64_t timeout_ns;      // bound on every wait inside the kernel
   int32_t* status;          // device status word (Sched::status)
+  const int32_t* token_of_row;  // kEpiCombineF32: token of each row
+  const float* gate_of_row;     // kEpiCombineF32: gate of each row
 };
 
 // Decode (weight-streaming) GEMM: P[s][tok][row] partial sums over K split s.

@@ -43,12 +43,14 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherArgs a, in
       for (int s = 0; s < S; ++s) {
         a.row_of[(size_t)S * t + s] = r[s];
         a.token_of_row[r[s]] = t;
+        if (a.gate_of_row) a.gate_of_row[r[s]] = a.gate[(size_t)S * t + s];
       }
     } else {
       atomicOr(&a.sched->status, kStatusBadRow);
     }
   }
   if (!ok) return;
+
   const size_t row_bytes = (size_t)a.d * ESIZE;
   const int nvec = (int)(row_bytes / 16);
   const int v0 = (nvec * part) / wpt, v1 = (nvec * (part + 1)) / wpt;

@@ -202,6 +202,15 @@ __device__ __forceinline__ void topk_store(const RouterArgs& a, const float (&L)
   }
 }
 
+// Fused combine: the down projection adds both expert outputs into out, so this CTA's token rows
+// start at zero.  Issued before the logits work, the stores drain while the loads wait on memory.
+__device__ __forceinline__ void zero_out_rows(const RouterArgs& a, int chunk_t0, int valid) {
+  if (a.zero_out == nullptr) return;
+  const int n4 = a.d / 4;
+  float4* o = reinterpret_cast<float4*>(a.zero_out + (size_t)chunk_t0 * a.d);
+  for (int i = threadIdx.x; i < valid * n4; i += kRouterThreads) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 // fp32 layers: FMA dot products with W_r staged in shared memory.
 template <typename Tin, int EMAX>
 __global__ void __launch_bounds__(kRouterThreads) router_top2_kernel(RouterArgs a) {
@@ -229,6 +238,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_top2_kernel(RouterArgs 
   const Tin* __restrict__ w = static_cast<const Tin*>(a.w_router);
   pdl_trigger();
   pdl_wait();  // x may come from the previous kernel; the workspace from the previous forward
+  zero_out_rows(a, chunk_t0, valid);
 
   float acc[4][EMAX];
 #pragma unroll
@@ -373,6 +383,7 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_top2_mma_kernel(Rout
   const int kb0 = (nblk * sl) / S, kb1 = (nblk * (sl + 1)) / S;
   pdl_trigger();
   pdl_wait();  // x may come from the previous kernel; the workspace from the previous forward
+  zero_out_rows(a, chunk_t0, valid);
   // one bulk L2 prefetch per token row of this warp's column range: only the first round of fragment
   // loads below waits on HBM, the later rounds hit L2
   if (lane < 16 && kb1 > kb0) {

@@ -215,6 +215,26 @@ def test_shared_expert_relu_bias_bf16_and_pair_kernel(monkeypatch):
     _full_check(li)
 
 
+@pytest.mark.parametrize("gemm", ["2sm", "1sm"])
+def test_fused_combine_equals_separate_combine(gemm, monkeypatch):
+    """Two slots, fp32 output: the down GEMM adds g*y into the zeroed output; with two fp32 additions
+    onto zero the result is the separate combine's RN(g0*y0 + g1*y1) bit for bit."""
+    monkeypatch.setenv("COLIBRI_MOE_GEMM", gemm)
+    shape = testgen.LayerShape("fused", 900, 512, 384, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True)
+    li = testgen.make_inputs(shape)
+    layer, out_f, r, ref, err = _full_check(li)
+    monkeypatch.setenv("COLIBRI_MOE_FUSED_COMBINE", "0")
+    layer2, out_s, r2, _, _ = _full_check(li)
+    assert np.array_equal(out_f, out_s)
+    # ReLU with biases: b2 is added before the gate scale in both forms
+    shape = testgen.LayerShape("fused-relu", 300, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")
+    li = testgen.make_inputs(shape)
+    _, out_s, _, _, _ = _full_check(li)
+    monkeypatch.delenv("COLIBRI_MOE_FUSED_COMBINE")
+    _, out_f, _, _, _ = _full_check(li)
+    assert np.array_equal(out_f, out_s)
+
+
 def test_1p3b_workload():
     li = testgen.make_inputs(testgen.CONFIGS["1.3b-8e"])
     _, _, _, _, err = _full_check(li)
