@@ -122,8 +122,10 @@ COLIBRI_API int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_w
 
 /* out[T, d] = MoE layer applied to x[T, d].  x (config.dtype) and out (config.out_dtype) are device
  * pointers, row-major and contiguous, and must not overlap.  Asynchronous on `stream`: no host
- * synchronisation and no allocation.  T == 0 is a no-op.  Calls on one context must be ordered
- * (same stream, or synchronised): the workspace is shared. */
+ * synchronisation and no allocation, so a call can be captured into a CUDA graph and replayed (the
+ * replay reads x and writes out at the captured addresses).  T == 0 is a no-op.  Calls on one context
+ * must be ordered (same stream, or synchronised): the workspace is shared.  With two routed slots and
+ * an fp32 output, out is written by accumulation (cleared first, then both expert outputs added). */
 COLIBRI_API int colibri_moe_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t T, void* stream);
 
 /* Same as forward with HOST buffers: copies x host->device into the context's staging buffer,

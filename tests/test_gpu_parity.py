@@ -235,6 +235,32 @@ def test_fused_combine_equals_separate_combine(gemm, monkeypatch):
     assert np.array_equal(out_f, out_s)
 
 
+@pytest.mark.parametrize("T", [24, 900])
+def test_forward_replays_from_a_cuda_graph(T):
+    """forward allocates nothing and never synchronises, so it can be captured into a CUDA graph; the
+    replay must reproduce the eager output bit for bit (prefill and decode paths)."""
+    shape = testgen.LayerShape("graph", T, 512, 384, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True)
+    li = testgen.make_inputs(shape)
+    layer = make_layer(li)
+    x = x_device(li)
+    eager = layer.forward(x).clone()
+    out = torch.empty_like(eager)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.forward(x, out, stream=s)   # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer.forward(x, out)
+    out.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    assert layer.device_status() == 0
+
+
 def test_1p3b_workload():
     li = testgen.make_inputs(testgen.CONFIGS["1.3b-8e"])
     _, _, _, _, err = _full_check(li)
