@@ -31,7 +31,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 STAGES = ["router", "gather", "gemm_up", "gemm_down", "combine"]
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture of the kernel as it now
 # stands (profiles/gemm_pair_mixtral_prefill.md); None where no capture of the current kernel exists.
-NCU_TRAFFIC = {("mixtral-prefill", 8192, "gemm_up", "2sm"): 3.836e9, ("mixtral-prefill", 8192, "gemm_down", "2sm"): 3.466e9}
+NCU_TRAFFIC = {("mixtral-prefill", 8192, "gemm_up", "2sm"): 4.623e9, ("mixtral-prefill", 8192, "gemm_down", "2sm"): 4.248e9}
 
 
 def log(*a):
@@ -391,7 +391,7 @@ def main():
         "stages_us": {n: float(v * 1e3) for n, v in zip(STAGES, mean_stage)},
         "stages_note": "stage split from a separate 50-step pass with an event at every stage boundary",
         "e2e": e2e,
-        "gpu_launches": args.steps * n_st,
+        "gpu_launches": args.steps * layer.last_kernel_count(),
         "clocks": clk,
         "cpu_baseline": cpu,
         "device_status": status,

@@ -151,8 +151,15 @@ COLIBRI_API int colibri_moe_get_routing(colibri_moe_t* ctx, int32_t* idx, float*
  * the allocated row count (may be NULL). */
 COLIBRI_API int colibri_moe_debug_buffer(colibri_moe_t* ctx, int32_t which, void** ptr, int64_t* rows);
 
-/* Number of pipeline stages (kernel launches) forward enqueues, for a nonzero T. */
+/* Number of timed pipeline stages of forward (router, dispatch, up GEMM, down GEMM, combine), for
+ * set_stage_events.  A stage holds one kernel, two (the decode path's GEMM + reduction) or none
+ * (the combine, when fused into the down GEMM). */
 COLIBRI_API int colibri_moe_num_stages(const colibri_moe_t* ctx, int32_t* n_stages);
+
+/* *n = the number of kernels the most recent forward (or forward_host) enqueued: 4 on the bf16
+ * prefill path with the combine fused into the down GEMM, 5 with a separate combine, 6 on the
+ * decode path (T <= 64); 0 before the first forward and after a forward with T = 0. */
+COLIBRI_API int colibri_moe_last_kernel_count(const colibri_moe_t* ctx, int32_t* n);
 
 /* Stage timing: with n == num_stages + 1 cudaEvent_t values (passed as void*), every later forward
  * records events[i] just before stage i and events[n-1] after the last stage, on its stream; NULL

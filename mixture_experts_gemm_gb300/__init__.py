@@ -33,7 +33,8 @@ _ACTS = {"relu_bias": ACT_RELU_BIAS, "relu": ACT_RELU_BIAS, "swiglu": ACT_SWIGLU
 # every function include/colibri_moe.h declares
 EXPORTED = ("colibri_moe_create", "colibri_moe_load_weights", "colibri_moe_forward", "colibri_moe_forward_host",
             "colibri_moe_get_routing", "colibri_moe_debug_buffer", "colibri_moe_num_stages",
-            "colibri_moe_set_stage_events", "colibri_moe_device_status", "colibri_moe_route_noalloc",
+            "colibri_moe_last_kernel_count", "colibri_moe_set_stage_events", "colibri_moe_device_status",
+            "colibri_moe_route_noalloc",
             "colibri_moe_destroy", "colibri_moe_strerror")
 
 
@@ -77,6 +78,7 @@ def lib() -> ctypes.CDLL:
             "colibri_moe_get_routing": ([vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
             "colibri_moe_debug_buffer": ([vp, i32, ctypes.POINTER(vp), ctypes.POINTER(i64)], ctypes.c_int),
             "colibri_moe_num_stages": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
+            "colibri_moe_last_kernel_count": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
             "colibri_moe_set_stage_events": ([vp, vp, i32], ctypes.c_int),
             "colibri_moe_device_status": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
             "colibri_moe_route_noalloc": ([vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp], ctypes.c_int),
@@ -255,6 +257,12 @@ class MoELayer:
     def num_stages(self) -> int:
         n = ctypes.c_int32()
         _check(lib().colibri_moe_num_stages(self._h, ctypes.byref(n)), "colibri_moe_num_stages")
+        return n.value
+
+    def last_kernel_count(self) -> int:
+        """Kernels the most recent forward enqueued."""
+        n = ctypes.c_int32()
+        _check(lib().colibri_moe_last_kernel_count(self._h, ctypes.byref(n)), "colibri_moe_last_kernel_count")
         return n.value
 
     def set_stage_events(self, events):

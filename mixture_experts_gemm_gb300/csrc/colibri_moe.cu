@@ -77,8 +77,10 @@ struct colibri_moe {
   int decode_max_t = 0;
   bool pair_gemm = false;    // prefill GEMMs on CTA pairs (256x256 tiles)
   bool fuse_combine = true;  // two-slot fp32 layers: gate-weighted combine inside the down GEMM
+  bool gather_a = false;     // bf16 prefill: up GEMM reads A rows from x through token_of_row
   int pair_ctas = 0;         // co-resident CTAs of the pair kernel (persistent grid size)
   int32_t last_T = -1;
+  int32_t last_kernels = 0;  // kernels enqueued by the last forward
   std::vector<cudaEvent_t> events;
   uint64_t timeout_ns = 2000000000ull;
 };
@@ -167,12 +169,20 @@ int check_config(const colibri_moe_config_t* c) {
   return COLIBRI_OK;
 }
 
-// Prefill GEMMs run on CTA pairs (cta_group::2) unless COLIBRI_MOE_GEMM=1sm selects the single-CTA kernel.
+// Two-slot fp32 layers fuse the combine into the down GEMM unless COLIBRI_MOE_FUSED_COMBINE=0.
 bool env_fuse_combine() {
   const char* s = std::getenv("COLIBRI_MOE_FUSED_COMBINE");
   return !(s && s[0] == '0');
 }
 
+// COLIBRI_MOE_GATHER=fused: the prefill up GEMM gathers its A rows from x (no Xp).  Off by default:
+// on GB300 at the Mixtral shape it measured 2-4 % slower than the TMA-fed GEMM over Xp.
+bool env_gather_a() {
+  const char* s = std::getenv("COLIBRI_MOE_GATHER");
+  return s && std::strcmp(s, "fused") == 0;
+}
+
+// Prefill GEMMs run on CTA pairs (cta_group::2) unless COLIBRI_MOE_GEMM=1sm selects the single-CTA kernel.
 bool env_pair_gemm() {
   const char* s = std::getenv("COLIBRI_MOE_GEMM");
   return !(s && std::strcmp(s, "1sm") == 0);
@@ -252,6 +262,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   c->timeout_ns = env_timeout_ns();
   c->pair_gemm = env_pair_gemm() && (sms % 2 == 0);
   c->fuse_combine = env_fuse_combine();
+  c->gather_a = env_gather_a();
   const int64_t d = cfg->d_model, f = cfg->d_ff, E = cfg->num_experts, T = cfg->max_tokens;
   c->esize = cfg->dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
   c->out_esize = cfg->out_dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
@@ -471,14 +482,18 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   // (cleared by the router); two fp32 additions onto zero give the same value in either order.
   const bool decode = bf16 && T <= ctx->decode_max_t;
   const bool fuse = bf16 && !decode && ctx->fuse_combine && ctx->S == 2 && c.out_dtype == COLIBRI_DTYPE_F32;
+  // bf16 prefill: the up GEMM gathers its A rows from x through token_of_row instead of reading a
+  // materialised Xp; the dispatch kernel then only writes the row bookkeeping.
+  const bool gather_a = bf16 && !decode && ctx->gather_a;
   mark(0);
   RouterArgs ra{x, ctx->w_router, ctx->b_router, T, d, c.num_experts, ctx->dchunk, ctx->idx, ctx->gate,
                 ctx->row_of, ctx->hist, ctx->sched, ctx->k, c.gate_mode, c.has_shared_expert, ctx->S, ctx->Ex,
                 fuse ? static_cast<float*>(out) : nullptr};
   if (launch_router(c.dtype, ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   mark(1);
-  GatherArgs ga{x, ctx->idx, ctx->row_of, ctx->hist, T, d, E, ctx->S, ctx->rows_alloc, ctx->xp, ctx->tok_of_row,
-                ctx->sched, ctx->gate, fuse ? ctx->gate_of_row : nullptr};
+  GatherArgs ga{x, ctx->idx, ctx->row_of, ctx->hist, T, d, E, ctx->S, ctx->rows_alloc,
+                gather_a ? nullptr : ctx->xp, ctx->tok_of_row, ctx->sched, ctx->gate,
+                fuse ? ctx->gate_of_row : nullptr};
   if (launch_gather(c.dtype, ga, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   mark(2);
   if (decode) {
@@ -503,6 +518,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     if (launch_decode_combine(c.out_dtype, cb, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
     mark(5);
     ctx->last_T = T;
+    ctx->last_kernels = 6;
     return COLIBRI_OK;
   }
   if (bf16 && ctx->pair_gemm) {
@@ -510,10 +526,10 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     const int bn = tc_gemm_block_n();
     const int64_t max_pairs = (max_mtiles + E + 1) / 2;
     GemmArgs up{ctx->sched, E, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns,
-                &ctx->sched->status};
+                &ctx->sched->status, ctx->tok_of_row, nullptr, x};
     int64_t ctas = 2 * max_pairs * up.n_tiles;
     int grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
-    if (launch_pair_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, ctx->tm_xp, ctx->tm_w13_dec, up, grid, s) !=
+    if (launch_pair_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, gather_a, ctx->tm_xp, ctx->tm_w13_dec, up, grid, s) !=
         cudaSuccess)
       return COLIBRI_ERR_CUDA;
     mark(3);
@@ -521,22 +537,25 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
                 &ctx->sched->status, ctx->tok_of_row, ctx->gate_of_row};
     ctas = 2 * max_pairs * dn.n_tiles;
     grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
-    if (launch_pair_gemm(fuse ? kEpiCombineF32 : kEpiStoreF32, ctx->tm_h, ctx->tm_w2_dec, dn, grid, s) != cudaSuccess)
+    if (launch_pair_gemm(fuse ? kEpiCombineF32 : kEpiStoreF32, false, ctx->tm_h, ctx->tm_w2_dec, dn, grid, s) !=
+        cudaSuccess)
       return COLIBRI_ERR_CUDA;
   } else if (bf16) {
     const int bn = tc_gemm_block_n();
     GemmArgs up{ctx->sched, E, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns,
-                &ctx->sched->status};
+                &ctx->sched->status, ctx->tok_of_row, nullptr, x};
     int64_t tiles = max_mtiles * up.n_tiles;
     int grid = static_cast<int>(tiles < ctx->num_sms ? tiles : ctx->num_sms);
-    if (launch_tc_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, ctx->tm_xp, ctx->tm_w13, up, grid, s) != cudaSuccess)
+    if (launch_tc_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, gather_a, ctx->tm_xp, ctx->tm_w13, up, grid, s) !=
+        cudaSuccess)
       return COLIBRI_ERR_CUDA;
     mark(3);
     GemmArgs dn{ctx->sched, E, f, d, d / bn, fuse ? out : ctx->y, d, ctx->b2, d, ctx->timeout_ns,
                 &ctx->sched->status, ctx->tok_of_row, ctx->gate_of_row};
     tiles = max_mtiles * dn.n_tiles;
     grid = static_cast<int>(tiles < ctx->num_sms ? tiles : ctx->num_sms);
-    if (launch_tc_gemm(fuse ? kEpiCombineF32 : kEpiStoreF32, ctx->tm_h, ctx->tm_w2, dn, grid, s) != cudaSuccess)
+    if (launch_tc_gemm(fuse ? kEpiCombineF32 : kEpiStoreF32, false, ctx->tm_h, ctx->tm_w2, dn, grid, s) !=
+        cudaSuccess)
       return COLIBRI_ERR_CUDA;
   } else {
     SimtGemmArgs up{ctx->sched, E, d, f, static_cast<const float*>(ctx->xp), static_cast<const float*>(ctx->w13),
@@ -555,6 +574,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   }
   mark(5);
   ctx->last_T = T;
+  ctx->last_kernels = fuse ? 4 : 5;
   return COLIBRI_OK;
 }
 
@@ -562,7 +582,10 @@ int colibri_moe_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t T,
   if (!ctx) return COLIBRI_ERR_INVALID_ARG;
   if (T < 0 || T > ctx->cfg.max_tokens) return COLIBRI_ERR_INVALID_ARG;
   if (!ctx->loaded) return COLIBRI_ERR_STATE;
-  if (T == 0) return COLIBRI_OK;
+  if (T == 0) {
+    ctx->last_kernels = 0;
+    return COLIBRI_OK;
+  }
   if (!x || !out) return COLIBRI_ERR_INVALID_ARG;
   const size_t xb = static_cast<size_t>(T) * ctx->cfg.d_model * ctx->esize;
   const size_t ob = static_cast<size_t>(T) * ctx->cfg.d_model * ctx->out_esize;
@@ -578,7 +601,10 @@ int colibri_moe_forward_host(colibri_moe_t* ctx, const void* x_host, void* out_h
   if (!ctx) return COLIBRI_ERR_INVALID_ARG;
   if (T < 0 || T > ctx->cfg.max_tokens) return COLIBRI_ERR_INVALID_ARG;
   if (!ctx->loaded) return COLIBRI_ERR_STATE;
-  if (T == 0) return COLIBRI_OK;
+  if (T == 0) {
+    ctx->last_kernels = 0;
+    return COLIBRI_OK;
+  }
   if (!x_host || !out_host) return COLIBRI_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
   if (!g.ok) return COLIBRI_ERR_CUDA;
@@ -654,6 +680,12 @@ int colibri_moe_debug_buffer(colibri_moe_t* ctx, int32_t which, void** ptr, int6
 int colibri_moe_num_stages(const colibri_moe_t* ctx, int32_t* n_stages) {
   if (!ctx || !n_stages) return COLIBRI_ERR_INVALID_ARG;
   *n_stages = kNumStages;
+  return COLIBRI_OK;
+}
+
+int colibri_moe_last_kernel_count(const colibri_moe_t* ctx, int32_t* n) {
+  if (!ctx || !n) return COLIBRI_ERR_INVALID_ARG;
+  *n = ctx->last_kernels;
   return COLIBRI_OK;
 }
 

@@ -27,7 +27,11 @@
 // Every mbarrier wait is bounded (GemmArgs::timeout_ns): on expiry the kernel raises a bit in the
 // device status word, stops all roles, waits (bounded) for its own TMA copies and MMAs, frees
 // TMEM and returns.
-#include "tcgen05_ptx.cuh"
+//
+// Gathered A (GA, up projection only): A rows come straight from the token rows x through
+// token_of_row (gather_a.cuh): extra warps copy them with cp.async, and a forwarder thread arrives
+// on `full` once they are in place, next to the TMA bytes of B.
+#include "gather_a.cuh"
 
 namespace colibri {
 namespace {
@@ -40,8 +44,10 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS_GA = 192 + 32 * (kGatherWarps + kForwarders);  // + A gather and forwarder warps
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
+constexpr int NUM_BARS = 3 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain, gfull
+static_assert(STAGES % kForwarders == 0, "a stage keeps its forwarder across ring cycles");
 constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 4 * (3 * kMaxE + 3);
 
 struct TileCoord {
@@ -61,8 +67,8 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const int* mtile_star
   return c;
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int EPI, bool GA>
+__global__ void __launch_bounds__(GA ? NUM_THREADS_GA : NUM_THREADS, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -81,6 +87,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tfull0 = smem_u32(bars + 2 * STAGES);
   const uint32_t tempty0 = smem_u32(bars + 2 * STAGES + 2);
   const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
+  const uint32_t gfull0 = smem_u32(bars + 2 * STAGES + 5);  // gathered A: rows of a stage landed
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E;
@@ -88,7 +95,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   pdl_trigger();
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, GA ? 2 : 1);  // TMA arrive (+ the A forwarder)
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -96,9 +103,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(tempty0 + 8 * i, 4);
     }
     mbar_init(drain, 1);
+    if constexpr (GA)
+      for (int s = 0; s < STAGES; ++s) mbar_init(gfull0 + 8 * s, kGatherThreads);
     *s_abort = 0;
     fence_mbar_init();
-    prefetch_tmap(&tmA);
+    if constexpr (!GA) prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
   }
   if (warp == 1) {
@@ -136,10 +145,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full0 + 8 * stage, STAGE_BYTES);
+          mbar_arrive_expect_tx(full0 + 8 * stage, GA ? B_BYTES : STAGE_BYTES);
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-          tma_load_2d(smem_u32(sA + stage * A_BYTES), &tmA, full0 + 8 * stage, kb * BK, a_row);
+          if constexpr (!GA) tma_load_2d(smem_u32(sA + stage * A_BYTES), &tmA, full0 + 8 * stage, kb * BK, a_row);
           tma_load_2d(smem_u32(sB + stage * B_BYTES), &tmB, full0 + 8 * stage, kb * BK, b_row);
           if (++stage == STAGES) {
             stage = 0;
@@ -157,6 +166,71 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           volatile int never = 0;
           mbar_wait(full0 + 8 * s, (armed_phase >> s) & 1u, &never, a.timeout_ns);
         }
+    }
+  } else if (GA && warp >= kGatherWarp0 && warp < kForwardWarp0) {
+    // -------------------------------------------------------------- A gather warps
+    AGather g;
+    g.init(a.gather_x, a.K, warp - kGatherWarp0, lane);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    auto prefetch = [&](int tile) {
+      if (tile >= total_tiles) return;
+      const TileCoord c = decode_tile(tile, s_mstart, E, a.n_tiles);
+      g.prefetch_tokens(a.token_of_row, s_offsets[c.e] + c.m * BM, s_offsets[c.e] + s_counts[c.e]);
+    };
+    prefetch(blockIdx.x);
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      g.advance_tile();
+      prefetch(tile + gridDim.x);
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const bool got = __all_sync(0xffffffffu, mbar_wait(empty0 + 8 * stage, phase ^ 1u, s_abort, a.timeout_ns));
+        if (!got) {
+          ok = false;
+          break;
+        }
+        g.issue(smem_u32(sA + stage * A_BYTES), kb);
+        cp_async_arrive_noinc(gfull0 + 8 * stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    cp_async_wait<0>();  // nothing of this thread in flight when the CTA leaves
+    if (!ok && lane == 0) {
+      if (!*s_abort) atomicOr(a.status, kStatusTimeoutProducer);
+      *s_abort = 1;
+    }
+  } else if (GA && warp >= kForwardWarp0) {
+    // -------------------------------------------------------------- A forwarders (lane 0 of each forwarder warp)
+    // forwarder f handles the stages s with s % kForwarders == f, so the per-stage wake-up, proxy
+    // fence and arrive of consecutive stages overlap
+    const int fwd = warp - kForwardWarp0;
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (stage % kForwarders == fwd) {
+            if (!mbar_wait(gfull0 + 8 * stage, phase, s_abort, a.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(full0 + 8 * stage);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        if (!*s_abort) atomicOr(a.status, kStatusTimeoutProducer);
+        *s_abort = 1;
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -209,7 +283,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       volatile int never = 0;
       mbar_wait(drain, 0, &never, a.timeout_ns);
     }
-  } else {
+  } else if (warp < 6) {
     // -------------------------------------------------------------- epilogue (warps 2..5)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int acc = 0;
@@ -337,39 +411,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <int EPI>
+template <int EPI, bool GA>
 cudaError_t launch_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid, cudaStream_t s) {
-  return pdl_launch(tc_grouped_gemm_kernel<EPI>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, tmA, tmB, a);
+  return pdl_launch(tc_grouped_gemm_kernel<EPI, GA>, dim3(grid), dim3(GA ? NUM_THREADS_GA : NUM_THREADS), SMEM_BYTES,
+                    s, tmA, tmB, a);
+}
+
+template <int EPI, bool GA>
+cudaError_t set_smem() {
+  return cudaFuncSetAttribute(tc_grouped_gemm_kernel<EPI, GA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              SMEM_BYTES);
 }
 
 }  // namespace
 
 cudaError_t prepare_tc_gemm() {
-  cudaError_t e = cudaFuncSetAttribute(tc_grouped_gemm_kernel<kEpiSwiGLU>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(tc_grouped_gemm_kernel<kEpiReluBias>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(tc_grouped_gemm_kernel<kEpiStoreF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(tc_grouped_gemm_kernel<kEpiCombineF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES);
+  cudaError_t e = set_smem<kEpiSwiGLU, false>();
+  if (e == cudaSuccess) e = set_smem<kEpiSwiGLU, true>();
+  if (e == cudaSuccess) e = set_smem<kEpiReluBias, false>();
+  if (e == cudaSuccess) e = set_smem<kEpiReluBias, true>();
+  if (e == cudaSuccess) e = set_smem<kEpiStoreF32, false>();
+  if (e == cudaSuccess) e = set_smem<kEpiCombineF32, false>();
   return e;
 }
 
 int tc_gemm_block_n() { return BN; }
 int tc_gemm_threads() { return NUM_THREADS; }
 
-cudaError_t launch_tc_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
-                           cudaStream_t s) {
+// gather_a: A rows are gathered from a.gather_x through a.token_of_row (up-projection epilogues
+// only) and tmA is not read.
+cudaError_t launch_tc_gemm(int epi, bool gather_a, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const GemmArgs& a, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
   switch (epi) {
-    case kEpiSwiGLU: return launch_t<kEpiSwiGLU>(tmA, tmB, a, grid, s);
-    case kEpiReluBias: return launch_t<kEpiReluBias>(tmA, tmB, a, grid, s);
-    case kEpiCombineF32: return launch_t<kEpiCombineF32>(tmA, tmB, a, grid, s);
-    default: return launch_t<kEpiStoreF32>(tmA, tmB, a, grid, s);
+    case kEpiSwiGLU:
+      return gather_a ? launch_t<kEpiSwiGLU, true>(tmA, tmB, a, grid, s) : launch_t<kEpiSwiGLU, false>(tmA, tmB, a, grid, s);
+    case kEpiReluBias:
+      return gather_a ? launch_t<kEpiReluBias, true>(tmA, tmB, a, grid, s)
+                      : launch_t<kEpiReluBias, false>(tmA, tmB, a, grid, s);
+    case kEpiCombineF32:
+      if (gather_a) return cudaErrorInvalidValue;
+      return launch_t<kEpiCombineF32, false>(tmA, tmB, a, grid, s);
+    default:
+      if (gather_a) return cudaErrorInvalidValue;
+      return launch_t<kEpiStoreF32, false>(tmA, tmB, a, grid, s);
   }
 }
 

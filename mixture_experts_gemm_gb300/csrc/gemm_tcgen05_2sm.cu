@@ -16,7 +16,12 @@
 // an odd number of M tiles, the second CTA of its last pair computes rows past the expert's segment
 // (read as they are or as zeros past the buffer) and stores nothing.  Waits are bounded as in the
 // single-CTA kernel; TMEM is allocated and freed collectively by one warp of each CTA.
-#include "tcgen05_ptx.cuh"
+//
+// Gathered A (GA, up projection): the A rows come straight from the token rows x through
+// token_of_row (gather_a.cuh); extra warps of each CTA copy them with cp.async and a forwarder
+// thread of each CTA arrives on the leader's `full` barrier once they are in place, next to the
+// TMA bytes of B.  The MMA issuer waits on `full` with a cluster-scope acquire.
+#include "gather_a.cuh"
 
 namespace colibri {
 namespace {
@@ -29,10 +34,12 @@ constexpr int PA_BYTES = PBM * PBK * 2;         // 16 KB: this CTA's A rows
 constexpr int PB_BYTES = (PBN / 2) * PBK * 2;   // 16 KB: this CTA's half of B
 constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
 constexpr int PNUM_THREADS = 192;
+constexpr int PNUM_THREADS_GA = 192 + 32 * (kGatherWarps + kForwarders);  // + A gather and forwarder warps
 constexpr uint32_t PTMEM_COLS = 512;
-constexpr int PNUM_BARS = 2 * PSTAGES + 5;
+constexpr int PNUM_BARS = 3 * PSTAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain, gfull
 constexpr int PSMEM_BYTES = 1024 + PSTAGES * PSTAGE_BYTES + PNUM_BARS * 8 + 16 + 4 * (4 * kMaxE + 4);
 static_assert(PSMEM_BYTES <= 227 * 1024, "pair GEMM shared memory");
+static_assert(PSTAGES % kForwarders == 0, "a stage keeps its forwarder across ring cycles");
 
 struct PairCoord {
   int e, pm, n;
@@ -50,8 +57,8 @@ __device__ __forceinline__ PairCoord decode_pair(int p, const int* pstart, int E
   return c;
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(PNUM_THREADS, 1)
+template <int EPI, bool GA>
+__global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS, 1)
     tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -71,6 +78,7 @@ __global__ void __launch_bounds__(PNUM_THREADS, 1)
   const uint32_t tfull0 = smem_u32(bars + 2 * PSTAGES);
   const uint32_t tempty0 = smem_u32(bars + 2 * PSTAGES + 2);
   const uint32_t drain = smem_u32(bars + 2 * PSTAGES + 4);
+  const uint32_t gfull0 = smem_u32(bars + 2 * PSTAGES + 5);  // gathered A: rows of a stage landed
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E;
@@ -80,7 +88,8 @@ __global__ void __launch_bounds__(PNUM_THREADS, 1)
   pdl_trigger();
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < PSTAGES; ++s) {
-      mbar_init(full0 + 8 * s, 1);   // leader's: one arrive (with both CTAs' bytes) per phase
+      // leader's: one arrive with both CTAs' TMA bytes per phase (+ each CTA's A forwarder)
+      mbar_init(full0 + 8 * s, GA ? 3 : 1);
       mbar_init(empty0 + 8 * s, 1);  // each CTA's: one multicast commit per phase
     }
     for (int i = 0; i < 2; ++i) {
@@ -88,9 +97,11 @@ __global__ void __launch_bounds__(PNUM_THREADS, 1)
       mbar_init(tempty0 + 8 * i, 8);  // leader's: 4 epilogue warps of each CTA
     }
     mbar_init(drain, 1);
+    if constexpr (GA)
+      for (int s = 0; s < PSTAGES; ++s) mbar_init(gfull0 + 8 * s, kGatherThreads);
     *s_abort = 0;
     fence_mbar_init();
-    prefetch_tmap(&tmA);
+    if constexpr (!GA) prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
   }
   if (warp == 1) {
@@ -138,11 +149,12 @@ __global__ void __launch_bounds__(PNUM_THREADS, 1)
           }
           const uint32_t full_leader = mapa_shared(full0 + 8 * stage, 0);
           if (leader) {
-            mbar_arrive_expect_tx(full0 + 8 * stage, 2 * PSTAGE_BYTES);
+            mbar_arrive_expect_tx(full0 + 8 * stage, GA ? 2 * PB_BYTES : 2 * PSTAGE_BYTES);
             armed |= 1u << stage;
             armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           }
-          tma_load_2d_pair(smem_u32(sA + stage * PA_BYTES), &tmA, full_leader, kb * PBK, a_row);
+          if constexpr (!GA)
+            tma_load_2d_pair(smem_u32(sA + stage * PA_BYTES), &tmA, full_leader, kb * PBK, a_row);
           tma_load_2d_pair(smem_u32(sB + stage * PB_BYTES), &tmB, full_leader, kb * PBK, b_row);
           if (++stage == PSTAGES) {
             stage = 0;
@@ -161,6 +173,72 @@ __global__ void __launch_bounds__(PNUM_THREADS, 1)
           mbar_wait(full0 + 8 * s, (armed_phase >> s) & 1u, &never, a.timeout_ns);
         }
     }
+  } else if (GA && warp >= kGatherWarp0 && warp < kForwardWarp0) {
+    // -------------------------------------------------------------- A gather warps
+    AGather g;
+    g.init(a.gather_x, a.K, warp - kGatherWarp0, lane);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    auto prefetch = [&](int p) {
+      if (p >= total) return;
+      const PairCoord c = decode_pair(p, s_pstart, E, a.n_tiles);
+      g.prefetch_tokens(a.token_of_row, s_offsets[c.e] + (2 * c.pm + static_cast<int>(rank)) * PBM,
+                        s_offsets[c.e] + s_counts[c.e]);
+    };
+    prefetch(pair_id);
+    for (int p = pair_id; ok && p < total; p += n_pairs) {
+      g.advance_tile();
+      prefetch(p + n_pairs);
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const bool got = __all_sync(0xffffffffu, mbar_wait(empty0 + 8 * stage, phase ^ 1u, s_abort, a.timeout_ns));
+        if (!got) {
+          ok = false;
+          break;
+        }
+        g.issue(smem_u32(sA + stage * PA_BYTES), kb);
+        cp_async_arrive_noinc(gfull0 + 8 * stage);
+        if (++stage == PSTAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    cp_async_wait<0>();  // nothing of this thread in flight when the CTA leaves
+    if (!ok && lane == 0) {
+      if (!*s_abort) atomicOr(a.status, kStatusTimeoutProducer);
+      *s_abort = 1;
+    }
+  } else if (GA && warp >= kForwardWarp0) {
+    // -------------------------------------------------------------- A forwarders (lane 0 of each forwarder warp)
+    // forwarder f handles the stages s with s % kForwarders == f, so the per-stage wake-up, proxy
+    // fence and arrive of consecutive stages overlap
+    const int fwd = warp - kForwardWarp0;
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int p = pair_id; ok && p < total; p += n_pairs) {
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (stage % kForwarders == fwd) {
+            if (!mbar_wait(gfull0 + 8 * stage, phase, s_abort, a.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive_peer(mapa_shared(full0 + 8 * stage, 0));
+          }
+          if (++stage == PSTAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        if (!*s_abort) atomicOr(a.status, kStatusTimeoutProducer);
+        *s_abort = 1;
+      }
+    }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------------------ MMA issuer (leader only)
@@ -176,7 +254,9 @@ __global__ void __launch_bounds__(PNUM_THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PBN);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(full0 + 8 * stage, phase, s_abort, a.timeout_ns)) {
+          const bool got = GA ? mbar_wait_cluster(full0 + 8 * stage, phase, s_abort, a.timeout_ns)
+                              : mbar_wait(full0 + 8 * stage, phase, s_abort, a.timeout_ns);
+          if (!got) {
             ok = false;
             break;
           }
@@ -208,7 +288,7 @@ __global__ void __launch_bounds__(PNUM_THREADS, 1)
       volatile int never = 0;
       mbar_wait(drain, 0, &never, a.timeout_ns);
     }
-  } else {
+  } else if (warp < 6) {
     // -------------------------------------------------------------- epilogue (warps 2..5, both CTAs)
     const int q = warp & 3;
     int acc = 0;
@@ -332,12 +412,12 @@ __global__ void __launch_bounds__(PNUM_THREADS, 1)
   }
 }
 
-template <int EPI>
+template <int EPI, bool GA>
 cudaError_t launch_pair_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
                           cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(PNUM_THREADS);
+  cfg.blockDim = dim3(GA ? PNUM_THREADS_GA : PNUM_THREADS);
   cfg.dynamicSmemBytes = PSMEM_BYTES;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -349,24 +429,24 @@ cudaError_t launch_pair_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const 
   attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<EPI>, tmA, tmB, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<EPI, GA>, tmA, tmB, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
 
+template <int EPI, bool GA>
+cudaError_t set_pair_smem() {
+  return cudaFuncSetAttribute(tc_pair_gemm_kernel<EPI, GA>, cudaFuncAttributeMaxDynamicSharedMemorySize, PSMEM_BYTES);
+}
+
 cudaError_t prepare_pair_gemm() {
-  cudaError_t e = cudaFuncSetAttribute(tc_pair_gemm_kernel<kEpiSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       PSMEM_BYTES);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(tc_pair_gemm_kernel<kEpiReluBias>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PSMEM_BYTES);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(tc_pair_gemm_kernel<kEpiStoreF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PSMEM_BYTES);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(tc_pair_gemm_kernel<kEpiCombineF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PSMEM_BYTES);
+  cudaError_t e = set_pair_smem<kEpiSwiGLU, false>();
+  if (e == cudaSuccess) e = set_pair_smem<kEpiSwiGLU, true>();
+  if (e == cudaSuccess) e = set_pair_smem<kEpiReluBias, false>();
+  if (e == cudaSuccess) e = set_pair_smem<kEpiReluBias, true>();
+  if (e == cudaSuccess) e = set_pair_smem<kEpiStoreF32, false>();
+  if (e == cudaSuccess) e = set_pair_smem<kEpiCombineF32, false>();
   return e;
 }
 
@@ -384,23 +464,32 @@ int pair_gemm_max_ctas() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, tc_pair_gemm_kernel<kEpiStoreF32>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&clusters, tc_pair_gemm_kernel<kEpiStoreF32, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return 2 * clusters;
 }
 
-// grid: an even number of CTAs (one pair per two SMs)
-cudaError_t launch_pair_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
-                             cudaStream_t s) {
+// grid: an even number of CTAs (one pair per two SMs).  gather_a: A rows are gathered from
+// a.gather_x through a.token_of_row (up-projection epilogues only) and tmA is not read.
+cudaError_t launch_pair_gemm(int epi, bool gather_a, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                             const GemmArgs& a, int grid, cudaStream_t s) {
   grid &= ~1;
   if (grid <= 0) return cudaSuccess;
   switch (epi) {
-    case kEpiSwiGLU: return launch_pair_t<kEpiSwiGLU>(tmA, tmB, a, grid, s);
-    case kEpiReluBias: return launch_pair_t<kEpiReluBias>(tmA, tmB, a, grid, s);
-    case kEpiCombineF32: return launch_pair_t<kEpiCombineF32>(tmA, tmB, a, grid, s);
-    default: return launch_pair_t<kEpiStoreF32>(tmA, tmB, a, grid, s);
+    case kEpiSwiGLU:
+      return gather_a ? launch_pair_t<kEpiSwiGLU, true>(tmA, tmB, a, grid, s)
+                      : launch_pair_t<kEpiSwiGLU, false>(tmA, tmB, a, grid, s);
+    case kEpiReluBias:
+      return gather_a ? launch_pair_t<kEpiReluBias, true>(tmA, tmB, a, grid, s)
+                      : launch_pair_t<kEpiReluBias, false>(tmA, tmB, a, grid, s);
+    case kEpiCombineF32:
+      if (gather_a) return cudaErrorInvalidValue;
+      return launch_pair_t<kEpiCombineF32, false>(tmA, tmB, a, grid, s);
+    default:
+      if (gather_a) return cudaErrorInvalidValue;
+      return launch_pair_t<kEpiStoreF32, false>(tmA, tmB, a, grid, s);
   }
 }
 

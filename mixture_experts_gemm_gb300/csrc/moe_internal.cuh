@@ -67,7 +67,7 @@ struct GatherArgs {
   int T, d, E;             // E = scheduled experts (Ex)
   int S;
   int64_t rows_alloc;
-  void* xp;                // [rows_alloc, d]
+  void* xp;                // [rows_alloc, d], or nullptr: bookkeeping only (A gathered by the GEMM)
   int32_t* token_of_row;   // [rows_alloc]
   Sched* sched;
   const float* gate;       // [T, S]
@@ -102,8 +102,9 @@ struct GemmArgs {
   int out_cols;             // output columns per expert (f for up, d for down)
   uint64_t timeout_ns;      // bound on every wait inside the kernel
   int32_t* status;          // device status word (Sched::status)
-  const int32_t* token_of_row;  // kEpiCombineF32: token of each row
+  const int32_t* token_of_row;  // kEpiCombineF32 and gathered A: token of each row
   const float* gate_of_row;     // kEpiCombineF32: gate of each row
+  const void* gather_x;         // gathered A: token rows x [T, K] bf16 (16-byte aligned rows)
 };
 
 // Decode (weight-streaming) GEMM: P[s][tok][row] partial sums over K split s.
@@ -183,8 +184,8 @@ cudaError_t pdl_launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 cudaError_t launch_router(int dtype, const RouterArgs& a, int nchunks, cudaStream_t s);
 cudaError_t launch_gather(int dtype, const GatherArgs& a, cudaStream_t s);
 cudaError_t launch_combine(int out_dtype, const CombineArgs& a, int num_sms, cudaStream_t s);
-cudaError_t launch_tc_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                           int grid, cudaStream_t s);
+cudaError_t launch_tc_gemm(int epi, bool gather_a, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_simt_gemm(int epi, const SimtGemmArgs& a, int max_mtiles, cudaStream_t s);
 int router_smem_bytes(int dtype, int E, int dchunk);
 // One-time kernel attribute set-up (dynamic shared memory limits) for the current device.
@@ -193,8 +194,8 @@ cudaError_t prepare_tc_gemm();
 cudaError_t prepare_decode_gemm();
 cudaError_t prepare_pair_gemm();
 int pair_gemm_max_ctas();
-cudaError_t launch_pair_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
-                             cudaStream_t s);
+cudaError_t launch_pair_gemm(int epi, bool gather_a, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                             const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_decode_gemm(const CUtensorMap& tmW, const CUtensorMap& tmX, const DecodeArgs& a, int grid,
                                cudaStream_t s);
 cudaError_t launch_decode_act(bool swiglu, const DecodeActArgs& a, cudaStream_t s);

@@ -80,9 +80,45 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherArgs a, in
   }
 }
 
+// Bookkeeping only, for the path whose up GEMM gathers its A rows from x itself: one thread per
+// token, same rows as gather_kernel.
+__global__ void __launch_bounds__(kGatherThreads) dispatch_rows_kernel(GatherArgs a) {
+  const int t = blockIdx.x * kGatherThreads + threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
+  if (t >= a.T) return;
+  const int chunk = t / kRouterChunk;
+  const int S = a.S;
+  int r[kMaxSlots];
+  bool ok = true;
+#pragma unroll
+  for (int s = 0; s < kMaxSlots; ++s) {
+    r[s] = 0;
+    if (s < S) {
+      const int e = a.idx[(size_t)S * t + s];
+      r[s] = a.chunk_base[(size_t)chunk * a.E + e] + a.row_of[(size_t)S * t + s];
+      ok = ok && r[s] >= 0 && r[s] < a.rows_alloc;
+    }
+  }
+  if (!ok) {
+    atomicOr(&a.sched->status, kStatusBadRow);
+    return;
+  }
+#pragma unroll
+  for (int s = 0; s < kMaxSlots; ++s)
+    if (s < S) {
+      a.row_of[(size_t)S * t + s] = r[s];
+      a.token_of_row[r[s]] = t;
+      if (a.gate_of_row) a.gate_of_row[r[s]] = a.gate[(size_t)S * t + s];
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_gather(int dtype, const GatherArgs& a, cudaStream_t s) {
+  if (a.xp == nullptr)
+    return pdl_launch(dispatch_rows_kernel, dim3((a.T + kGatherThreads - 1) / kGatherThreads), dim3(kGatherThreads),
+                      0, s, a);
   const int per = kGatherThreads / 32;
   const int wpt = a.T >= 1024 ? 1 : (a.T >= 256 ? 2 : (a.T >= 64 ? 4 : 8));
   const int grid = (a.T * wpt + per - 1) / per;

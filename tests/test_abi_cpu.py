@@ -72,6 +72,7 @@ def test_null_arguments(cuda_lib):
     assert L.colibri_moe_set_stage_events(None, None, 0) == -1
     n = ctypes.c_int32()
     assert L.colibri_moe_num_stages(None, ctypes.byref(n)) == -1
+    assert L.colibri_moe_last_kernel_count(None, ctypes.byref(n)) == -1
     L.colibri_moe_destroy(None)  # NULL-safe
 
 

@@ -235,6 +235,34 @@ def test_fused_combine_equals_separate_combine(gemm, monkeypatch):
     assert np.array_equal(out_f, out_s)
 
 
+@pytest.mark.parametrize("gemm", ["2sm", "1sm"])
+def test_gathered_a_rows_equal_copied_xp(gemm, monkeypatch):
+    """The up GEMM reading its A rows from x through token_of_row (cp.async gather warps) multiplies the same
+    bf16 values as the GEMM over the materialised Xp, so H and the output agree bit for bit.  Cases:
+    ragged expert segments (odd tile counts, empty experts), ReLU+bias, top-4 with a shared expert."""
+    monkeypatch.setenv("COLIBRI_MOE_GEMM", gemm)
+    cases = [
+        testgen.LayerShape("ga-swiglu", 900, 512, 384, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True),
+        testgen.LayerShape("ga-relu", 300, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16"),
+        testgen.LayerShape("ga-k4-shared", 700, 512, 384, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True,
+                           top_k=4, shared_expert=True),
+    ]
+    for shape in cases:
+        li = testgen.make_inputs(shape)
+        monkeypatch.setenv("COLIBRI_MOE_GATHER", "fused")
+        layer_g, out_g, r, _, _ = _full_check(li)
+        monkeypatch.delenv("COLIBRI_MOE_GATHER")
+        layer_c, out_c, _, _, _ = _full_check(li)
+        assert np.array_equal(out_g, out_c), shape.name
+        rows = np.sort(r["row_of"].ravel())
+        if shape.shared_expert:
+            off = r["offsets"]
+            rows = np.concatenate([rows, np.arange(off[-1], off[-1] + shape.T)])
+        Hg = layer_g.debug_tensor(1).float().cpu().numpy()[rows]
+        Hc = layer_c.debug_tensor(1).float().cpu().numpy()[rows]
+        assert np.array_equal(Hg, Hc), shape.name
+
+
 @pytest.mark.parametrize("T", [24, 900])
 def test_forward_replays_from_a_cuda_graph(T):
     """forward allocates nothing and never synchronises, so it can be captured into a CUDA graph; the
@@ -404,6 +432,25 @@ def test_error_paths():
     with pytest.raises(ColibriError) as e:
         MoELayer(250, 256, 4, 64)
     assert e.value.code == -6   # d not a multiple of 8
+
+
+def test_last_kernel_count_matches_the_path(monkeypatch):
+    shape = testgen.LayerShape("count", 300, 512, 384, 8, testgen.ACT_SWIGLU, "bf16")
+    li = testgen.make_inputs(shape)
+    layer = make_layer(li)
+    assert layer.last_kernel_count() == 0
+    x = x_device(li)
+    layer.forward(x)
+    assert layer.last_kernel_count() == 4          # router, dispatch, up GEMM, down GEMM + combine
+    layer.forward(x[:20].contiguous())
+    assert layer.last_kernel_count() == 6          # decode: router, dispatch, 2 x (GEMM, reduction)
+    layer.forward(x[:0])
+    assert layer.last_kernel_count() == 0
+    monkeypatch.setenv("COLIBRI_MOE_FUSED_COMBINE", "0")
+    layer2 = make_layer(li)
+    layer2.forward(x)
+    assert layer2.last_kernel_count() == 5
+    torch.cuda.synchronize()
 
 
 def test_stage_events_time_every_stage():
