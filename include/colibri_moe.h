@@ -133,6 +133,21 @@ COLIBRI_API int colibri_moe_forward(colibri_moe_t* ctx, const void* x, void* out
  * asynchronous copies; pageable memory works but copies synchronously. */
 COLIBRI_API int colibri_moe_forward_host(colibri_moe_t* ctx, const void* x_host, void* out_host, int32_t T, void* stream);
 
+/* Pipelined form of forward_host for serving loops (no counterpart in the articles, which run one
+ * synchronous batch at a time): returns without waiting.  The context keeps two device staging
+ * slots used in turn and two internal copy streams, so the host->device copy of one call and the
+ * device->host copy of the previous one overlap the forwards on `stream`.  The forward is enqueued
+ * on `stream` after this call's input copy; the result copy is ordered after it on an internal
+ * stream.  out_host holds the result, and x_host may be reused, once colibri_moe_host_sync returns
+ * (until then the copies may still be reading or writing them).  Host buffers should be pinned:
+ * pageable memory makes the copies synchronous.  Calls on one context must use one `stream` (or be
+ * ordered by the caller).  Errors as forward; -4 if a copy or event call fails. */
+COLIBRI_API int colibri_moe_forward_host_async(colibri_moe_t* ctx, const void* x_host, void* out_host, int32_t T,
+                                               void* stream);
+
+/* Waits until every copy of earlier forward_host_async calls has completed. */
+COLIBRI_API int colibri_moe_host_sync(colibri_moe_t* ctx);
+
 /* Routing of the most recent forward, copied into caller DEVICE buffers on `stream` (any may be
  * NULL): idx[T,k] int32 (slot 0 = highest logit), gate[T,k] fp32, counts[E] int32 (routed
  * experts), offsets[E+1] int32 (row where each routed expert's segment starts; segments padded to

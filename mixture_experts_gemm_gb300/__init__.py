@@ -33,6 +33,7 @@ _ACTS = {"relu_bias": ACT_RELU_BIAS, "relu": ACT_RELU_BIAS, "swiglu": ACT_SWIGLU
 # every function include/colibri_moe.h declares
 EXPORTED = ("colibri_moe_create", "colibri_moe_load_weights", "colibri_moe_forward", "colibri_moe_forward_host",
             "colibri_moe_get_routing", "colibri_moe_debug_buffer", "colibri_moe_num_stages",
+            "colibri_moe_forward_host_async", "colibri_moe_host_sync",
             "colibri_moe_last_kernel_count", "colibri_moe_set_stage_events", "colibri_moe_device_status",
             "colibri_moe_route_noalloc",
             "colibri_moe_destroy", "colibri_moe_strerror")
@@ -75,6 +76,8 @@ def lib() -> ctypes.CDLL:
             "colibri_moe_load_weights": ([vp, ctypes.POINTER(Weights), vp], ctypes.c_int),
             "colibri_moe_forward": ([vp, vp, vp, i32, vp], ctypes.c_int),
             "colibri_moe_forward_host": ([vp, vp, vp, i32, vp], ctypes.c_int),
+            "colibri_moe_forward_host_async": ([vp, vp, vp, i32, vp], ctypes.c_int),
+            "colibri_moe_host_sync": ([vp], ctypes.c_int),
             "colibri_moe_get_routing": ([vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
             "colibri_moe_debug_buffer": ([vp, i32, ctypes.POINTER(vp), ctypes.POINTER(i64)], ctypes.c_int),
             "colibri_moe_num_stages": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
@@ -215,6 +218,16 @@ class MoELayer:
         _check(lib().colibri_moe_forward_host(self._h, _ptr(x_host), _ptr(out_host), T, _stream_handle(stream)),
                "colibri_moe_forward_host")
         return out_host
+
+    def forward_host_async(self, x_host, out_host, stream=None):
+        """Pipelined host-buffer forward: returns at once; out_host is valid after host_sync()."""
+        T = x_host.shape[0]
+        _check(lib().colibri_moe_forward_host_async(self._h, _ptr(x_host), _ptr(out_host), T,
+                                                    _stream_handle(stream)), "colibri_moe_forward_host_async")
+        return out_host
+
+    def host_sync(self):
+        _check(lib().colibri_moe_host_sync(self._h), "colibri_moe_host_sync")
 
     def get_routing(self, T: int, stream=None):
         """Routing of the last forward (T tokens) as CUDA tensors."""

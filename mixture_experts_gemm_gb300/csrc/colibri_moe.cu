@@ -67,8 +67,14 @@ struct colibri_moe {
   float* gate_of_row = nullptr;
   int32_t* hist = nullptr;
   Sched* sched = nullptr;
-  void* x_stage = nullptr;
+  void* x_stage = nullptr;    // forward_host staging (also slot 0 of the pipelined host path)
   void* out_stage = nullptr;
+  // pipelined host path (forward_host_async): two staging slots, copy streams and their events
+  void* x_stage2 = nullptr;
+  void* out_stage2 = nullptr;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_done[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr};
+  int slot = 0;
 
   CUtensorMap tm_xp{}, tm_h{}, tm_w13{}, tm_w2{};
   // decode path (T <= decode_max_t): 128-row weight boxes, token boxes of 16/32/48/64 rows
@@ -228,6 +234,15 @@ void colibri_moe_destroy(colibri_moe_t* ctx) {
   if (!ctx) return;
   {
     DeviceGuard g(ctx->device);
+    if (ctx->h2d) cudaStreamSynchronize(ctx->h2d);
+    if (ctx->d2h) cudaStreamSynchronize(ctx->d2h);
+    for (int i = 0; i < 2; ++i) {
+      if (ctx->ev_in[i]) cudaEventDestroy(ctx->ev_in[i]);
+      if (ctx->ev_done[i]) cudaEventDestroy(ctx->ev_done[i]);
+      if (ctx->ev_free[i]) cudaEventDestroy(ctx->ev_free[i]);
+    }
+    if (ctx->h2d) cudaStreamDestroy(ctx->h2d);
+    if (ctx->d2h) cudaStreamDestroy(ctx->d2h);
     if (ctx->warena) cudaFree(ctx->warena);
     if (ctx->ws) cudaFree(ctx->ws);
   }
@@ -309,6 +324,8 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   const size_t o_part = carve(part_floats * 4);
   const size_t o_xs = carve(T * d * c->esize);
   const size_t o_os = carve(T * d * c->out_esize);
+  const size_t o_xs2 = carve(T * d * c->esize);
+  const size_t o_os2 = carve(T * d * c->out_esize);
   c->ws_bytes = off;
   if (cudaMalloc(&c->ws, c->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -329,6 +346,19 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   c->partial = part_floats > 0 ? reinterpret_cast<float*>(b + o_part) : nullptr;
   c->x_stage = b + o_xs;
   c->out_stage = b + o_os;
+  c->x_stage2 = b + o_xs2;
+  c->out_stage2 = b + o_os2;
+  bool streams_ok = cudaStreamCreateWithFlags(&c->h2d, cudaStreamNonBlocking) == cudaSuccess &&
+                    cudaStreamCreateWithFlags(&c->d2h, cudaStreamNonBlocking) == cudaSuccess;
+  for (int i = 0; i < 2 && streams_ok; ++i)
+    streams_ok = cudaEventCreateWithFlags(&c->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&c->ev_done[i], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&c->ev_free[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!streams_ok) {
+    cudaGetLastError();
+    colibri_moe_destroy(c);
+    return COLIBRI_ERR_CUDA;
+  }
   if (cudaMemset(c->ws, 0, c->ws_bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
     colibri_moe_destroy(c);
@@ -611,7 +641,10 @@ int colibri_moe_forward_host(colibri_moe_t* ctx, const void* x_host, void* out_h
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t xb = static_cast<size_t>(T) * ctx->cfg.d_model * ctx->esize;
   const size_t ob = static_cast<size_t>(T) * ctx->cfg.d_model * ctx->out_esize;
-  if (cudaMemcpyAsync(ctx->x_stage, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+  // after any pipelined call still copying out of the staging slots
+  if (cudaStreamWaitEvent(s, ctx->ev_free[0], 0) != cudaSuccess ||
+      cudaStreamWaitEvent(s, ctx->ev_free[1], 0) != cudaSuccess ||
+      cudaMemcpyAsync(ctx->x_stage, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
     cudaGetLastError();
     return COLIBRI_ERR_CUDA;
   }
@@ -619,6 +652,54 @@ int colibri_moe_forward_host(colibri_moe_t* ctx, const void* x_host, void* out_h
   if (rc) return rc;
   if (cudaMemcpyAsync(out_host, ctx->out_stage, ob, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return COLIBRI_ERR_CUDA;
+  }
+  return COLIBRI_OK;
+}
+
+int colibri_moe_forward_host_async(colibri_moe_t* ctx, const void* x_host, void* out_host, int32_t T,
+                                   void* stream) {
+  if (!ctx) return COLIBRI_ERR_INVALID_ARG;
+  if (T < 0 || T > ctx->cfg.max_tokens) return COLIBRI_ERR_INVALID_ARG;
+  if (!ctx->loaded) return COLIBRI_ERR_STATE;
+  if (T == 0) {
+    ctx->last_kernels = 0;
+    return COLIBRI_OK;
+  }
+  if (!x_host || !out_host) return COLIBRI_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return COLIBRI_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int k = ctx->slot;
+  void* xs = k ? ctx->x_stage2 : ctx->x_stage;
+  void* os = k ? ctx->out_stage2 : ctx->out_stage;
+  const size_t xb = static_cast<size_t>(T) * ctx->cfg.d_model * ctx->esize;
+  const size_t ob = static_cast<size_t>(T) * ctx->cfg.d_model * ctx->out_esize;
+  // slot k is free once the call two back has copied its result out (its forward read x before)
+  if (cudaStreamWaitEvent(ctx->h2d, ctx->ev_free[k], 0) != cudaSuccess ||
+      cudaMemcpyAsync(xs, x_host, xb, cudaMemcpyHostToDevice, ctx->h2d) != cudaSuccess ||
+      cudaEventRecord(ctx->ev_in[k], ctx->h2d) != cudaSuccess || cudaStreamWaitEvent(s, ctx->ev_in[k], 0) != cudaSuccess) {
+    cudaGetLastError();
+    return COLIBRI_ERR_CUDA;
+  }
+  const int rc = enqueue_forward(ctx, xs, os, T, s);
+  if (rc) return rc;
+  if (cudaEventRecord(ctx->ev_done[k], s) != cudaSuccess || cudaStreamWaitEvent(ctx->d2h, ctx->ev_done[k], 0) != cudaSuccess ||
+      cudaMemcpyAsync(out_host, os, ob, cudaMemcpyDeviceToHost, ctx->d2h) != cudaSuccess ||
+      cudaEventRecord(ctx->ev_free[k], ctx->d2h) != cudaSuccess) {
+    cudaGetLastError();
+    return COLIBRI_ERR_CUDA;
+  }
+  ctx->slot = k ^ 1;
+  return COLIBRI_OK;
+}
+
+int colibri_moe_host_sync(colibri_moe_t* ctx) {
+  if (!ctx) return COLIBRI_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return COLIBRI_ERR_CUDA;
+  if (cudaStreamSynchronize(ctx->h2d) != cudaSuccess || cudaStreamSynchronize(ctx->d2h) != cudaSuccess) {
     cudaGetLastError();
     return COLIBRI_ERR_CUDA;
   }

@@ -67,6 +67,8 @@ def test_null_arguments(cuda_lib):
     assert L.colibri_moe_create(None, 0, None) == -1
     assert L.colibri_moe_forward(None, None, None, 4, None) == -1
     assert L.colibri_moe_forward_host(None, None, None, 4, None) == -1
+    assert L.colibri_moe_forward_host_async(None, None, None, 4, None) == -1
+    assert L.colibri_moe_host_sync(None) == -1
     assert L.colibri_moe_load_weights(None, None, None) == -1
     assert L.colibri_moe_get_routing(None, None, None, None, None, None, None) == -1
     assert L.colibri_moe_set_stage_events(None, None, 0) == -1

@@ -434,6 +434,34 @@ def test_error_paths():
     assert e.value.code == -6   # d not a multiple of 8
 
 
+def test_pipelined_host_forward_matches_device_forward():
+    """forward_host_async: calls overlap their copies with the neighbouring forwards through two
+    staging slots; every result must equal the device forward of its own input bit for bit, also
+    when a synchronous forward_host call is interleaved."""
+    shape = testgen.LayerShape("async", 600, 512, 384, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True)
+    li = testgen.make_inputs(shape)
+    layer = make_layer(li)
+    xs = [x_device(li)]
+    for sd in (1, 2, 3):
+        _, bits = testgen.make_x(shape, seed=sd, want_f32=False)
+        xs.append(torch_from_bits(bits).cuda())
+    refs = [layer.forward(x).cpu() for x in xs]
+    xh = [x.cpu().pin_memory() for x in xs]
+    oh = [torch.empty_like(r).pin_memory() for r in refs]
+    for rep in range(2):
+        for i in range(len(xs)):
+            layer.forward_host_async(xh[i], oh[i])
+        if rep == 0:
+            o_sync = torch.empty_like(refs[0]).pin_memory()
+            layer.forward_host(xh[2], o_sync)
+            assert torch.equal(o_sync, refs[2])
+        layer.host_sync()
+        for i in range(len(xs)):
+            assert torch.equal(oh[i], refs[i]), (rep, i)
+            oh[i].zero_()
+    assert layer.device_status() == 0
+
+
 def test_last_kernel_count_matches_the_path(monkeypatch):
     shape = testgen.LayerShape("count", 300, 512, 384, 8, testgen.ACT_SWIGLU, "bf16")
     li = testgen.make_inputs(shape)
