@@ -509,16 +509,20 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   if (max_mtiles > ctx->rows_alloc / kRowTile) max_mtiles = ctx->rows_alloc / kRowTile;
 
   // Two slots with an fp32 output on the prefill path: the down GEMM adds g * y straight into out
-  // (cleared by the router); two fp32 additions onto zero give the same value in either order.
+  // (cleared first); two fp32 additions onto zero give the same value in either order.
   const bool decode = bf16 && T <= ctx->decode_max_t;
   const bool fuse = bf16 && !decode && ctx->fuse_combine && ctx->S == 2 && c.out_dtype == COLIBRI_DTYPE_F32;
   // bf16 prefill: the up GEMM gathers its A rows from x through token_of_row instead of reading a
   // materialised Xp; the dispatch kernel then only writes the row bookkeeping.
   const bool gather_a = bf16 && !decode && ctx->gather_a;
   mark(0);
+  // With the combine fused, out is cleared before the down GEMM adds into it: by extra warps of the
+  // (tensor-bound) up GEMM, or by the router on the gathered-A path whose extra warps gather.
+  float4* const clear_in_gemm = fuse && !gather_a ? static_cast<float4*>(out) : nullptr;
+  const int64_t out_vec4 = static_cast<int64_t>(T) * d / 4;
   RouterArgs ra{x, ctx->w_router, ctx->b_router, T, d, c.num_experts, ctx->dchunk, ctx->idx, ctx->gate,
                 ctx->row_of, ctx->hist, ctx->sched, ctx->k, c.gate_mode, c.has_shared_expert, ctx->S, ctx->Ex,
-                fuse ? static_cast<float*>(out) : nullptr};
+                fuse && gather_a ? static_cast<float*>(out) : nullptr};
   if (launch_router(c.dtype, ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   mark(1);
   GatherArgs ga{x, ctx->idx, ctx->row_of, ctx->hist, T, d, E, ctx->S, ctx->rows_alloc,
@@ -556,7 +560,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     const int bn = tc_gemm_block_n();
     const int64_t max_pairs = (max_mtiles + E + 1) / 2;
     GemmArgs up{ctx->sched, E, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns,
-                &ctx->sched->status, ctx->tok_of_row, nullptr, x};
+                &ctx->sched->status, ctx->tok_of_row, nullptr, x, clear_in_gemm, out_vec4};
     int64_t ctas = 2 * max_pairs * up.n_tiles;
     int grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
     if (launch_pair_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, gather_a, ctx->tm_xp, ctx->tm_w13_dec, up, grid, s) !=
@@ -573,7 +577,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   } else if (bf16) {
     const int bn = tc_gemm_block_n();
     GemmArgs up{ctx->sched, E, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns,
-                &ctx->sched->status, ctx->tok_of_row, nullptr, x};
+                &ctx->sched->status, ctx->tok_of_row, nullptr, x, clear_in_gemm, out_vec4};
     int64_t tiles = max_mtiles * up.n_tiles;
     int grid = static_cast<int>(tiles < ctx->num_sms ? tiles : ctx->num_sms);
     if (launch_tc_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, gather_a, ctx->tm_xp, ctx->tm_w13, up, grid, s) !=

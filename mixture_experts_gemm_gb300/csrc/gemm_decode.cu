@@ -99,7 +99,10 @@ __global__ void __launch_bounds__(DNUM_THREADS, 1)
     tmem_alloc(smem_u32(tmem_slot), DTMEM_COLS);
     tmem_relinquish();
   }
-  pdl_wait();  // the routing summary and the token rows come from earlier kernels
+  // The routing summary (Sched) comes from the router, two or more kernels back.  The kernel right
+  // before this one triggers its dependents only after its own griddepcontrol.wait, so this grid
+  // starts after the router has finished and may read Sched before waiting.  The token rows (Xp or
+  // H) and the partial-sum buffer belong to the kernel right before: touched only after pdl_wait.
   if (threadIdx.x < kMaxE) s_counts[threadIdx.x] = threadIdx.x < E ? a.sched->counts[threadIdx.x] : 0;
   if (threadIdx.x < kMaxE + 1) s_offsets[threadIdx.x] = threadIdx.x <= E ? a.sched->offsets[threadIdx.x] : 0;
   if (threadIdx.x == 0) *s_nact = active_experts(a.sched, E, s_act);
@@ -116,9 +119,23 @@ __global__ void __launch_bounds__(DNUM_THREADS, 1)
   const int n_pad = a.n_pad;
   const uint32_t b_bytes = static_cast<uint32_t>(n_pad) * DBK * 2;
 
+  if (!(warp == 0 && lane == 0)) pdl_wait();
   if (warp == 0) {
     if (lane == 0) {
-      int stage = 0;
+      // The weights do not depend on the previous kernel: the weight tiles of the first DSTAGES
+      // stages are requested before waiting for it (their full barriers expect the token bytes too)
+      int pre = 0;
+      for (int it = blockIdx.x; pre < DSTAGES && it < total; it += gridDim.x) {
+        const int ai = it / (MT * S), r = it - ai * (MT * S), mt = r / S, sp = r - (r / S) * S;
+        const int kb0 = (KB * sp) / S, kb1 = (KB * (sp + 1)) / S;
+        const int w_row = s_act[ai] * a.n_per_expert + mt * DBM;
+        for (int kb = kb0; kb < kb1 && pre < DSTAGES; ++kb, ++pre) {
+          mbar_arrive_expect_tx(full0 + 8 * pre, DA_BYTES + b_bytes);
+          tma_load_2d(smem_u32(sA + pre * DA_BYTES), &tmW, full0 + 8 * pre, kb * DBK, w_row);
+        }
+      }
+      pdl_wait();
+      int stage = 0, g = 0;
       uint32_t phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
       for (int it = blockIdx.x; ok && it < total; it += gridDim.x) {
@@ -127,15 +144,17 @@ __global__ void __launch_bounds__(DNUM_THREADS, 1)
         const int kb0 = (KB * sp) / S, kb1 = (KB * (sp + 1)) / S;
         const int w_row = e * a.n_per_expert + mt * DBM;
         const int x_row = s_offsets[e];
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, s_abort, a.timeout_ns)) {
-            ok = false;
-            break;
+        for (int kb = kb0; kb < kb1; ++kb, ++g) {
+          if (g >= pre) {  // stages before `pre` are in their first round: free, weights in flight
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, s_abort, a.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(full0 + 8 * stage, DA_BYTES + b_bytes);
+            tma_load_2d(smem_u32(sA + stage * DA_BYTES), &tmW, full0 + 8 * stage, kb * DBK, w_row);
           }
-          mbar_arrive_expect_tx(full0 + 8 * stage, DA_BYTES + b_bytes);
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-          tma_load_2d(smem_u32(sA + stage * DA_BYTES), &tmW, full0 + 8 * stage, kb * DBK, w_row);
           tma_load_2d(smem_u32(sB + stage * DB_SLOT), &tmX, full0 + 8 * stage, kb * DBK, x_row);
           if (++stage == DSTAGES) {
             stage = 0;
@@ -254,8 +273,8 @@ __global__ void __launch_bounds__(256) decode_act_kernel(DecodeActArgs a) {
   __shared__ int s_act[kMaxE];
   __shared__ int s_S;
   const int e = blockIdx.y;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // after the wait: the down GEMM reads the router's summary before its own wait
   const int cnt = a.sched->counts[e];
   if (cnt == 0) return;
   if (threadIdx.x == 0) {

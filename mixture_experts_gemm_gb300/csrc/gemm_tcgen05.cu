@@ -44,6 +44,7 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS_ZERO = 192 + 32 * kZeroWarps;  // + the warps clearing out (up GEMM)
 constexpr int NUM_THREADS_GA = 192 + 32 * (kGatherWarps + kForwarders);  // + A gather and forwarder warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int NUM_BARS = 3 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain, gfull
@@ -68,7 +69,7 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const int* mtile_star
 }
 
 template <int EPI, bool GA>
-__global__ void __launch_bounds__(GA ? NUM_THREADS_GA : NUM_THREADS, 1)
+__global__ void __launch_bounds__(GA ? NUM_THREADS_GA : NUM_THREADS_ZERO, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -401,6 +402,9 @@ __global__ void __launch_bounds__(GA ? NUM_THREADS_GA : NUM_THREADS, 1)
         acc_phase ^= 1u;
       }
     }
+  } else if (!GA && a.zero_out != nullptr) {
+    // -------------------------------------------------------------- clearing warps (up GEMM)
+    clear_share(a.zero_out, a.zero_vec4, blockIdx.x, gridDim.x, threadIdx.x - 32 * kZeroWarp0);
   }
 
   tc_fence_before();
@@ -413,8 +417,8 @@ __global__ void __launch_bounds__(GA ? NUM_THREADS_GA : NUM_THREADS, 1)
 
 template <int EPI, bool GA>
 cudaError_t launch_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid, cudaStream_t s) {
-  return pdl_launch(tc_grouped_gemm_kernel<EPI, GA>, dim3(grid), dim3(GA ? NUM_THREADS_GA : NUM_THREADS), SMEM_BYTES,
-                    s, tmA, tmB, a);
+  const int threads = GA ? NUM_THREADS_GA : (a.zero_out ? NUM_THREADS_ZERO : NUM_THREADS);
+  return pdl_launch(tc_grouped_gemm_kernel<EPI, GA>, dim3(grid), dim3(threads), SMEM_BYTES, s, tmA, tmB, a);
 }
 
 template <int EPI, bool GA>

@@ -34,6 +34,7 @@ constexpr int PA_BYTES = PBM * PBK * 2;         // 16 KB: this CTA's A rows
 constexpr int PB_BYTES = (PBN / 2) * PBK * 2;   // 16 KB: this CTA's half of B
 constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
 constexpr int PNUM_THREADS = 192;
+constexpr int PNUM_THREADS_ZERO = 192 + 32 * kZeroWarps;  // + the warps clearing out (up GEMM)
 constexpr int PNUM_THREADS_GA = 192 + 32 * (kGatherWarps + kForwarders);  // + A gather and forwarder warps
 constexpr uint32_t PTMEM_COLS = 512;
 constexpr int PNUM_BARS = 3 * PSTAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain, gfull
@@ -58,7 +59,7 @@ __device__ __forceinline__ PairCoord decode_pair(int p, const int* pstart, int E
 }
 
 template <int EPI, bool GA>
-__global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS, 1)
+__global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
     tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -402,6 +403,9 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS, 1)
         acc_phase ^= 1u;
       }
     }
+  } else if (!GA && a.zero_out != nullptr) {
+    // -------------------------------------------------------------- clearing warps (up GEMM)
+    clear_share(a.zero_out, a.zero_vec4, blockIdx.x, gridDim.x, threadIdx.x - 32 * kZeroWarp0);
   }
 
   tc_fence_before();
@@ -417,7 +421,7 @@ cudaError_t launch_pair_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const 
                           cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(GA ? PNUM_THREADS_GA : PNUM_THREADS);
+  cfg.blockDim = dim3(GA ? PNUM_THREADS_GA : (a.zero_out ? PNUM_THREADS_ZERO : PNUM_THREADS));
   cfg.dynamicSmemBytes = PSMEM_BYTES;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];

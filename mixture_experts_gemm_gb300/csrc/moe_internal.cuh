@@ -105,7 +105,21 @@ struct GemmArgs {
   const int32_t* token_of_row;  // kEpiCombineF32 and gathered A: token of each row
   const float* gate_of_row;     // kEpiCombineF32: gate of each row
   const void* gather_x;         // gathered A: token rows x [T, K] bf16 (16-byte aligned rows)
+  float4* zero_out;             // up GEMM with the combine fused downstream: out cleared by two extra
+  int64_t zero_vec4;            //   warps per CTA (zero_vec4 float4s), else nullptr
 };
+
+constexpr int kZeroWarp0 = 6;   // the clearing warps follow producer, MMA and the 4 epilogue warps
+constexpr int kZeroWarps = 2;
+
+// Clears this CTA's share of out[0 .. n4) (float4s) with streaming stores: the share of CTA c of g
+// is [c*n4/g, (c+1)*n4/g).  Run by the kZeroWarps extra warps while the mainloop is tensor-bound,
+// so the 4 bytes per output element cost no step time.
+__device__ __forceinline__ void clear_share(float4* out, int64_t n4, int cta, int nctas, int tid) {
+  const int64_t b = n4 * cta / nctas, e = n4 * (cta + 1) / nctas;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t i = b + tid; i < e; i += 32 * kZeroWarps) __stcs(out + i, z);
+}
 
 // Decode (weight-streaming) GEMM: P[s][tok][row] partial sums over K split s.
 struct DecodeArgs {

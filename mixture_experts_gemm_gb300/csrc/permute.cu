@@ -21,8 +21,8 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherArgs a, in
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gw = blockIdx.x * (kGatherThreads / 32) + warp;
   const int t = gw / wpt, part = gw - t * wpt;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // after the wait: the next kernel may then read what the router wrote before waiting
   if (t >= a.T) return;
   const int chunk = t / kRouterChunk;
   const int S = a.S;
@@ -84,8 +84,8 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherArgs a, in
 // token, same rows as gather_kernel.
 __global__ void __launch_bounds__(kGatherThreads) dispatch_rows_kernel(GatherArgs a) {
   const int t = blockIdx.x * kGatherThreads + threadIdx.x;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // after the wait: the next kernel may then read what the router wrote before waiting
   if (t >= a.T) return;
   const int chunk = t / kRouterChunk;
   const int S = a.S;
