@@ -358,7 +358,12 @@ def main():
     mean_stage = stage_ms.mean(axis=0)
     dur = float(dom_ms.mean()) / 1e3  # live, inside the timed region
     timed_note = f"CUDA events around the kernel on {len(dom_steps)} of the {args.steps} timed steps"
-    if shape.dtype == "bf16" and T >= 256 and dominant in (2, 3):
+    # the binding roofline follows the layer's arithmetic intensity against the ridge point of the
+    # measured peaks: tensor above it, HBM over the active experts' weights below it
+    ridge = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])) * 1e12 / \
+        (float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])) * 1e9)
+    tensor_bound = alg["flops"] / alg["bytes"] > ridge
+    if shape.dtype == "bf16" and tensor_bound and dominant in (2, 3):
         fl = alg["flops_up"] if dominant == 2 else alg["flops_down"]
         ach = fl / dur / 1e12
         # timed inside a seconds-long loop of steps: the sustained (power-capped) peak applies
@@ -382,6 +387,9 @@ def main():
                 "frac": ach / peak, "traffic": NCU_TRAFFIC.get((shape.name, T, STAGES[dominant], "decode")),
                 "peak_source": f"{peak_src} copy", "algorithmic_bytes_per_launch": byts,
                 "step_frac_of_hbm": alg["bytes"] / (ms_per_step / 1e3) / 1e9 / peak, "timing": timed_note}
+
+    roof["layer_flop_per_byte"] = alg["flops"] / alg["bytes"]
+    roof["ridge_flop_per_byte"] = ridge
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
