@@ -1,9 +1,12 @@
 // fp32 grouped expert GEMM on the SIMT FMA pipes (the fp32 dtype path).
 //
 // tcgen05 has no fp32-input kind and TF32 (10-bit mantissa) cannot hold fp32 parity, so fp32
-// layers run here: one CTA per (expert, 128-row tile, 64-column tile), 256 threads with an 8x4
-// register tile each, K staged through shared memory 16 at a time.  Each expert is an affine layer
-// out = in W^T (+ b) with W stored [out, in] (hnwysp.cn/news/30485 3.2), two layers per expert
+// layers run here: one CTA per (expert, 32-row slice of a 128-row tile, 64-column tile), 256
+// threads with a 2x4 register tile each (slices past the expert's rows exit at once, so the work
+// follows the real row count), K staged through shared memory 32 at a time; the global loads of the next K
+// slab are issued into registers before the current slab is multiplied, so their latency overlaps
+// the FMAs (these layers are small: latency, not FMA throughput, sets their time).  Each expert is
+// an affine layer out = in W^T (+ b) with W stored [out, in] (hnwysp.cn/news/30485 3.2), two layers per expert
 // W1 | b1 | W2 | b2 (m.nxbn.cn/news/48047 3.1), the activation applied in the epilogue
 // (m.nxbn.cn 2.1: matmul and activation fused per expert).
 #include "moe_internal.cuh"
@@ -11,7 +14,10 @@
 namespace colibri {
 namespace {
 
-constexpr int SBM = 128, SBN = 64, SBK = 16;
+constexpr int SBM = 32, SBN = 64, SBK = 32;
+constexpr int kSlices = kRowTile / SBM;  // row slices per 128-row tile
+constexpr int TM = SBM / 16;             // rows per thread
+constexpr int kLoadsA = SBM * SBK / 256, kLoadsB = SBN * SBK / 256;  // per thread per K slab
 
 template <int EPI>
 __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
@@ -21,7 +27,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
   __shared__ float B3s[kSwiGLU ? SBK : 1][SBN + 4];
   const Sched* sc = a.sched;
   const int n_tiles = (a.N + SBN - 1) / SBN;
-  const int tile = blockIdx.x;
+  const int tile = blockIdx.x / kSlices, slice = blockIdx.x % kSlices;
   pdl_trigger();
   pdl_wait();
   if (tile >= sc->mtile_start[a.E] * n_tiles) return;
@@ -30,47 +36,64 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
   const int local = tile - sc->mtile_start[e] * n_tiles;
   const int mt_e = sc->mtile_start[e + 1] - sc->mtile_start[e];
   const int n = local / mt_e, m = local - n * mt_e;
-  const int row0 = sc->offsets[e] + m * SBM;
+  const int row0 = sc->offsets[e] + m * kRowTile + slice * SBM;
   const int seg_end = sc->offsets[e] + sc->counts[e];
+  if (row0 >= seg_end) return;  // padding rows only
   const int n0 = n * SBN;
   const float* __restrict__ A = a.a;
   const float* __restrict__ B = a.b + (size_t)e * a.N * a.K;
   const float* __restrict__ B3 = kSwiGLU ? a.b3 + (size_t)e * a.N * a.K : nullptr;
 
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  float acc[8][4], acc3[8][4];
+  float acc[TM][4], acc3[TM][4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < TM; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = acc3[i][j] = 0.f;
 
-  for (int k0 = 0; k0 < a.K; k0 += SBK) {
-    __syncthreads();
+  float ra[kLoadsA], rb[kLoadsB], rb3[kSwiGLU ? kLoadsB : 1];
+  auto load_slab = [&](int k0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int id = tid + i * 256, r = id >> 4, k = id & 15;
-      As[k][r] = (k0 + k < a.K) ? A[(size_t)(row0 + r) * a.K + k0 + k] : 0.f;
+    for (int i = 0; i < kLoadsA; ++i) {
+      const int id = tid + i * 256, r = id / SBK, k = id % SBK;
+      ra[i] = (k0 + k < a.K) ? A[(size_t)(row0 + r) * a.K + k0 + k] : 0.f;
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int id = tid + i * 256, c = id >> 4, k = id & 15;
+    for (int i = 0; i < kLoadsB; ++i) {
+      const int id = tid + i * 256, c = id / SBK, k = id % SBK;
       const bool in = (n0 + c < a.N) && (k0 + k < a.K);
-      Bs[k][c] = in ? B[(size_t)(n0 + c) * a.K + k0 + k] : 0.f;
-      if constexpr (kSwiGLU) B3s[k][c] = in ? B3[(size_t)(n0 + c) * a.K + k0 + k] : 0.f;
+      rb[i] = in ? B[(size_t)(n0 + c) * a.K + k0 + k] : 0.f;
+      if constexpr (kSwiGLU) rb3[i] = in ? B3[(size_t)(n0 + c) * a.K + k0 + k] : 0.f;
+    }
+  };
+  load_slab(0);
+  for (int k0 = 0; k0 < a.K; k0 += SBK) {
+    __syncthreads();  // every thread is done with the previous slab
+#pragma unroll
+    for (int i = 0; i < kLoadsA; ++i) {
+      const int id = tid + i * 256;
+      As[id % SBK][id / SBK] = ra[i];
+    }
+#pragma unroll
+    for (int i = 0; i < kLoadsB; ++i) {
+      const int id = tid + i * 256;
+      Bs[id % SBK][id / SBK] = rb[i];
+      if constexpr (kSwiGLU) B3s[id % SBK][id / SBK] = rb3[i];
     }
     __syncthreads();
+    if (k0 + SBK < a.K) load_slab(k0 + SBK);  // in flight while this slab is multiplied
 #pragma unroll
     for (int kk = 0; kk < SBK; ++kk) {
-      float af[8], bf[4], bf3[4];
+      float af[TM], bf[4], bf3[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) af[i] = As[kk][ty * 8 + i];
+      for (int i = 0; i < TM; ++i) af[i] = As[kk][ty * TM + i];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         bf[j] = Bs[kk][tx * 4 + j];
         if constexpr (kSwiGLU) bf3[j] = B3s[kk][tx * 4 + j];
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < TM; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           acc[i][j] = fmaf(af[i], bf[j], acc[i][j]);
@@ -80,8 +103,8 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
   }
 
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = row0 + ty * 8 + i;
+  for (int i = 0; i < TM; ++i) {
+    const int r = row0 + ty * TM + i;
     if (r >= seg_end) continue;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -104,7 +127,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
 
 cudaError_t launch_simt_gemm(int epi, const SimtGemmArgs& a, int max_mtiles, cudaStream_t s) {
   const int n_tiles = (a.N + SBN - 1) / SBN;
-  const int grid = max_mtiles * n_tiles;
+  const int grid = max_mtiles * n_tiles * kSlices;
   if (grid <= 0) return cudaSuccess;
   switch (epi) {
     case kEpiSwiGLU: return pdl_launch(simt_gemm_kernel<kEpiSwiGLU>, dim3(grid), dim3(256), 0, s, a);
