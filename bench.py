@@ -29,6 +29,8 @@ METRIC = "MoE-layer tokens/s at Mixtral-8x7B shape; % of bf16 tensor peak / HBM 
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 STAGES = ["router", "gather", "gemm_up", "gemm_down", "combine"]
+# (the cooperative decode kernel runs inside the "gemm_up" stage: up GEMM, activation, down GEMM and
+# combine in one launch, the other stages empty)
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture of the kernel as it now
 # stands (profiles/gemm_pair_mixtral_prefill.md); None where no capture of the current kernel exists.
 DOM_EVERY = 8  # the dominant kernel is timed with events on every 8th step of the timed region
@@ -381,6 +383,8 @@ def main():
         n_w = active + int(shape.shared_expert)
         byts = {2: n_w * n_up * shape.d_model * shape.d_ff * es,
                 3: n_w * shape.d_model * shape.d_ff * es}.get(dominant, alg["bytes"])
+        if layer.last_kernel_count() == 2:  # cooperative decode kernel: streams both projections' weights
+            byts = n_w * (n_up + 1) * shape.d_model * shape.d_ff * es
         ach = byts / dur / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         roof = {"bound": "hbm", "kernel": STAGES[dominant], "achieved": ach, "peak": peak, "unit": "GB/s",

@@ -85,6 +85,8 @@ struct colibri_moe {
   bool fuse_combine = true;  // two-slot fp32 layers: gate-weighted combine inside the down GEMM
   bool gather_a = false;     // bf16 prefill: up GEMM reads A rows from x through token_of_row
   int pair_ctas = 0;         // co-resident CTAs of the pair kernel (persistent grid size)
+  bool decode_fused = true;  // decode batches: one cooperative kernel after the router
+  int fused_ctas = 0;        // its grid (one CTA per SM)
   int32_t last_T = -1;
   int32_t last_kernels = 0;  // kernels enqueued by the last forward
   std::vector<cudaEvent_t> events;
@@ -192,6 +194,13 @@ bool env_gather_a() {
 bool env_pair_gemm() {
   const char* s = std::getenv("COLIBRI_MOE_GEMM");
   return !(s && std::strcmp(s, "1sm") == 0);
+}
+
+// Decode-sized batches run the cooperative fused kernel unless COLIBRI_MOE_DECODE_FUSED=0 selects
+// the separate kernels (dispatch, GEMM, activation, GEMM, combine).
+bool env_decode_fused() {
+  const char* s = std::getenv("COLIBRI_MOE_DECODE_FUSED");
+  return !(s && s[0] == '0');
 }
 
 int env_decode_max_t() {
@@ -366,7 +375,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   }
   if (prepare_router(cfg->dtype, cfg->num_experts) != cudaSuccess ||
       (cfg->dtype == COLIBRI_DTYPE_BF16 && (prepare_tc_gemm() != cudaSuccess || prepare_decode_gemm() != cudaSuccess ||
-                                             prepare_pair_gemm() != cudaSuccess))) {
+                                             prepare_pair_gemm() != cudaSuccess || prepare_decode_fused() != cudaSuccess))) {
     cudaGetLastError();
     colibri_moe_destroy(c);
     return COLIBRI_ERR_CUDA;
@@ -374,6 +383,12 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   if (c->pair_gemm) {
     c->pair_ctas = pair_gemm_max_ctas();
     if (c->pair_ctas < 2) c->pair_gemm = false;
+  }
+  c->decode_fused = env_decode_fused() && c->decode_max_t > 0;
+  if (c->decode_fused) {
+    const int co = decode_fused_max_ctas(sms);
+    c->fused_ctas = co < sms ? co : sms;
+    if (c->fused_ctas < 1) c->decode_fused = false;
   }
   if (cfg->dtype == COLIBRI_DTYPE_BF16) {
     bool ok = make_tmap(&c->tm_xp, c->xp, d, c->rows_alloc, kRowTile) &&
@@ -515,6 +530,11 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   // bf16 prefill: the up GEMM gathers its A rows from x through token_of_row instead of reading a
   // materialised Xp; the dispatch kernel then only writes the row bookkeeping.
   const bool gather_a = bf16 && !decode && ctx->gather_a;
+  // decode batches: one cooperative kernel after the router, with x as the token operand of its up
+  // GEMM (a tensor map of the caller's buffer, encoded per call)
+  CUtensorMap tm_xt;
+  const bool fused_decode = decode && ctx->decode_fused &&
+                            make_tmap(&tm_xt, x, d, static_cast<uint64_t>(T), static_cast<uint32_t>((T + 15) / 16 * 16));
   mark(0);
   // With the combine fused, out is cleared before the down GEMM adds into it: by extra warps of the
   // (tensor-bound) up GEMM, or by the router on the gathered-A path whose extra warps gather.
@@ -528,6 +548,25 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   GatherArgs ga{x, ctx->idx, ctx->row_of, ctx->hist, T, d, E, ctx->S, ctx->rows_alloc,
                 gather_a ? nullptr : ctx->xp, ctx->tok_of_row, ctx->sched, ctx->gate,
                 fuse ? ctx->gate_of_row : nullptr};
+  if (fused_decode) {
+    // decode-sized batch, one cooperative kernel: up GEMM, activation, down GEMM, combine (it also
+    // writes the dispatch bookkeeping, so no gather kernel runs)
+    const int n_pad = (T + 15) / 16 * 16;
+    mark(2);
+    FusedDecodeArgs fa{ctx->sched, E, d, f, ctx->n_up, T, n_pad, ctx->S, ctx->idx, ctx->gate, ctx->row_of,
+                       ctx->tok_of_row, ctx->hist, ctx->rows_alloc, ctx->partial, ctx->b1, ctx->b2, ctx->h, out,
+                       c.out_dtype == COLIBRI_DTYPE_BF16 ? 1 : 0, swiglu ? 1 : 0, ctx->timeout_ns,
+                       &ctx->sched->status};
+    if (launch_decode_fused(ctx->tm_w13_dec, tm_xt, ctx->tm_w2_dec, ctx->tm_h_dec[n_pad / 16 - 1], fa,
+                            ctx->fused_ctas, s) != cudaSuccess)
+      return COLIBRI_ERR_CUDA;
+    mark(3);
+    mark(4);
+    mark(5);
+    ctx->last_T = T;
+    ctx->last_kernels = 2;
+    return COLIBRI_OK;
+  }
   if (launch_gather(c.dtype, ga, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   mark(2);
   if (decode) {

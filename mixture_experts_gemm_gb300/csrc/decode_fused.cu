@@ -1,0 +1,509 @@
+// Decode-sized batches (T <= 64) in one cooperative kernel: up projection, activation, down
+// projection and combine, separated by grid-wide barriers instead of kernel boundaries.
+//
+// What is computed is the separate-kernel decode path's (gemm_decode.cu: the Compute stage of
+// zskr.cn/news/2272131 "Colibri: a lightweight C MoE inference engine for edge devices" 2.1 as a
+// stream over the weights of the experts that received tokens, 2.2), reorganised for latency:
+//
+//   phase U  P[s][t][e rows] = sum over K split s of W13_e[rows, k] x[t, k]   (tcgen05, TMEM)
+//   phase A  H[e * n_pad + t, :] = act(sum_s P[s][t][e rows])  for every routed (token, expert)
+//   phase D  P[s][t][e rows] = sum over split s of W2_e[rows, k] H[e * n_pad + t, k]
+//   phase C  out[t, :] = sum over t's slots in order of g * (sum_s P[s][t][e rows] (+ b2))
+//
+// The token operand of phase U is x itself (all n_pad >= T token rows of the batch, rows past T
+// read as zeros by TMA), so no dispatch copy is needed: a column t of expert e's accumulator is
+// kept only when t was routed to e (a 64-bit token mask per expert).  One persistent CTA per SM,
+// the warp roles of the decode GEMM (TMA producer, MMA issuer, 4 epilogue warps); every thread
+// joins the element-wise phases.  The weight tiles of phase D are requested before the barriers
+// that precede it (they do not depend on phase A), so the HBM stream continues across them.
+//
+// Barriers: one arrival per CTA on a counter in the routing summary (cleared by the router), the
+// arriving thread fences (gpu scope) first and spins with acquire loads, bounded by the wait
+// timeout; H is written through the generic proxy and read by TMA, so its writers fence the proxy
+// before arriving.  Splits are summed in order: results are deterministic.
+#include "tcgen05_ptx.cuh"
+
+namespace colibri {
+namespace {
+
+using namespace ptx;
+
+constexpr int FBM = 128, FBK = 64, FUMMA_K = 16;
+constexpr int FSTAGES = 8;
+constexpr int FA_BYTES = FBM * FBK * 2;          // 16 KB weight tile
+constexpr int FB_SLOT = kDecodeMaxT * FBK * 2;   // 8 KB token tile slot (n_pad rows used)
+constexpr int FNUM_THREADS = 192;
+constexpr uint32_t FTMEM_COLS = 128;             // two accumulators of up to 64 fp32 columns
+constexpr int FNUM_BARS = 2 * FSTAGES + 5;
+constexpr int FSMEM_BYTES =
+    1024 + FSTAGES * (FA_BYTES + FB_SLOT) + FNUM_BARS * 8 + 16 + 8 * kMaxE + 4 * (2 * kMaxE + 2);
+static_assert(FSMEM_BYTES <= 227 * 1024, "fused decode shared memory");
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Grid-wide barrier number `n` (1, 2, ...): every CTA arrives once; bounded wait.
+__device__ __forceinline__ void grid_barrier(Sched* sc, uint32_t n, volatile int* s_abort, uint64_t timeout_ns,
+                                             int32_t* status) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(&sc->grid_sync, 1u);
+    const uint32_t target = n * gridDim.x;
+    if (ld_acquire_gpu(&sc->grid_sync) < target) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_gpu(&sc->grid_sync) < target) {
+        if (globaltimer_ns() - t0 > timeout_ns) {
+          atomicOr(status, kStatusTimeoutGridSync);
+          *s_abort = 1;
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+// One weight-streaming GEMM phase: items (active expert, 128-row weight tile, K split).
+struct Phase {
+  const CUtensorMap* tmW;
+  const CUtensorMap* tmX;
+  int K;        // reduction length
+  int rows;     // weight rows per expert
+  int x_step;   // first token row of expert e's operand = e * x_step
+  int MT, KB, S, total;
+  float* partial;  // [S][n_pad][E * rows]
+};
+
+__device__ __forceinline__ Phase make_phase(const CUtensorMap* tmW, const CUtensorMap* tmX, int K, int rows, int x_step,
+                                            int n_act, int s_max, float* partial) {
+  Phase p;
+  p.tmW = tmW;
+  p.tmX = tmX;
+  p.K = K;
+  p.rows = rows;
+  p.x_step = x_step;
+  p.MT = rows / FBM;
+  p.KB = (K + FBK - 1) / FBK;
+  p.S = decode_splits(n_act * p.MT, p.KB, gridDim.x, s_max);
+  p.total = n_act * p.MT * p.S;
+  p.partial = partial;
+  return p;
+}
+
+struct Item {
+  int e, mt, sp, kb0, kb1;
+};
+__device__ __forceinline__ Item item_of(const Phase& p, int it, const int* s_act) {
+  Item r;
+  const int ai = it / (p.MT * p.S), rem = it - ai * (p.MT * p.S);
+  r.e = s_act[ai];
+  r.mt = rem / p.S;
+  r.sp = rem - r.mt * p.S;
+  r.kb0 = (p.KB * r.sp) / p.S;
+  r.kb1 = (p.KB * (r.sp + 1)) / p.S;
+  return r;
+}
+
+struct Ring {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++stage == FSTAGES) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+__global__ void __launch_bounds__(FNUM_THREADS, 1)
+    decode_fused_kernel(const __grid_constant__ CUtensorMap tmW13, const __grid_constant__ CUtensorMap tmX,
+                        const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmH,
+                        const FusedDecodeArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + FSTAGES * FA_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + FSTAGES * FB_SLOT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + FNUM_BARS);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  unsigned long long* s_mask = reinterpret_cast<unsigned long long*>(tmem_slot + 4);  // tokens routed to e
+  int* s_act = reinterpret_cast<int*>(s_mask + kMaxE);
+  int* s_nact = s_act + kMaxE;
+
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + FSTAGES);
+  const uint32_t tfull0 = smem_u32(bars + 2 * FSTAGES);
+  const uint32_t tempty0 = smem_u32(bars + 2 * FSTAGES + 2);
+  const uint32_t drain = smem_u32(bars + 2 * FSTAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = a.E, T = a.T, Sl = a.S, n_pad = a.n_pad;
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < FSTAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull0 + 8 * i, 1);
+      mbar_init(tempty0 + 8 * i, 4);
+    }
+    mbar_init(drain, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmW13);
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmW2);
+    prefetch_tmap(&tmH);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), FTMEM_COLS);
+    tmem_relinquish();
+  }
+  if (threadIdx.x < kMaxE) s_mask[threadIdx.x] = 0ull;
+  pdl_trigger();
+  pdl_wait();  // routing (idx, gates, counts) comes from the router
+  __syncthreads();
+  for (int i = threadIdx.x; i < T * Sl; i += blockDim.x) {
+    const int e = a.idx[i];
+    if (e >= 0 && e < E) atomicOr(&s_mask[e], 1ull << (i / Sl));
+  }
+  if (threadIdx.x == 0) *s_nact = active_experts(a.sched, E, s_act);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int n_act = *s_nact;
+  const int gtid = blockIdx.x * blockDim.x + threadIdx.x, gstride = gridDim.x * blockDim.x;
+
+  // row bookkeeping of the dispatch layout (what get_routing reports; nothing below reads it)
+  for (int i = gtid; i < T * Sl; i += gstride) {
+    const int t = i / Sl;
+    const int r = a.chunk_base[static_cast<size_t>(t / kRouterChunk) * E + a.idx[i]] + a.row_of[i];
+    if (r >= 0 && r < a.rows_alloc) {
+      a.row_of[i] = r;
+      a.token_of_row[r] = t;
+    } else {
+      atomicOr(a.status, kStatusBadRow);
+    }
+  }
+  const uint32_t b_bytes = static_cast<uint32_t>(n_pad) * FBK * 2;
+  const uint32_t idesc = make_idesc_bf16(FBM, n_pad);
+
+  const Phase PU = make_phase(&tmW13, &tmX, a.d, a.n_up, 0, n_act, kDecodeSplitsUp, a.partial);
+  const Phase PD = make_phase(&tmW2, &tmH, a.f, a.d, n_pad, n_act, kDecodeSplitsDown, a.partial);
+
+  // per-role state, carried from phase U to phase D
+  Ring ring;                         // producer and MMA issuer: shared-memory ring position
+  int acc = 0;                       // MMA issuer and epilogue: TMEM accumulator in use
+  uint32_t acc_phase = 0;
+  uint32_t armed = 0, armed_phase = 0;  // producer: stages with copies issued (last phase of each)
+  int pre = 0;                       // producer: stages of phase D whose weight tile is in flight
+  Ring pre_start;
+
+  // Producer: weight tile + token tile per stage.  Stages [0, pre) of this phase had their weight
+  // tile requested earlier (from pre_start on); only their token tile is issued here.
+  auto produce = [&](const Phase& P, int n_pre, Ring start) {
+    Ring cur = n_pre > 0 ? start : ring;
+    int g = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < P.total; it += gridDim.x) {
+      const Item im = item_of(P, it, s_act);
+      const int w_row = im.e * P.rows + im.mt * FBM;
+      const int x_row = im.e * P.x_step;
+      for (int kb = im.kb0; kb < im.kb1; ++kb, ++g) {
+        const uint32_t fb = full0 + 8 * cur.stage;
+        if (g >= n_pre) {
+          if (!mbar_wait(empty0 + 8 * cur.stage, cur.phase ^ 1u, s_abort, a.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(fb, FA_BYTES + b_bytes);
+          tma_load_2d(smem_u32(sA + cur.stage * FA_BYTES), P.tmW, fb, kb * FBK, w_row);
+        }
+        armed |= 1u << cur.stage;
+        armed_phase = (armed_phase & ~(1u << cur.stage)) | (cur.phase << cur.stage);
+        tma_load_2d(smem_u32(sB + cur.stage * FB_SLOT), P.tmX, fb, kb * FBK, x_row);
+        cur.next();
+      }
+    }
+    if (!ok) {
+      if (!*s_abort) atomicOr(a.status, kStatusTimeoutProducer);
+      *s_abort = 1;
+    }
+    ring = cur;
+  };
+  // Producer: request the weight tiles of phase P's first stages (its token operand is not ready).
+  auto prefetch_weights = [&](const Phase& P) {
+    pre_start = ring;
+    pre = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; ok && pre < FSTAGES && it < P.total; it += gridDim.x) {
+      const Item im = item_of(P, it, s_act);
+      const int w_row = im.e * P.rows + im.mt * FBM;
+      for (int kb = im.kb0; kb < im.kb1 && pre < FSTAGES; ++kb, ++pre) {
+        if (!mbar_wait(empty0 + 8 * ring.stage, ring.phase ^ 1u, s_abort, a.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = full0 + 8 * ring.stage;
+        mbar_arrive_expect_tx(fb, FA_BYTES + b_bytes);
+        tma_load_2d(smem_u32(sA + ring.stage * FA_BYTES), P.tmW, fb, kb * FBK, w_row);
+        ring.next();
+      }
+    }
+    if (!ok) {
+      if (!*s_abort) atomicOr(a.status, kStatusTimeoutProducer);
+      *s_abort = 1;
+    }
+  };
+  auto mma = [&](const Phase& P) {
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < P.total; it += gridDim.x) {
+      const Item im = item_of(P, it, s_act);
+      if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, s_abort, a.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kDecodeMaxT);
+      for (int kb = im.kb0; kb < im.kb1; ++kb) {
+        if (!mbar_wait(full0 + 8 * ring.stage, ring.phase, s_abort, a.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(sA + ring.stage * FA_BYTES);
+        const uint32_t b_addr = smem_u32(sB + ring.stage * FB_SLOT);
+#pragma unroll
+        for (int k = 0; k < FBK / FUMMA_K; ++k)
+          umma_bf16(d_tmem, sw128_desc(a_addr + k * FUMMA_K * 2), sw128_desc(b_addr + k * FUMMA_K * 2), idesc,
+                    (kb > im.kb0 || k > 0) ? 1u : 0u);
+        umma_commit(empty0 + 8 * ring.stage);
+        ring.next();
+      }
+      if (!ok) break;
+      umma_commit(tfull0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (!ok) {
+      if (!*s_abort) atomicOr(a.status, kStatusTimeoutMma);
+      *s_abort = 1;
+    }
+  };
+  // Epilogue: thread = weight row of the item's tile; token column t kept when t was routed to e.
+  auto epilogue = [&](const Phase& P) {
+    const int q = warp & 3;
+    const size_t rows_total = static_cast<size_t>(E) * P.rows;
+    for (int it = blockIdx.x; it < P.total; it += gridDim.x) {
+      const Item im = item_of(P, it, s_act);
+      const unsigned long long mask = s_mask[im.e];
+      bool ok = mbar_wait(tfull0 + 8 * acc, acc_phase, s_abort, a.timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0 && !*s_abort) atomicOr(a.status, kStatusTimeoutEpilogue);
+        if (lane == 0) *s_abort = 1;
+        break;
+      }
+      tc_fence_after();
+      const size_t row = static_cast<size_t>(im.e) * P.rows + im.mt * FBM + q * 32 + lane;
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kDecodeMaxT);
+      float* out = P.partial + static_cast<size_t>(im.sp) * n_pad * rows_total + row;
+      for (int c = 0; c < n_pad; c += 16) {
+        uint32_t v[16];
+        tmem_ld16_sync(tbase + c, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if ((mask >> (c + j)) & 1ull) out[static_cast<size_t>(c + j) * rows_total] = __uint_as_float(v[j]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  };
+
+  // ---------------------------------------------------------------- phase U
+  if (warp == 0) {
+    if (lane == 0) {
+      produce(PU, 0, ring);
+      prefetch_weights(PD);  // phase D's first weight tiles, independent of phases U and A
+    }
+  } else if (warp == 1) {
+    if (lane == 0) mma(PU);
+  } else {
+    epilogue(PU);
+  }
+  grid_barrier(a.sched, 1, s_abort, a.timeout_ns, a.status);
+
+  // ---------------------------------------------------------------- phase A: H rows of routed pairs
+  if (!*s_abort) {
+    const int f = a.f, f4 = f / 4;
+    const size_t rows_total = static_cast<size_t>(E) * a.n_up;
+    for (int w = gtid; w < T * Sl * f4; w += gstride) {
+      const int pair = w / f4, c = (w - pair * f4) * 4;
+      const int t = pair / Sl;
+      const int e = a.idx[pair];
+      float hv[4];
+      if (a.swiglu) {
+        const size_t grow = static_cast<size_t>(e) * a.n_up + 256 * (c / 128) + (c % 128);
+        float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+        for (int s = 0; s < PU.S; ++s) {
+          const float* P = a.partial + (static_cast<size_t>(s) * n_pad + t) * rows_total;
+          const float4 pg = *reinterpret_cast<const float4*>(P + grow);
+          const float4 pu = *reinterpret_cast<const float4*>(P + grow + 128);
+          g.x += pg.x; g.y += pg.y; g.z += pg.z; g.w += pg.w;
+          u.x += pu.x; u.y += pu.y; u.z += pu.z; u.w += pu.w;
+        }
+        hv[0] = silu_fast(g.x) * u.x;
+        hv[1] = silu_fast(g.y) * u.y;
+        hv[2] = silu_fast(g.z) * u.z;
+        hv[3] = silu_fast(g.w) * u.w;
+      } else {
+        const size_t grow = static_cast<size_t>(e) * a.n_up + c;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < PU.S; ++s) {
+          const float4 p = *reinterpret_cast<const float4*>(a.partial + (static_cast<size_t>(s) * n_pad + t) *
+                                                                            rows_total + grow);
+          v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
+        }
+        const float* b = a.b1 + static_cast<size_t>(e) * f + c;
+        hv[0] = fmaxf(v.x + b[0], 0.f);
+        hv[1] = fmaxf(v.y + b[1], 0.f);
+        hv[2] = fmaxf(v.z + b[2], 0.f);
+        hv[3] = fmaxf(v.w + b[3], 0.f);
+      }
+      uint2 o;
+      o.x = pack_bf16(hv[0], hv[1]);
+      o.y = pack_bf16(hv[2], hv[3]);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.h) + (static_cast<size_t>(e) * n_pad + t) * f + c) = o;
+    }
+    fence_proxy_async_global();  // H is read next by TMA (async proxy)
+  }
+  grid_barrier(a.sched, 2, s_abort, a.timeout_ns, a.status);
+
+  // ---------------------------------------------------------------- phase D
+  if (warp == 0) {
+    if (lane == 0) produce(PD, pre, pre_start);
+  } else if (warp == 1) {
+    if (lane == 0) mma(PD);
+  } else {
+    epilogue(PD);
+  }
+  grid_barrier(a.sched, 3, s_abort, a.timeout_ns, a.status);
+
+  // ---------------------------------------------------------------- phase C: combine in slot order
+  if (!*s_abort) {
+    const int d = a.d, d4 = d / 4;
+    const size_t rows_total = static_cast<size_t>(E) * d;
+    for (int w = gtid; w < T * d4; w += gstride) {
+      const int t = w / d4, c = (w - t * d4) * 4;
+      float o[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int k = 0; k < Sl; ++k) {
+        const int e = a.idx[t * Sl + k];
+        const size_t grow = static_cast<size_t>(e) * d + c;
+        float4 p[kDecodeSplitsDown];
+#pragma unroll
+        for (int s = 0; s < kDecodeSplitsDown; ++s)
+          p[s] = s < PD.S ? *reinterpret_cast<const float4*>(a.partial + (static_cast<size_t>(s) * n_pad + t) *
+                                                                             rows_total + grow)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 v = p[0];
+#pragma unroll
+        for (int s = 1; s < kDecodeSplitsDown; ++s)
+          if (s < PD.S) {
+            v.x += p[s].x; v.y += p[s].y; v.z += p[s].z; v.w += p[s].w;
+          }
+        if (a.b2) {
+          const float* b = a.b2 + grow;
+          v.x += b[0]; v.y += b[1]; v.z += b[2]; v.w += b[3];
+        }
+        const float gk = a.gate[t * Sl + k];
+        const float y[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = k == 0 ? __fmul_rn(gk, y[i]) : __fadd_rn(o[i], __fmul_rn(gk, y[i]));
+      }
+      if (a.out_bf16) {
+        uint2 pk;
+        pk.x = pack_bf16(o[0], o[1]);
+        pk.y = pack_bf16(o[2], o[3]);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(t) * d + c) = pk;
+      } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + static_cast<size_t>(t) * d + c) =
+            make_float4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  if (warp == 0 && lane == 0) {
+    // copies issued but never consumed (only after a timeout) land before the CTA leaves
+    for (int s = 0; s < FSTAGES; ++s)
+      if (armed & (1u << s)) {
+        volatile int never = 0;
+        mbar_wait(full0 + 8 * s, (armed_phase >> s) & 1u, &never, a.timeout_ns);
+      }
+  }
+  if (warp == 1 && lane == 0) {
+    umma_commit(drain);
+    volatile int never = 0;
+    mbar_wait(drain, 0, &never, a.timeout_ns);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, FTMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t prepare_decode_fused() {
+  return cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FSMEM_BYTES);
+}
+
+// CTAs of the cooperative decode kernel that can be resident at once (0 on error).
+int decode_fused_max_ctas(int num_sms) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_kernel, FNUM_THREADS, FSMEM_BYTES) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return per_sm * num_sms;
+}
+
+cudaError_t launch_decode_fused(const CUtensorMap& tmW13, const CUtensorMap& tmX, const CUtensorMap& tmW2,
+                                const CUtensorMap& tmH, const FusedDecodeArgs& a, int grid, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(FNUM_THREADS);
+  cfg.dynamicSmemBytes = FSMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_fused_kernel, tmW13, tmX, tmW2, tmH, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace colibri

@@ -32,30 +32,6 @@ constexpr int DNUM_BARS = 2 * DSTAGES + 5;
 constexpr int DSMEM_BYTES = 1024 + DSTAGES * (DA_BYTES + DB_SLOT) + DNUM_BARS * 8 + 16 + 4 * (3 * kMaxE + 2);
 static_assert(DSMEM_BYTES <= 227 * 1024, "decode GEMM shared memory");
 
-// Number of K splits: the smallest S whose items fill >= 90 % of their waves, else the best fill.
-__device__ __forceinline__ int decode_splits(int items0, int kblocks, int grid, int s_max) {
-  int best = 1;
-  int best_num = -1, best_den = 1;
-  for (int S = 1; S <= s_max && S <= kblocks; ++S) {
-    const int items = items0 * S;
-    const int waves = (items + grid - 1) / grid;
-    if (items >= grid && items * 10 >= waves * grid * 9) return S;
-    if (static_cast<long long>(items) * best_den > static_cast<long long>(best_num) * (waves * grid)) {
-      best_num = items;
-      best_den = waves * grid;
-      best = S;
-    }
-  }
-  return best;
-}
-
-__device__ __forceinline__ int active_experts(const Sched* sc, int E, int* list) {
-  int n = 0;
-  for (int e = 0; e < E; ++e)
-    if (sc->counts[e] > 0) list[n++] = e;
-  return n;
-}
-
 __global__ void __launch_bounds__(DNUM_THREADS, 1)
     tc_decode_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                           const DecodeArgs a) {

@@ -28,6 +28,7 @@ enum : int32_t {
   kStatusTimeoutMma = 1 << 1,
   kStatusTimeoutEpilogue = 1 << 2,
   kStatusBadRow = 1 << 3,
+  kStatusTimeoutGridSync = 1 << 4,
 };
 
 // Routing summary in device memory.  Written by the last CTA of the router kernel, read by
@@ -37,6 +38,7 @@ struct Sched {
   int32_t offsets[kMaxE + 1];      // first row of each expert segment (segments padded to 128 rows)
   int32_t mtile_start[kMaxE + 1];  // prefix sum of ceil(counts / 128): M tiles before each expert
   uint32_t ticket;                 // router CTAs finished (reset to 0 by the last one)
+  uint32_t grid_sync;              // arrivals at the cooperative decode kernel's grid barriers (reset by the router)
   int32_t status;                  // device status word (kStatus* bits)
 };
 
@@ -157,6 +159,28 @@ struct DecodeCombineArgs {
   int S;
 };
 
+// Cooperative decode kernel (T <= 64): up projection, activation, down projection, combine.
+struct FusedDecodeArgs {
+  Sched* sched;
+  int E;                    // scheduled experts (routed + shared)
+  int d, f, n_up;           // model width, hidden width, up-projection weight rows per expert
+  int T, n_pad, S;          // tokens, token columns (16..64, >= T), slots per token
+  const int32_t* idx;       // [T, S] from the router
+  const float* gate;        // [T, S]
+  int32_t* row_of;          // [T, S] in: rank in chunk, out: row of the dispatch layout
+  int32_t* token_of_row;    // [rows_alloc]
+  const int32_t* chunk_base;  // [nchunks, E] first row of each (chunk, expert)
+  int64_t rows_alloc;
+  float* partial;           // [splits][n_pad][E * rows] fp32
+  const float* b1;          // [E, f] (ReLU) or nullptr
+  const float* b2;          // [E, d] or nullptr
+  void* h;                  // H rows e * n_pad + t, bf16 [.., f]
+  void* out;                // [T, d]
+  int out_bf16, swiglu;
+  uint64_t timeout_ns;
+  int32_t* status;
+};
+
 // fp32 SIMT grouped GEMM operands (row-major, K contiguous)
 struct SimtGemmArgs {
   const Sched* sched;
@@ -194,6 +218,31 @@ cudaError_t pdl_launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// Decode-path helpers shared by the separate-kernel and the cooperative decode path.
+// Number of K splits: the smallest S whose items fill >= 90 % of their waves, else the best fill.
+__device__ __forceinline__ int decode_splits(int items0, int kblocks, int grid, int s_max) {
+  int best = 1;
+  int best_num = -1, best_den = 1;
+  for (int S = 1; S <= s_max && S <= kblocks; ++S) {
+    const int items = items0 * S;
+    const int waves = (items + grid - 1) / grid;
+    if (items >= grid && items * 10 >= waves * grid * 9) return S;
+    if (static_cast<long long>(items) * best_den > static_cast<long long>(best_num) * (waves * grid)) {
+      best_num = items;
+      best_den = waves * grid;
+      best = S;
+    }
+  }
+  return best;
+}
+
+__device__ __forceinline__ int active_experts(const Sched* sc, int E, int* list) {
+  int n = 0;
+  for (int e = 0; e < E; ++e)
+    if (sc->counts[e] > 0) list[n++] = e;
+  return n;
+}
+
 // launchers (return cudaGetLastError() of the launch)
 cudaError_t launch_router(int dtype, const RouterArgs& a, int nchunks, cudaStream_t s);
 cudaError_t launch_gather(int dtype, const GatherArgs& a, cudaStream_t s);
@@ -213,6 +262,10 @@ cudaError_t launch_pair_gemm(int epi, bool gather_a, const CUtensorMap& tmA, con
 cudaError_t launch_decode_gemm(const CUtensorMap& tmW, const CUtensorMap& tmX, const DecodeArgs& a, int grid,
                                cudaStream_t s);
 cudaError_t launch_decode_act(bool swiglu, const DecodeActArgs& a, cudaStream_t s);
+cudaError_t prepare_decode_fused();
+int decode_fused_max_ctas(int num_sms);
+cudaError_t launch_decode_fused(const CUtensorMap& tmW13, const CUtensorMap& tmX, const CUtensorMap& tmW2,
+                                const CUtensorMap& tmH, const FusedDecodeArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_decode_combine(int out_dtype, const DecodeCombineArgs& a, cudaStream_t s);
 int tc_gemm_block_n();
 int tc_gemm_threads();

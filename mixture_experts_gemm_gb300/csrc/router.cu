@@ -94,6 +94,7 @@ __device__ void scan_offsets(const RouterArgs& a, int nchunks) {
     a.sched->offsets[E] = off;
     a.sched->mtile_start[E] = mt;
     a.sched->ticket = 0;  // ready for the next forward
+    a.sched->grid_sync = 0;
   }
   __syncthreads();
 #pragma unroll

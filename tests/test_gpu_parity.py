@@ -138,6 +138,30 @@ def test_decode_path_matches_oracle_and_prefill_path(T, monkeypatch):
     assert rel_err(out_d, out_p) <= TOL_BF16
 
 
+@pytest.mark.parametrize("case", ["t1", "t7", "t33", "t64", "relu", "k4-shared"])
+def test_cooperative_decode_kernel_equals_separate_kernels(case, monkeypatch):
+    """Decode batches run one cooperative kernel (grid barriers between up GEMM, activation, down GEMM
+    and combine; x itself as the up GEMM's token operand).  It sums the same partials in the same order
+    as the separate kernels, so outputs and routing bookkeeping agree bit for bit."""
+    if case == "relu":
+        shape = testgen.LayerShape("coop-relu", 20, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")
+    elif case == "k4-shared":
+        shape = testgen.LayerShape("coop-k4s", 40, 512, 384, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True,
+                                   top_k=4, shared_expert=True)
+    else:
+        shape = testgen.LayerShape("coop", int(case[1:]), 512, 384, 8, testgen.ACT_SWIGLU, "bf16",
+                                   zipf_router_bias=True)
+    li = testgen.make_inputs(shape)
+    layer_f, out_f, r_f, _, _ = _full_check(li)
+    assert layer_f.last_kernel_count() == 2
+    monkeypatch.setenv("COLIBRI_MOE_DECODE_FUSED", "0")
+    layer_s, out_s, r_s, _, _ = _full_check(li)
+    assert layer_s.last_kernel_count() == 6
+    assert np.array_equal(out_f, out_s)
+    for k in ("idx", "gate", "counts", "offsets", "row_of"):
+        assert np.array_equal(r_f[k], r_s[k]), k
+
+
 def test_decode_path_relu_bias():
     shape = testgen.LayerShape("decode-relu", 20, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")
     li = testgen.make_inputs(shape)
@@ -471,13 +495,16 @@ def test_last_kernel_count_matches_the_path(monkeypatch):
     layer.forward(x)
     assert layer.last_kernel_count() == 4          # router, dispatch, up GEMM, down GEMM + combine
     layer.forward(x[:20].contiguous())
-    assert layer.last_kernel_count() == 6          # decode: router, dispatch, 2 x (GEMM, reduction)
+    assert layer.last_kernel_count() == 2          # decode: router + one cooperative kernel
     layer.forward(x[:0])
     assert layer.last_kernel_count() == 0
     monkeypatch.setenv("COLIBRI_MOE_FUSED_COMBINE", "0")
+    monkeypatch.setenv("COLIBRI_MOE_DECODE_FUSED", "0")
     layer2 = make_layer(li)
     layer2.forward(x)
     assert layer2.last_kernel_count() == 5
+    layer2.forward(x[:20].contiguous())
+    assert layer2.last_kernel_count() == 6        # router, dispatch, 2 x (GEMM, reduction), combine
     torch.cuda.synchronize()
 
 
