@@ -80,6 +80,7 @@ struct colibri_moe {
   // decode path (T <= decode_max_t): 128-row weight boxes, token boxes of 16/32/48/64 rows
   CUtensorMap tm_w13_dec{}, tm_w2_dec{}, tm_xp_dec[4]{}, tm_h_dec[4]{};
   float* partial = nullptr;  // decode partial sums [splits][n_pad][E * rows]
+  uint32_t* tile_done = nullptr;  // cooperative decode kernel: items done per down-projection tile
   int decode_max_t = 0;
   bool pair_gemm = false;    // prefill GEMMs on CTA pairs (256x256 tiles)
   bool fuse_combine = true;  // two-slot fp32 layers: gate-weighted combine inside the down GEMM
@@ -96,6 +97,9 @@ struct colibri_moe {
 namespace {
 
 constexpr int kNumStages = 5;  // router, gather, up GEMM, down GEMM, combine
+// Cooperative decode kernel: batches up to this size combine per tile (no third grid barrier);
+// measured on GB300 at the Mixtral shape: T=1 2 us faster, T=4 even, T >= 16 slower.
+constexpr int kTileCombineMaxT = 4;
 
 struct DeviceGuard {
   int prev = -1;
@@ -331,6 +335,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
                                                       kDecodeSplitsDown * npad_max * Ex * d)
                                   : 0;
   const size_t o_part = carve(part_floats * 4);
+  const size_t o_tiles = carve((d / 128 + 1) * sizeof(uint32_t));
   const size_t o_xs = carve(T * d * c->esize);
   const size_t o_os = carve(T * d * c->out_esize);
   const size_t o_xs2 = carve(T * d * c->esize);
@@ -353,6 +358,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   c->hist = reinterpret_cast<int32_t*>(b + o_hist);
   c->sched = reinterpret_cast<Sched*>(b + o_sched);
   c->partial = part_floats > 0 ? reinterpret_cast<float*>(b + o_part) : nullptr;
+  c->tile_done = reinterpret_cast<uint32_t*>(b + o_tiles);
   c->x_stage = b + o_xs;
   c->out_stage = b + o_os;
   c->x_stage2 = b + o_xs2;
@@ -542,7 +548,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   const int64_t out_vec4 = static_cast<int64_t>(T) * d / 4;
   RouterArgs ra{x, ctx->w_router, ctx->b_router, T, d, c.num_experts, ctx->dchunk, ctx->idx, ctx->gate,
                 ctx->row_of, ctx->hist, ctx->sched, ctx->k, c.gate_mode, c.has_shared_expert, ctx->S, ctx->Ex,
-                fuse && gather_a ? static_cast<float*>(out) : nullptr};
+                fuse && gather_a ? static_cast<float*>(out) : nullptr, ctx->tile_done, d / 128};
   if (launch_router(c.dtype, ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   mark(1);
   GatherArgs ga{x, ctx->idx, ctx->row_of, ctx->hist, T, d, E, ctx->S, ctx->rows_alloc,
@@ -556,7 +562,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     FusedDecodeArgs fa{ctx->sched, E, d, f, ctx->n_up, T, n_pad, ctx->S, ctx->idx, ctx->gate, ctx->row_of,
                        ctx->tok_of_row, ctx->hist, ctx->rows_alloc, ctx->partial, ctx->b1, ctx->b2, ctx->h, out,
                        c.out_dtype == COLIBRI_DTYPE_BF16 ? 1 : 0, swiglu ? 1 : 0, ctx->timeout_ns,
-                       &ctx->sched->status};
+                       &ctx->sched->status, ctx->tile_done, T <= kTileCombineMaxT ? 1 : 0};
     if (launch_decode_fused(ctx->tm_w13_dec, tm_xt, ctx->tm_w2_dec, ctx->tm_h_dec[n_pad / 16 - 1], fa,
                             ctx->fused_ctas, s) != cudaSuccess)
       return COLIBRI_ERR_CUDA;

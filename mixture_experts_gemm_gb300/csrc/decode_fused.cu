@@ -8,13 +8,17 @@
 //   phase U  P[s][t][e rows] = sum over K split s of W13_e[rows, k] x[t, k]   (tcgen05, TMEM)
 //   phase A  H[e * n_pad + t, :] = act(sum_s P[s][t][e rows])  for every routed (token, expert)
 //   phase D  P[s][t][e rows] = sum over split s of W2_e[rows, k] H[e * n_pad + t, k]
-//   phase C  out[t, :] = sum over t's slots in order of g * (sum_s P[s][t][e rows] (+ b2))
+//   phase C  out[t, :] = sum over t's slots in order of g * (sum_s P[s][t][e rows] (+ b2)): after a
+//            third barrier, or (tile_combine, the smallest batches) for the 128 columns of a down-
+//            projection weight tile by the CTA that finished the tile's last item (a per-tile
+//            counter, reset by that CTA), with no barrier.  The counter costs a gpu-scope fence per
+//            item, which only pays off while items are few and each combine is a handful of rows.
 //
 // The token operand of phase U is x itself (all n_pad >= T token rows of the batch, rows past T
 // read as zeros by TMA), so no dispatch copy is needed: a column t of expert e's accumulator is
 // kept only when t was routed to e (a 64-bit token mask per expert).  One persistent CTA per SM,
 // the warp roles of the decode GEMM (TMA producer, MMA issuer, 4 epilogue warps); every thread
-// joins the element-wise phases.  The weight tiles of phase D are requested before the barriers
+// joins the element-wise phase A.  The weight tiles of phase D are requested before the barriers
 // that precede it (they do not depend on phase A), so the HBM stream continues across them.
 //
 // Barriers: one arrival per CTA on a counter in the routing summary (cleared by the router), the
@@ -36,7 +40,7 @@ constexpr int FNUM_THREADS = 192;
 constexpr uint32_t FTMEM_COLS = 128;             // two accumulators of up to 64 fp32 columns
 constexpr int FNUM_BARS = 2 * FSTAGES + 5;
 constexpr int FSMEM_BYTES =
-    1024 + FSTAGES * (FA_BYTES + FB_SLOT) + FNUM_BARS * 8 + 16 + 8 * kMaxE + 4 * (2 * kMaxE + 2);
+    1024 + FSTAGES * (FA_BYTES + FB_SLOT) + FNUM_BARS * 8 + 16 + 8 * kMaxE + 4 * (2 * kMaxE + 4);
 static_assert(FSMEM_BYTES <= 227 * 1024, "fused decode shared memory");
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
@@ -46,6 +50,22 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
 }
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// The four epilogue warps (2..5) only.
+__device__ __forceinline__ void named_barrier_epilogue() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Same barrier, and the AND of `v` over the four epilogue warps (so they all stop or go on together).
+__device__ __forceinline__ bool epilogue_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
 }
 
 // Grid-wide barrier number `n` (1, 2, ...): every CTA arrives once; bounded wait.
@@ -137,6 +157,7 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
   unsigned long long* s_mask = reinterpret_cast<unsigned long long*>(tmem_slot + 4);  // tokens routed to e
   int* s_act = reinterpret_cast<int*>(s_mask + kMaxE);
   int* s_nact = s_act + kMaxE;
+  volatile int* s_last = s_nact + 1;  // this CTA completed the current weight tile (phase D)
 
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = smem_u32(bars + FSTAGES);
@@ -170,30 +191,26 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
   if (threadIdx.x < kMaxE) s_mask[threadIdx.x] = 0ull;
   pdl_trigger();
   pdl_wait();  // routing (idx, gates, counts) comes from the router
-  __syncthreads();
-  for (int i = threadIdx.x; i < T * Sl; i += blockDim.x) {
-    const int e = a.idx[i];
-    if (e >= 0 && e < E) atomicOr(&s_mask[e], 1ull << (i / Sl));
+  // every routing load of this thread in flight at once (T * S <= 320 slots, E <= 17 counts)
+  const int n_slots = T * Sl;
+  const int i0 = threadIdx.x, i1 = threadIdx.x + FNUM_THREADS;
+  const int e0 = i0 < n_slots ? a.idx[i0] : -1;
+  const int e1 = i1 < n_slots ? a.idx[i1] : -1;
+  const int cnt = threadIdx.x < E ? a.sched->counts[threadIdx.x] : 0;
+  __syncthreads();  // masks cleared
+  if (e0 >= 0 && e0 < E) atomicOr(&s_mask[e0], 1ull << (i0 / Sl));
+  if (e1 >= 0 && e1 < E) atomicOr(&s_mask[e1], 1ull << (i1 / Sl));
+  if (warp == 0) {  // active experts in index order, from the counts
+    const unsigned act = __ballot_sync(0xffffffffu, lane < E && cnt > 0);
+    if (lane < E && cnt > 0) s_act[__popc(act & ((1u << lane) - 1u))] = lane;
+    if (lane == 0) *s_nact = __popc(act);
   }
-  if (threadIdx.x == 0) *s_nact = active_experts(a.sched, E, s_act);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int n_act = *s_nact;
   const int gtid = blockIdx.x * blockDim.x + threadIdx.x, gstride = gridDim.x * blockDim.x;
-
-  // row bookkeeping of the dispatch layout (what get_routing reports; nothing below reads it)
-  for (int i = gtid; i < T * Sl; i += gstride) {
-    const int t = i / Sl;
-    const int r = a.chunk_base[static_cast<size_t>(t / kRouterChunk) * E + a.idx[i]] + a.row_of[i];
-    if (r >= 0 && r < a.rows_alloc) {
-      a.row_of[i] = r;
-      a.token_of_row[r] = t;
-    } else {
-      atomicOr(a.status, kStatusBadRow);
-    }
-  }
   const uint32_t b_bytes = static_cast<uint32_t>(n_pad) * FBK * 2;
   const uint32_t idesc = make_idesc_bf16(FBM, n_pad);
 
@@ -301,8 +318,55 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
       *s_abort = 1;
     }
   };
+  // Phase D's combine, for the 128 output columns of weight tile mt, by the CTA whose item completed
+  // that tile last (all experts' splits of those rows are then in the partial buffer).
+  auto combine_tile = [&](const Phase& P, int mt) {
+    const int d = a.d;
+    const size_t rows_total = static_cast<size_t>(E) * d;
+    const int et = threadIdx.x - 64;  // epilogue thread 0..127
+    for (int w = et; w < T * (FBM / 4); w += 128) {
+      const int t = w / (FBM / 4), c = mt * FBM + (w - t * (FBM / 4)) * 4;
+      float o[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int k = 0; k < Sl; ++k) {
+        const int e = a.idx[t * Sl + k];
+        const size_t grow = static_cast<size_t>(e) * d + c;
+        float4 p[kDecodeSplitsDown];
+#pragma unroll
+        for (int sp = 0; sp < kDecodeSplitsDown; ++sp)
+          p[sp] = sp < P.S ? __ldcg(reinterpret_cast<const float4*>(a.partial + (static_cast<size_t>(sp) * n_pad + t) *
+                                                                                rows_total + grow))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 v = p[0];
+#pragma unroll
+        for (int sp = 1; sp < kDecodeSplitsDown; ++sp)
+          if (sp < P.S) {
+            v.x += p[sp].x; v.y += p[sp].y; v.z += p[sp].z; v.w += p[sp].w;
+          }
+        if (a.b2) {
+          const float* b = a.b2 + grow;
+          v.x += b[0]; v.y += b[1]; v.z += b[2]; v.w += b[3];
+        }
+        const float gk = a.gate[t * Sl + k];
+        const float y[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = k == 0 ? __fmul_rn(gk, y[i]) : __fadd_rn(o[i], __fmul_rn(gk, y[i]));
+      }
+      if (a.out_bf16) {
+        uint2 pk;
+        pk.x = pack_bf16(o[0], o[1]);
+        pk.y = pack_bf16(o[2], o[3]);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(t) * d + c) = pk;
+      } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + static_cast<size_t>(t) * d + c) =
+            make_float4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  };
+
   // Epilogue: thread = weight row of the item's tile; token column t kept when t was routed to e.
-  auto epilogue = [&](const Phase& P) {
+  // With `combine`, each item then counts itself done for its weight tile; the CTA completing the
+  // tile's last item (every active expert, every split) combines that tile's output columns.
+  auto epilogue = [&](const Phase& P, bool combine) {
     const int q = warp & 3;
     const size_t rows_total = static_cast<size_t>(E) * P.rows;
     for (int it = blockIdx.x; it < P.total; it += gridDim.x) {
@@ -310,6 +374,7 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
       const unsigned long long mask = s_mask[im.e];
       bool ok = mbar_wait(tfull0 + 8 * acc, acc_phase, s_abort, a.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
+      if (combine) ok = epilogue_all(ok);  // the named barriers below need all four warps
       if (!ok) {
         if (lane == 0 && !*s_abort) atomicOr(a.status, kStatusTimeoutEpilogue);
         if (lane == 0) *s_abort = 1;
@@ -334,6 +399,21 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
         acc = 0;
         acc_phase ^= 1u;
       }
+      if (combine) {
+        named_barrier_epilogue();  // all 128 rows of the item stored
+        if (threadIdx.x == 64) {
+          __threadfence();
+          const uint32_t before = atomicAdd(&a.tile_done[im.mt], 1u);
+          const bool last = before == static_cast<uint32_t>(n_act * P.S) - 1u;
+          if (last) {
+            __threadfence();
+            a.tile_done[im.mt] = 0;  // ready for the next forward
+          }
+          *s_last = last ? 1 : 0;
+        }
+        named_barrier_epilogue();
+        if (*s_last) combine_tile(P, im.mt);
+      }
     }
   };
 
@@ -346,7 +426,7 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) mma(PU);
   } else {
-    epilogue(PU);
+    epilogue(PU, false);
   }
   grid_barrier(a.sched, 1, s_abort, a.timeout_ns, a.status);
 
@@ -364,8 +444,8 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
         float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
         for (int s = 0; s < PU.S; ++s) {
           const float* P = a.partial + (static_cast<size_t>(s) * n_pad + t) * rows_total;
-          const float4 pg = *reinterpret_cast<const float4*>(P + grow);
-          const float4 pu = *reinterpret_cast<const float4*>(P + grow + 128);
+          const float4 pg = __ldcg(reinterpret_cast<const float4*>(P + grow));
+          const float4 pu = __ldcg(reinterpret_cast<const float4*>(P + grow + 128));
           g.x += pg.x; g.y += pg.y; g.z += pg.z; g.w += pg.w;
           u.x += pu.x; u.y += pu.y; u.z += pu.z; u.w += pu.w;
         }
@@ -377,8 +457,8 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
         const size_t grow = static_cast<size_t>(e) * a.n_up + c;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s = 0; s < PU.S; ++s) {
-          const float4 p = *reinterpret_cast<const float4*>(a.partial + (static_cast<size_t>(s) * n_pad + t) *
-                                                                            rows_total + grow);
+          const float4 p = __ldcg(reinterpret_cast<const float4*>(a.partial + (static_cast<size_t>(s) * n_pad + t) *
+                                                                                  rows_total + grow));
           v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
         }
         const float* b = a.b1 + static_cast<size_t>(e) * f + c;
@@ -396,56 +476,69 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
   }
   grid_barrier(a.sched, 2, s_abort, a.timeout_ns, a.status);
 
-  // ---------------------------------------------------------------- phase D
+  // ---------------------------------------------------------------- phase D (+ combine per tile)
   if (warp == 0) {
     if (lane == 0) produce(PD, pre, pre_start);
   } else if (warp == 1) {
     if (lane == 0) mma(PD);
   } else {
-    epilogue(PD);
+    epilogue(PD, a.tile_combine != 0);
   }
-  grid_barrier(a.sched, 3, s_abort, a.timeout_ns, a.status);
-
-  // ---------------------------------------------------------------- phase C: combine in slot order
-  if (!*s_abort) {
-    const int d = a.d, d4 = d / 4;
-    const size_t rows_total = static_cast<size_t>(E) * d;
-    for (int w = gtid; w < T * d4; w += gstride) {
-      const int t = w / d4, c = (w - t * d4) * 4;
-      float o[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int k = 0; k < Sl; ++k) {
-        const int e = a.idx[t * Sl + k];
-        const size_t grow = static_cast<size_t>(e) * d + c;
-        float4 p[kDecodeSplitsDown];
+  if (!a.tile_combine) {
+    // ------------------------------------------------------------ phase C: combine after a barrier
+    grid_barrier(a.sched, 3, s_abort, a.timeout_ns, a.status);
+    if (!*s_abort) {
+      const int d = a.d, d4 = d / 4;
+      const size_t rows_total = static_cast<size_t>(E) * d;
+      for (int w = gtid; w < T * d4; w += gstride) {
+        const int t = w / d4, c = (w - t * d4) * 4;
+        float o[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k = 0; k < Sl; ++k) {
+          const int e = a.idx[t * Sl + k];
+          const size_t grow = static_cast<size_t>(e) * d + c;
+          float4 p[kDecodeSplitsDown];
 #pragma unroll
-        for (int s = 0; s < kDecodeSplitsDown; ++s)
-          p[s] = s < PD.S ? *reinterpret_cast<const float4*>(a.partial + (static_cast<size_t>(s) * n_pad + t) *
-                                                                             rows_total + grow)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 v = p[0];
+          for (int sp = 0; sp < kDecodeSplitsDown; ++sp)
+            p[sp] = sp < PD.S ? __ldcg(reinterpret_cast<const float4*>(
+                                    a.partial + (static_cast<size_t>(sp) * n_pad + t) * rows_total + grow))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+          float4 v = p[0];
 #pragma unroll
-        for (int s = 1; s < kDecodeSplitsDown; ++s)
-          if (s < PD.S) {
-            v.x += p[s].x; v.y += p[s].y; v.z += p[s].z; v.w += p[s].w;
+          for (int sp = 1; sp < kDecodeSplitsDown; ++sp)
+            if (sp < PD.S) {
+              v.x += p[sp].x; v.y += p[sp].y; v.z += p[sp].z; v.w += p[sp].w;
+            }
+          if (a.b2) {
+            const float* b = a.b2 + grow;
+            v.x += b[0]; v.y += b[1]; v.z += b[2]; v.w += b[3];
           }
-        if (a.b2) {
-          const float* b = a.b2 + grow;
-          v.x += b[0]; v.y += b[1]; v.z += b[2]; v.w += b[3];
-        }
-        const float gk = a.gate[t * Sl + k];
-        const float y[4] = {v.x, v.y, v.z, v.w};
+          const float gk = a.gate[t * Sl + k];
+          const float y[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = k == 0 ? __fmul_rn(gk, y[i]) : __fadd_rn(o[i], __fmul_rn(gk, y[i]));
+          for (int i = 0; i < 4; ++i) o[i] = k == 0 ? __fmul_rn(gk, y[i]) : __fadd_rn(o[i], __fmul_rn(gk, y[i]));
+        }
+        if (a.out_bf16) {
+          uint2 pk;
+          pk.x = pack_bf16(o[0], o[1]);
+          pk.y = pack_bf16(o[2], o[3]);
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(t) * d + c) = pk;
+        } else {
+          *reinterpret_cast<float4*>(static_cast<float*>(a.out) + static_cast<size_t>(t) * d + c) =
+              make_float4(o[0], o[1], o[2], o[3]);
+        }
       }
-      if (a.out_bf16) {
-        uint2 pk;
-        pk.x = pack_bf16(o[0], o[1]);
-        pk.y = pack_bf16(o[2], o[3]);
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(t) * d + c) = pk;
-      } else {
-        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + static_cast<size_t>(t) * d + c) =
-            make_float4(o[0], o[1], o[2], o[3]);
-      }
+    }
+  }
+
+  // row bookkeeping of the dispatch layout (what get_routing reports; nothing here reads it)
+  for (int i = gtid; i < n_slots; i += gstride) {
+    const int t = i / Sl;
+    const int r = a.chunk_base[static_cast<size_t>(t / kRouterChunk) * E + a.idx[i]] + a.row_of[i];
+    if (r >= 0 && r < a.rows_alloc) {
+      a.row_of[i] = r;
+      a.token_of_row[r] = t;
+    } else {
+      atomicOr(a.status, kStatusBadRow);
     }
   }
 

@@ -59,6 +59,8 @@ struct RouterArgs {
   int S;                   // slots per token = k + shared
   int Ex;                  // scheduled experts = E + shared
   float* zero_out;         // fused combine: out [T, d] fp32 rows of this CTA's tokens cleared, else nullptr
+  uint32_t* tile_done;     // cooperative decode kernel's per-tile counters, cleared by the last CTA
+  int n_tile_done;
 };
 
 struct GatherArgs {
@@ -179,6 +181,8 @@ struct FusedDecodeArgs {
   int out_bf16, swiglu;
   uint64_t timeout_ns;
   int32_t* status;
+  uint32_t* tile_done;      // [d / 128] items finished per down-projection weight tile (self-resetting)
+  int tile_combine;         // 1: combine per tile by its last CTA; 0: after a grid barrier
 };
 
 // fp32 SIMT grouped GEMM operands (row-major, K contiguous)

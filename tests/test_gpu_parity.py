@@ -138,16 +138,17 @@ def test_decode_path_matches_oracle_and_prefill_path(T, monkeypatch):
     assert rel_err(out_d, out_p) <= TOL_BF16
 
 
-@pytest.mark.parametrize("case", ["t1", "t7", "t33", "t64", "relu", "k4-shared"])
+@pytest.mark.parametrize("case", ["t1", "t3", "t7", "t33", "t64", "relu", "k4-shared", "k4-shared-t4"])
 def test_cooperative_decode_kernel_equals_separate_kernels(case, monkeypatch):
     """Decode batches run one cooperative kernel (grid barriers between up GEMM, activation, down GEMM
     and combine; x itself as the up GEMM's token operand).  It sums the same partials in the same order
-    as the separate kernels, so outputs and routing bookkeeping agree bit for bit."""
+    as the separate kernels, so outputs and routing bookkeeping agree bit for bit.  Batches of <= 4
+    tokens combine per output tile in the CTA finishing the tile; larger ones after a grid barrier."""
     if case == "relu":
         shape = testgen.LayerShape("coop-relu", 20, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")
-    elif case == "k4-shared":
-        shape = testgen.LayerShape("coop-k4s", 40, 512, 384, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True,
-                                   top_k=4, shared_expert=True)
+    elif case.startswith("k4-shared"):
+        shape = testgen.LayerShape("coop-k4s", 4 if case.endswith("t4") else 40, 512, 384, 8, testgen.ACT_SWIGLU,
+                                   "bf16", zipf_router_bias=True, top_k=4, shared_expert=True)
     else:
         shape = testgen.LayerShape("coop", int(case[1:]), 512, 384, 8, testgen.ACT_SWIGLU, "bf16",
                                    zipf_router_bias=True)
