@@ -128,11 +128,39 @@ __device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[kMaxSlots],
       a.rank[(size_t)S * (chunk_t0 + tt) + s] = r;
     }
   }
+  __shared__ int s_cnt[kMaxE];
   if (threadIdx.x < Ex) {
     int c = 0;
     for (int u = 0; u < valid; ++u)
       for (int q = 0; q < S; ++q) c += (s_idx[u][q] == (int)threadIdx.x);
-    a.hist[(size_t)blockIdx.x * Ex + threadIdx.x] = c;
+    if (gridDim.x > 1)
+      a.hist[(size_t)blockIdx.x * Ex + threadIdx.x] = c;
+    else
+      s_cnt[threadIdx.x] = c;
+  }
+  if (gridDim.x == 1) {
+    // one chunk (T <= 32, decode-sized batches): no other CTA to wait for, so the summary comes
+    // straight from this CTA's counts; the chunk's first row of each expert is the expert's offset
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int off = 0, mt = 0;
+      for (int e = 0; e < Ex; ++e) {
+        const int tot = s_cnt[e];
+        a.sched->counts[e] = tot;
+        a.sched->offsets[e] = off;
+        a.sched->mtile_start[e] = mt;
+        a.hist[e] = off;
+        const int tiles = (tot + kRowTile - 1) / kRowTile;
+        off += tiles * kRowTile;
+        mt += tiles;
+      }
+      a.sched->offsets[Ex] = off;
+      a.sched->mtile_start[Ex] = mt;
+      a.sched->ticket = 0;
+      a.sched->grid_sync = 0;
+      for (int i = 0; i < a.n_tile_done; ++i) a.tile_done[i] = 0;
+    }
+    return;
   }
   __threadfence();
   __syncthreads();
