@@ -100,6 +100,7 @@ constexpr int kNumStages = 5;  // router, gather, up GEMM, down GEMM, combine
 // Cooperative decode kernel: batches up to this size combine per tile (no third grid barrier);
 // measured on GB300 at the Mixtral shape: T=1 2 us faster, T=4 even, T >= 16 slower.
 constexpr int kTileCombineMaxT = 4;
+constexpr int kRouterTmaMinT = 1024;  // batches from this size use the TMA-staged router
 
 struct DeviceGuard {
   int prev = -1;
@@ -549,7 +550,15 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   RouterArgs ra{x, ctx->w_router, ctx->b_router, T, d, c.num_experts, ctx->dchunk, ctx->idx, ctx->gate,
                 ctx->row_of, ctx->hist, ctx->sched, ctx->k, c.gate_mode, c.has_shared_expert, ctx->S, ctx->Ex,
                 fuse && gather_a ? static_cast<float*>(out) : nullptr, ctx->tile_done, d / 128};
-  if (launch_router(c.dtype, ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  // large bf16 batches stream x into the router through shared memory by TMA (a per-call map of the
+  // caller's buffer); small ones read it straight from global memory
+  CUtensorMap tm_xr;
+  if (bf16 && T >= kRouterTmaMinT && d % router_tma_cols() == 0 &&
+      make_tmap(&tm_xr, x, d, static_cast<uint64_t>(T), kRouterChunk)) {
+    if (launch_router_tma(tm_xr, ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  } else if (launch_router(c.dtype, ra, nchunks, s) != cudaSuccess) {
+    return COLIBRI_ERR_CUDA;
+  }
   mark(1);
   GatherArgs ga{x, ctx->idx, ctx->row_of, ctx->hist, T, d, E, ctx->S, ctx->rows_alloc,
                 gather_a ? nullptr : ctx->xp, ctx->tok_of_row, ctx->sched, ctx->gate,

@@ -29,6 +29,7 @@ enum : int32_t {
   kStatusTimeoutEpilogue = 1 << 2,
   kStatusBadRow = 1 << 3,
   kStatusTimeoutGridSync = 1 << 4,
+  kStatusTimeoutRouter = 1 << 5,
 };
 
 // Routing summary in device memory.  Written by the last CTA of the router kernel, read by
@@ -249,6 +250,8 @@ __device__ __forceinline__ int active_experts(const Sched* sc, int E, int* list)
 
 // launchers (return cudaGetLastError() of the launch)
 cudaError_t launch_router(int dtype, const RouterArgs& a, int nchunks, cudaStream_t s);
+cudaError_t launch_router_tma(const CUtensorMap& tmx, const RouterArgs& a, int nchunks, cudaStream_t s);
+int router_tma_cols();  // the TMA-staged router needs d to be a multiple of this
 cudaError_t launch_gather(int dtype, const GatherArgs& a, cudaStream_t s);
 cudaError_t launch_combine(int out_dtype, const CombineArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_tc_gemm(int epi, bool gather_a, const CUtensorMap& tmA, const CUtensorMap& tmB,

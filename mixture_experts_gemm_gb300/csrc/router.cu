@@ -47,35 +47,50 @@ struct Vec<__nv_bfloat16> {
 };
 
 // Runs in the last router CTA: counts, padded offsets, M-tile prefix, and the first row of every
-// (chunk, expert) pair, written over the per-chunk counts.  Warp w scans experts w, w + 8, w + 16;
-// lane l of a warp owns a contiguous range of chunks, so one warp-wide scan gives every chunk's place
-// in chunk order.  Thread 0 then turns the expert totals into padded segment offsets.
+// (chunk, expert) pair, written over the per-chunk counts.  Thread t owns a contiguous range of
+// chunks and reads every expert's count of a chunk at once (independent loads, one L2 round trip
+// per chunk of its range); a block-wide exclusive scan over the threads, per expert, then gives every
+// chunk's place in chunk order.  Thread 0 turns the expert totals into padded segment offsets.
 __device__ void scan_offsets(const RouterArgs& a, int nchunks) {
-  constexpr int NW = kRouterThreads / 32;
-  constexpr int PER_WARP = (kMaxE + NW - 1) / NW;  // experts per warp
+  constexpr int NTH = kRouterThreads, NW = NTH / 32;
+  __shared__ int s_wsum[NW][kMaxE];  // per-warp totals, then their exclusive prefix over warps
   __shared__ int s_tot[kMaxE];
   __shared__ int s_off[kMaxE + 1];
   const int E = a.Ex;  // scheduled experts: routed (+ shared)
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int per = (nchunks + 31) / 32;
-  const int c0 = min(lane * per, nchunks), c1 = min(c0 + per, nchunks);
-  int excl[PER_WARP];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (nchunks + NTH - 1) / NTH;
+  const int c0 = min(tid * per, nchunks), c1 = min(c0 + per, nchunks);
+  int sum[kMaxE];
 #pragma unroll
-  for (int i = 0; i < PER_WARP; ++i) {
-    const int e = warp + i * NW;
-    excl[i] = 0;
-    if (e < E) {
-      int local = 0;
-      for (int c = c0; c < c1; ++c) local += __ldcg(&a.hist[(size_t)c * E + e]);
-      int inc = local;
+  for (int e = 0; e < kMaxE; ++e) sum[e] = 0;
+  for (int c = c0; c < c1; ++c) {
+    int v[kMaxE];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += n;
-      }
-      excl[i] = inc - local;
-      if (lane == 31) s_tot[e] = inc;
+    for (int e = 0; e < kMaxE; ++e) v[e] = e < E ? __ldcg(&a.hist[(size_t)c * E + e]) : 0;
+#pragma unroll
+    for (int e = 0; e < kMaxE; ++e) sum[e] += v[e];
+  }
+  int excl[kMaxE];
+#pragma unroll
+  for (int e = 0; e < kMaxE; ++e) {
+    int inc = sum[e];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += n;
     }
+    excl[e] = inc - sum[e];
+    if (lane == 31) s_wsum[warp][e] = inc;
+  }
+  __syncthreads();
+  if (tid < E) {
+    int run = 0;
+    for (int w = 0; w < NW; ++w) {
+      const int t = s_wsum[w][tid];
+      s_wsum[w][tid] = run;
+      run += t;
+    }
+    s_tot[tid] = run;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -98,17 +113,19 @@ __device__ void scan_offsets(const RouterArgs& a, int nchunks) {
     for (int i = 0; i < a.n_tile_done; ++i) a.tile_done[i] = 0;  // (normally already 0: self-resetting)
   }
   __syncthreads();
+  int run[kMaxE];
 #pragma unroll
-  for (int i = 0; i < PER_WARP; ++i) {
-    const int e = warp + i * NW;
-    if (e < E) {
-      int run = s_off[e] + excl[i];
-      for (int c = c0; c < c1; ++c) {
-        const int n = __ldcg(&a.hist[(size_t)c * E + e]);
-        a.hist[(size_t)c * E + e] = run;
-        run += n;
+  for (int e = 0; e < kMaxE; ++e) run[e] = e < E ? s_off[e] + s_wsum[warp][e] + excl[e] : 0;
+  for (int c = c0; c < c1; ++c) {
+    int v[kMaxE];
+#pragma unroll
+    for (int e = 0; e < kMaxE; ++e) v[e] = e < E ? __ldcg(&a.hist[(size_t)c * E + e]) : 0;
+#pragma unroll
+    for (int e = 0; e < kMaxE; ++e)
+      if (e < E) {
+        a.hist[(size_t)c * E + e] = run[e];
+        run[e] += v[e];
       }
-    }
   }
 }
 
@@ -487,6 +504,192 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_top2_mma_kernel(Rout
   finish_chunk(a, s_idx, valid, chunk_t0);
 }
 
+// Large batches: the same logits GEMM with x streamed through shared memory by TMA.  The CTA's 32
+// token rows arrive in stages of 512 columns (eight 64-column boxes, 128-byte swizzle: 1 KB of
+// every row at a time, which DRAM serves better than shorter pieces) in a kRtStages-deep ring, so
+// the copy engine keeps 96 KB per CTA in flight whatever the warps do;
+// warp (h, sl) multiplies the 16 rows of half h over its share of each stage's eight 32-column
+// blocks (fragments read from the swizzled rows without bank conflicts), W_r fragments come from
+// L1/L2 one stage ahead in registers.  Each warp sums its blocks stage by stage (a fixed order), the
+// warps' partial tiles are summed in slice order in shared memory; top-k and the histogram as above.
+constexpr int kRtStages = 3;
+constexpr int kRtCols = 512;                                 // columns per stage (1 KB of every row)
+constexpr int kRtBlk = kRtCols / 32;                         // 32-column blocks per stage
+constexpr int kRtStageBytes = kRouterChunk * kRtCols * 2;    // 32 KB
+constexpr int kRtSmem = 1024 + kRtStages * kRtStageBytes + 2 * kRtStages * 8;
+
+__device__ __forceinline__ uint32_t rt_smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ bool rt_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok = 0;
+  uint64_t t0 = 0;
+  for (int spin = 0;; ++spin) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    uint64_t now;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+    if (spin == 0) t0 = now;
+    else if (now - t0 > 2000000000ull) return false;  // 2 s: the copy engine never delivered
+  }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kRouterThreads, 2)
+    router_tma_kernel(const __grid_constant__ CUtensorMap tmx, RouterArgs a) {
+  constexpr int NW = kRouterThreads / 32;
+  constexpr int EMAX = 8 * NT;
+  extern __shared__ __align__(1024) uint8_t rt_raw[];
+  uint8_t* stg = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rt_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + kRtStages * kRtStageBytes);
+  const uint32_t full0 = rt_smem_u32(bars), empty0 = rt_smem_u32(bars + kRtStages);
+  __shared__ float s_part[NW][16][EMAX];
+  __shared__ int s_idx[kRouterChunk][kMaxSlots];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk_t0 = blockIdx.x * kRouterChunk;
+  const int T = a.T, d = a.d, E = a.E;
+  const int valid = min(kRouterChunk, T - chunk_t0);
+  const int H = valid > 16 ? 2 : 1;  // 16-token halves with work
+  const int S = NW / H;              // warps sharing a half: each takes 8 / S blocks of a stage
+  const int h = warp % H, sl = warp / H;
+  const int g = lane >> 2, q = lane & 3;
+  const int j0 = (kRtBlk * sl) / S, j1 = (kRtBlk * (sl + 1)) / S;  // this warp's blocks of each stage
+  constexpr int kJ = kRtBlk / 4;  // most blocks a warp takes per stage (4 or more warps share a half)
+  const int nst = d / kRtCols;
+  const uint4* wr[NT];
+  bool wv[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    wv[nt] = nt * 8 + g < E;
+    wr[nt] = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.w_router) +
+                                            (size_t)(wv[nt] ? nt * 8 + g : 0) * d);
+  }
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kRtStages; ++st) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(full0 + 8 * st), "r"(1) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empty0 + 8 * st), "r"(NW) : "memory");
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
+  }
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();  // x may come from the previous kernel; the workspace from the previous forward
+  zero_out_rows(a, chunk_t0, valid);
+  auto issue = [&](int st) {  // thread 0: stage st into slot st % kRtStages
+    const int slot = st % kRtStages;
+    const uint32_t fb = full0 + 8 * slot;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(kRtStageBytes) : "memory");
+#pragma unroll
+    for (int b = 0; b < kRtCols / 64; ++b)
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+          "[%4];" ::"r"(rt_smem_u32(stg + slot * kRtStageBytes + b * 4096)),
+          "l"(reinterpret_cast<uint64_t>(&tmx)), "r"(st * kRtCols + b * 64), "r"(chunk_t0), "r"(fb)
+          : "memory");
+  };
+  if (threadIdx.x == 0)
+    for (int st = 0; st < kRtStages && st < nst; ++st) issue(st);
+
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+  // W_r fragments of this warp's blocks, one stage ahead
+  uint4 Bn[kJ][NT];
+  auto load_b = [&](int st) {
+#pragma unroll
+    for (int u = 0; u < kJ; ++u)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int j = j0 + u;
+        Bn[u][nt] = (j < j1 && wv[nt]) ? __ldg(wr[nt] + 4 * (st * kRtBlk + j) + q) : make_uint4(0u, 0u, 0u, 0u);
+      }
+  };
+  load_b(0);
+  bool ok = true;
+  const int r_lo = 16 * h + g, r_hi = r_lo + 8;  // rows of this lane inside the CTA's 32
+  for (int st = 0; st < nst; ++st) {
+    const int slot = st % kRtStages;
+    const uint32_t par = static_cast<uint32_t>((st / kRtStages) & 1);
+    uint4 B[kJ][NT];
+#pragma unroll
+    for (int u = 0; u < kJ; ++u)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) B[u][nt] = Bn[u][nt];
+    if (st + 1 < nst) load_b(st + 1);
+    if (ok && !rt_wait(full0 + 8 * slot, par)) {
+      ok = false;
+      atomicOr(&a.sched->status, kStatusTimeoutRouter);
+    }
+    const uint8_t* sb = stg + slot * kRtStageBytes;
+#pragma unroll
+    for (int u = 0; u < kJ; ++u) {
+      const int j = j0 + u;
+      if (j < j1) {
+        // block j: box j / 2, 16-byte chunk 4 * (j % 2) + q of the row, swizzled by row % 8
+        const int c = 4 * (j & 1) + q;
+        const uint8_t* box = sb + (j >> 1) * 4096;
+        const uint4 A0 = *reinterpret_cast<const uint4*>(box + r_lo * 128 + ((c ^ (r_lo & 7)) << 4));
+        const uint4 A1 = *reinterpret_cast<const uint4*>(box + r_hi * 128 + ((c ^ (r_hi & 7)) << 4));
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          asm volatile(
+              "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+              "{%0,%1,%2,%3};"
+              : "+f"(acc[nt][0]), "+f"(acc[nt][1]), "+f"(acc[nt][2]), "+f"(acc[nt][3])
+              : "r"(A0.x), "r"(A1.x), "r"(A0.y), "r"(A1.y), "r"(B[u][nt].x), "r"(B[u][nt].y));
+          asm volatile(
+              "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+              "{%0,%1,%2,%3};"
+              : "+f"(acc[nt][0]), "+f"(acc[nt][1]), "+f"(acc[nt][2]), "+f"(acc[nt][3])
+              : "r"(A0.z), "r"(A1.z), "r"(A0.w), "r"(A1.w), "r"(B[u][nt].z), "r"(B[u][nt].w));
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty0 + 8 * slot) : "memory");
+    if (threadIdx.x == 0 && st + kRtStages < nst) {
+      // the slot is refilled once all warps have read it
+      if (ok && !rt_wait(empty0 + 8 * slot, par)) {
+        ok = false;
+        atomicOr(&a.sched->status, kStatusTimeoutRouter);
+      }
+      if (ok) issue(st + kRtStages);
+    }
+  }
+  // every copy issued has landed before the CTA may leave (bounded)
+  if (threadIdx.x == 0)
+    for (int st = nst - kRtStages > 0 ? nst - kRtStages : 0; st < nst; ++st)
+      rt_wait(full0 + 8 * (st % kRtStages), static_cast<uint32_t>((st / kRtStages) & 1));
+  // D fragment: acc[nt][0..1] = rows g, experts nt*8 + 2q, +1; acc[nt][2..3] = row g + 8
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    s_part[warp][g][nt * 8 + 2 * q] = acc[nt][0];
+    s_part[warp][g][nt * 8 + 2 * q + 1] = acc[nt][1];
+    s_part[warp][g + 8][nt * 8 + 2 * q] = acc[nt][2];
+    s_part[warp][g + 8][nt * 8 + 2 * q + 1] = acc[nt][3];
+  }
+  __syncthreads();
+  if (sl == 0 && lane < 16) {
+    const int t = chunk_t0 + 16 * h + lane;
+    float L[EMAX];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+      float v = s_part[h][lane][e];
+      for (int w = 1; w < S; ++w) v += s_part[h + w * H][lane][e];
+      L[e] = v + ((a.b_router != nullptr && e < E) ? a.b_router[e] : 0.f);
+    }
+    topk_store<EMAX>(a, L, t, s_idx[16 * h + lane]);
+  }
+  __syncthreads();
+  finish_chunk(a, s_idx, valid, chunk_t0);
+}
+
 template <typename Tin, int EMAX>
 cudaError_t launch_router_t(const RouterArgs& a, int nchunks, cudaStream_t s) {
   const int smem = EMAX * a.dchunk * (int)sizeof(Tin);
@@ -502,6 +705,12 @@ cudaError_t prepare_router_t() {
 }  // namespace
 
 cudaError_t prepare_router(int dtype, int E) {
+  if (dtype != 0) {
+    cudaError_t e = cudaFuncSetAttribute(router_tma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(router_tma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
+    if (e != cudaSuccess) return e;
+  }
   if (dtype == 0) return E <= 4 ? prepare_router_t<float, 4>() : E <= 8 ? prepare_router_t<float, 8>()
                                                                        : prepare_router_t<float, 16>();
   return E <= 4 ? prepare_router_t<__nv_bfloat16, 4>() : E <= 8 ? prepare_router_t<__nv_bfloat16, 8>()
@@ -511,6 +720,14 @@ cudaError_t prepare_router(int dtype, int E) {
 int router_smem_bytes(int dtype, int E, int dchunk) {
   const int emax = E <= 4 ? 4 : (E <= 8 ? 8 : 16);
   return emax * dchunk * (dtype == 0 ? 4 : 2);
+}
+
+int router_tma_cols() { return kRtCols; }
+
+// bf16, d a multiple of router_tma_cols(); tmx maps x [T, d] with 64 x 32 boxes, 128-byte swizzle
+cudaError_t launch_router_tma(const CUtensorMap& tmx, const RouterArgs& a, int nchunks, cudaStream_t s) {
+  if (a.E <= 8) return pdl_launch(router_tma_kernel<1>, dim3(nchunks), dim3(kRouterThreads), kRtSmem, s, tmx, a);
+  return pdl_launch(router_tma_kernel<2>, dim3(nchunks), dim3(kRouterThreads), kRtSmem, s, tmx, a);
 }
 
 cudaError_t launch_router(int dtype, const RouterArgs& a, int nchunks, cudaStream_t s) {
