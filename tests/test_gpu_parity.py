@@ -118,6 +118,15 @@ def test_small_bf16_swiglu(T):
     _full_check(li)
 
 
+@pytest.mark.parametrize("T,d", [(1040, 512), (1057, 512), (1100, 1024), (1100, 768)])
+def test_tma_router_ragged_last_chunk(T, d):
+    """Batches of >= 1024 tokens with d a multiple of 512 stream x into the router by TMA: a last
+    chunk of 16, 17 or 12 valid rows (rows past T read as zeros), and a d that is not a multiple of
+    512 (the global-load router instead) must all route exactly as the oracle."""
+    shape = testgen.LayerShape("tma-router", T, d, 256, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True)
+    _full_check(testgen.make_inputs(shape))
+
+
 def test_small_bf16_relu_bias_with_router_bias():
     shape = testgen.LayerShape("small-relu", 500, 512, 512, 6, testgen.ACT_RELU_BIAS, "bf16", zipf_router_bias=True)
     li = testgen.make_inputs(shape)
