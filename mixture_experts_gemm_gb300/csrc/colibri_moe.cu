@@ -85,6 +85,7 @@ struct colibri_moe {
   bool pair_gemm = false;    // prefill GEMMs on CTA pairs (256x256 tiles)
   bool fuse_combine = true;  // two-slot fp32 layers: gate-weighted combine inside the down GEMM
   bool gather_a = false;     // bf16 prefill: up GEMM reads A rows from x through token_of_row
+  bool dynamic_tiles = true; // CTA-pair GEMMs take tiles in index order from a shared counter
   int pair_ctas = 0;         // co-resident CTAs of the pair kernel (persistent grid size)
   bool decode_fused = true;  // decode batches: one cooperative kernel after the router
   int fused_ctas = 0;        // its grid (one CTA per SM)
@@ -195,6 +196,12 @@ bool env_gather_a() {
   return s && std::strcmp(s, "fused") == 0;
 }
 
+// CTA-pair GEMMs hand out tiles in index order at run time unless COLIBRI_MOE_TILE_ORDER=static.
+bool env_dynamic_tiles() {
+  const char* s = std::getenv("COLIBRI_MOE_TILE_ORDER");
+  return !(s && std::strcmp(s, "static") == 0);
+}
+
 // Prefill GEMMs run on CTA pairs (cta_group::2) unless COLIBRI_MOE_GEMM=1sm selects the single-CTA kernel.
 bool env_pair_gemm() {
   const char* s = std::getenv("COLIBRI_MOE_GEMM");
@@ -292,6 +299,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   c->pair_gemm = env_pair_gemm() && (sms % 2 == 0);
   c->fuse_combine = env_fuse_combine();
   c->gather_a = env_gather_a();
+  c->dynamic_tiles = env_dynamic_tiles();
   const int64_t d = cfg->d_model, f = cfg->d_ff, E = cfg->num_experts, T = cfg->max_tokens;
   c->esize = cfg->dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
   c->out_esize = cfg->out_dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
@@ -614,7 +622,8 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     const int bn = tc_gemm_block_n();
     const int64_t max_pairs = (max_mtiles + E + 1) / 2;
     GemmArgs up{ctx->sched, E, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns,
-                &ctx->sched->status, ctx->tok_of_row, nullptr, x, clear_in_gemm, out_vec4};
+                &ctx->sched->status, ctx->tok_of_row, nullptr, x,
+                ctx->dynamic_tiles ? &ctx->sched->tile_ctr[0] : nullptr, clear_in_gemm, out_vec4};
     int64_t ctas = 2 * max_pairs * up.n_tiles;
     int grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
     if (launch_pair_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, gather_a, ctx->tm_xp, ctx->tm_w13_dec, up, grid, s) !=
@@ -622,7 +631,8 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
       return COLIBRI_ERR_CUDA;
     mark(3);
     GemmArgs dn{ctx->sched, E, f, d, d / bn, fuse ? out : ctx->y, d, ctx->b2, d, ctx->timeout_ns,
-                &ctx->sched->status, ctx->tok_of_row, ctx->gate_of_row};
+                &ctx->sched->status, ctx->tok_of_row, ctx->gate_of_row, nullptr,
+                ctx->dynamic_tiles ? &ctx->sched->tile_ctr[1] : nullptr};
     ctas = 2 * max_pairs * dn.n_tiles;
     grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
     if (launch_pair_gemm(fuse ? kEpiCombineF32 : kEpiStoreF32, false, ctx->tm_h, ctx->tm_w2_dec, dn, grid, s) !=
@@ -631,7 +641,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   } else if (bf16) {
     const int bn = tc_gemm_block_n();
     GemmArgs up{ctx->sched, E, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns,
-                &ctx->sched->status, ctx->tok_of_row, nullptr, x, clear_in_gemm, out_vec4};
+                &ctx->sched->status, ctx->tok_of_row, nullptr, x, nullptr, clear_in_gemm, out_vec4};
     int64_t tiles = max_mtiles * up.n_tiles;
     int grid = static_cast<int>(tiles < ctx->num_sms ? tiles : ctx->num_sms);
     if (launch_tc_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, gather_a, ctx->tm_xp, ctx->tm_w13, up, grid, s) !=

@@ -37,8 +37,10 @@ constexpr int PNUM_THREADS = 192;
 constexpr int PNUM_THREADS_ZERO = 192 + 32 * kZeroWarps;  // + the warps clearing out (up GEMM)
 constexpr int PNUM_THREADS_GA = 192 + 32 * (kGatherWarps + kForwarders);  // + A gather and forwarder warps
 constexpr uint32_t PTMEM_COLS = 512;
-constexpr int PNUM_BARS = 3 * PSTAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain, gfull
-constexpr int PSMEM_BYTES = 1024 + PSTAGES * PSTAGE_BYTES + PNUM_BARS * 8 + 16 + 4 * (4 * kMaxE + 4);
+constexpr int PTQ = 4;  // tile-id queue depth (dynamic tile order)
+// full, empty, tmem_full[2], tmem_empty[2], drain, gfull, tile queue full / empty
+constexpr int PNUM_BARS = 3 * PSTAGES + 5 + 2 * PTQ;
+constexpr int PSMEM_BYTES = 1024 + PSTAGES * PSTAGE_BYTES + PNUM_BARS * 8 + 16 + 4 * (4 * kMaxE + 4 + PTQ);
 static_assert(PSMEM_BYTES <= 227 * 1024, "pair GEMM shared memory");
 static_assert(PSTAGES % kForwarders == 0, "a stage keeps its forwarder across ring cycles");
 
@@ -73,6 +75,7 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
   int* s_offsets = s_counts + kMaxE;
   int* s_mstart = s_offsets + kMaxE + 1;
   int* s_pstart = s_mstart + kMaxE + 1;
+  volatile int* s_tile = s_pstart + kMaxE + 1;  // tile-id queue (dynamic order)
 
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = smem_u32(bars + PSTAGES);
@@ -80,6 +83,9 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
   const uint32_t tempty0 = smem_u32(bars + 2 * PSTAGES + 2);
   const uint32_t drain = smem_u32(bars + 2 * PSTAGES + 4);
   const uint32_t gfull0 = smem_u32(bars + 2 * PSTAGES + 5);  // gathered A: rows of a stage landed
+  const uint32_t tqf0 = smem_u32(bars + 3 * PSTAGES + 5);     // tile queue: slot written (each CTA)
+  const uint32_t tqe0 = smem_u32(bars + 3 * PSTAGES + 5 + PTQ);  // tile queue: slot read (leader's)
+  const bool DYN = !GA && a.tile_ctr != nullptr;  // tiles handed out in order at run time (see below)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E;
@@ -100,6 +106,10 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
     mbar_init(drain, 1);
     if constexpr (GA)
       for (int s = 0; s < PSTAGES; ++s) mbar_init(gfull0 + 8 * s, kGatherThreads);
+    for (int i = 0; i < PTQ; ++i) {
+      mbar_init(tqf0 + 8 * i, 1);   // the leader's producer
+      mbar_init(tqe0 + 8 * i, 10);  // leader: MMA + 4 epilogue warps; peer: producer + 4 epilogue warps
+    }
     *s_abort = 0;
     fence_mbar_init();
     if constexpr (!GA) prefetch_tmap(&tmA);
@@ -133,13 +143,80 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
   const int num_kb = (a.K + PBK - 1) / PBK;
   const int pair_id = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
 
+  // Tile order.  Static: pair i takes tiles i, i + n_pairs, ...  Dynamic (DYN): the leader's producer
+  // takes the next tile index from a counter shared by all pairs (one atomic per tile) and hands it
+  // to the pair's other roles through a PTQ-deep queue in both CTAs' shared memory, so tiles run in
+  // index order whatever the pairs' speeds: the pairs that share a weight tile (consecutive indices)
+  // stay together and read it from L2, where a static order lets them drift apart over a launch.
+  struct Seq {
+    int slot = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+  };
+  auto take = [&](Seq& sq, bool arrive) -> int {  // next id from this CTA's queue; -1 = no more
+    if (!mbar_wait_cluster(tqf0 + 8 * sq.slot, sq.ph, s_abort, a.timeout_ns)) {
+      sq.ok = false;
+      return -1;
+    }
+    const int p = s_tile[sq.slot];
+    if (arrive) {
+      if (leader)
+        mbar_arrive(tqe0 + 8 * sq.slot);
+      else
+        mbar_arrive_peer(mapa_shared(tqe0 + 8 * sq.slot, 0));
+    }
+    if (++sq.slot == PTQ) {
+      sq.slot = 0;
+      sq.ph ^= 1u;
+    }
+    return p;
+  };
+  auto seq_first = [&](Seq& sq, bool arrive) -> int {
+    if (DYN) return take(sq, arrive);
+    return pair_id < total ? pair_id : -1;
+  };
+  auto seq_next = [&](Seq& sq, int p, bool arrive) -> int {
+    if (DYN) return take(sq, arrive);
+    p += n_pairs;
+    return p < total ? p : -1;
+  };
+
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer (both CTAs)
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
-      for (int p = pair_id; ok && p < total; p += n_pairs) {
+      Seq sq, pub;  // pub: the leader's publishing position in the queue
+      auto publish = [&](int p) -> bool {
+        if (!mbar_wait(tqe0 + 8 * pub.slot, pub.ph ^ 1u, s_abort, a.timeout_ns)) return false;
+        s_tile[pub.slot] = p;
+        st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(s_tile + pub.slot)), 1), p);
+        mbar_arrive(tqf0 + 8 * pub.slot);
+        mbar_arrive_remote(mapa_shared(tqf0 + 8 * pub.slot, 1));  // release.cluster: the id is there
+        if (++pub.slot == PTQ) {
+          pub.slot = 0;
+          pub.ph ^= 1u;
+        }
+        return true;
+      };
+      auto fetch = [&]() -> int {
+        const int p = static_cast<int>(atomicAdd(a.tile_ctr, 1u));
+        return p < total ? p : -1;
+      };
+      int p, p_next = -1;
+      if (DYN && leader) {  // the leader hands out ids one tile ahead of its own copies
+        p = fetch();
+        ok = publish(p);
+        if (ok && p >= 0) {
+          p_next = fetch();
+          ok = publish(p_next);
+        }
+      } else {
+        p = seq_first(sq, true);
+        ok = sq.ok;
+      }
+      for (; ok && p >= 0;) {
         const PairCoord c = decode_pair(p, s_pstart, E, a.n_tiles);
         const int a_row = s_offsets[c.e] + (2 * c.pm + static_cast<int>(rank)) * PBM;
         const int b_row = c.e * a.n_per_expert + c.n * PBN + static_cast<int>(rank) * (PBN / 2);
@@ -161,6 +238,17 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
             stage = 0;
             phase ^= 1u;
           }
+        }
+        if (!ok) break;
+        if (DYN && leader) {
+          p = p_next;
+          if (p >= 0) {
+            p_next = fetch();
+            ok = publish(p_next);
+          }
+        } else {
+          p = seq_next(sq, p, true);
+          ok = sq.ok;
         }
       }
       if (!ok) {
@@ -246,8 +334,10 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
       constexpr uint32_t idesc = make_idesc_bf16(2 * PBM, PBN);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      for (int p = pair_id; ok && p < total; p += n_pairs) {
+      Seq sq;
+      int p = seq_first(sq, true);
+      bool ok = sq.ok;
+      for (; ok && p >= 0; p = seq_next(sq, p, true), ok = ok && sq.ok) {
         if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, s_abort, a.timeout_ns)) {
           ok = false;
           break;
@@ -294,7 +384,8 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
     const int q = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int p = pair_id; p < total; p += n_pairs) {
+    Seq sq;
+    for (int p = seq_first(sq, lane == 0); __all_sync(0xffffffffu, sq.ok) && p >= 0; p = seq_next(sq, p, lane == 0)) {
       const PairCoord c = decode_pair(p, s_pstart, E, a.n_tiles);
       bool ok = mbar_wait(tfull0 + 8 * acc, acc_phase, s_abort, a.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);

@@ -40,6 +40,7 @@ struct Sched {
   int32_t mtile_start[kMaxE + 1];  // prefix sum of ceil(counts / 128): M tiles before each expert
   uint32_t ticket;                 // router CTAs finished (reset to 0 by the last one)
   uint32_t grid_sync;              // arrivals at the cooperative decode kernel's grid barriers (reset by the router)
+  uint32_t tile_ctr[2];            // next tile of the up / down CTA-pair GEMM (reset by the router)
   int32_t status;                  // device status word (kStatus* bits)
 };
 
@@ -110,6 +111,7 @@ struct GemmArgs {
   const int32_t* token_of_row;  // kEpiCombineF32 and gathered A: token of each row
   const float* gate_of_row;     // kEpiCombineF32: gate of each row
   const void* gather_x;         // gathered A: token rows x [T, K] bf16 (16-byte aligned rows)
+  uint32_t* tile_ctr;           // CTA-pair kernel: next tile index to hand out (cleared by the router)
   float4* zero_out;             // up GEMM with the combine fused downstream: out cleared by two extra
   int64_t zero_vec4;            //   warps per CTA (zero_vec4 float4s), else nullptr
 };
