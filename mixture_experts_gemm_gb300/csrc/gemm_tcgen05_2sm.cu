@@ -143,11 +143,13 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
   const int num_kb = (a.K + PBK - 1) / PBK;
   const int pair_id = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
 
-  // Tile order.  Static: pair i takes tiles i, i + n_pairs, ...  Dynamic (DYN): the leader's producer
-  // takes the next tile index from a counter shared by all pairs (one atomic per tile) and hands it
-  // to the pair's other roles through a PTQ-deep queue in both CTAs' shared memory, so tiles run in
-  // index order whatever the pairs' speeds: the pairs that share a weight tile (consecutive indices)
-  // stay together and read it from L2, where a static order lets them drift apart over a launch.
+  // Tile order.  Static: pair i takes tiles i, i + n_pairs, ...  Dynamic (DYN): pair i starts with
+  // tile i; after that the leader's producer takes the next tile index from a counter shared by all
+  // pairs (n_pairs + one atomic per tile, fetched while the current tile's first stage is in flight)
+  // and hands it to the pair's other roles through a PTQ-deep queue in both CTAs' shared memory, so
+  // tiles run in index order whatever the pairs' speeds: the pairs that share a weight tile
+  // (consecutive indices) stay together and read it from L2, where a static order lets them drift
+  // apart over a launch.
   struct Seq {
     int slot = 0;
     uint32_t ph = 0;
@@ -171,8 +173,9 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
     }
     return p;
   };
-  auto seq_first = [&](Seq& sq, bool arrive) -> int {
-    if (DYN) return take(sq, arrive);
+  auto seq_first = [&](Seq& sq, bool arrive) -> int {  // the first tile is pair_id in both orders
+    (void)sq;
+    (void)arrive;
     return pair_id < total ? pair_id : -1;
   };
   auto seq_next = [&](Seq& sq, int p, bool arrive) -> int {
@@ -201,21 +204,10 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
         return true;
       };
       auto fetch = [&]() -> int {
-        const int p = static_cast<int>(atomicAdd(a.tile_ctr, 1u));
+        const int p = n_pairs + static_cast<int>(atomicAdd(a.tile_ctr, 1u));
         return p < total ? p : -1;
       };
-      int p, p_next = -1;
-      if (DYN && leader) {  // the leader hands out ids one tile ahead of its own copies
-        p = fetch();
-        ok = publish(p);
-        if (ok && p >= 0) {
-          p_next = fetch();
-          ok = publish(p_next);
-        }
-      } else {
-        p = seq_first(sq, true);
-        ok = sq.ok;
-      }
+      int p = seq_first(sq, true), p_next = -1;
       for (; ok && p >= 0;) {
         const PairCoord c = decode_pair(p, s_pstart, E, a.n_tiles);
         const int a_row = s_offsets[c.e] + (2 * c.pm + static_cast<int>(rank)) * PBM;
@@ -238,14 +230,17 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
             stage = 0;
             phase ^= 1u;
           }
+          if (DYN && leader && kb == 0) {  // the next tile, while this tile's first stage loads
+            p_next = fetch();
+            if (!publish(p_next)) {
+              ok = false;
+              break;
+            }
+          }
         }
         if (!ok) break;
         if (DYN && leader) {
           p = p_next;
-          if (p >= 0) {
-            p_next = fetch();
-            ok = publish(p_next);
-          }
         } else {
           p = seq_next(sq, p, true);
           ok = sq.ok;
