@@ -81,6 +81,7 @@ struct colibri_moe {
   CUtensorMap tm_w13_dec{}, tm_w2_dec{}, tm_xp_dec[4]{}, tm_h_dec[4]{};
   float* partial = nullptr;  // decode partial sums [splits][n_pad][E * rows]
   uint32_t* tile_done = nullptr;  // cooperative decode kernel: items done per down-projection tile
+  float* split_part = nullptr;    // split router: partial logits of small batches
   int decode_max_t = 0;
   bool pair_gemm = false;    // prefill GEMMs on CTA pairs (256x256 tiles)
   bool fuse_combine = true;  // two-slot fp32 layers: gate-weighted combine inside the down GEMM
@@ -102,6 +103,8 @@ constexpr int kNumStages = 5;  // router, gather, up GEMM, down GEMM, combine
 // measured on GB300 at the Mixtral shape: T=1 2 us faster, T=4 even, T >= 16 slower.
 constexpr int kTileCombineMaxT = 4;
 constexpr int kRouterTmaMinT = 1024;  // batches from this size use the TMA-staged router
+constexpr int kRouterSplitMinT = 16;   // batches above this size (and up to 64) use the split router
+// (Mixtral-shaped router stage, GB300: T=32 23.2 -> 16.9 us split; T=16 equal; T=1 9.1 -> 10.5 us)
 
 struct DeviceGuard {
   int prev = -1;
@@ -345,6 +348,8 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
                                   : 0;
   const size_t o_part = carve(part_floats * 4);
   const size_t o_tiles = carve((d / 128 + 1) * sizeof(uint32_t));
+  const size_t o_spart = carve(static_cast<size_t>(kRouterSplitMaxChunks) * router_split_factor() * kRouterChunk *
+                               16 * sizeof(float));
   const size_t o_xs = carve(T * d * c->esize);
   const size_t o_os = carve(T * d * c->out_esize);
   const size_t o_xs2 = carve(T * d * c->esize);
@@ -368,6 +373,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   c->sched = reinterpret_cast<Sched*>(b + o_sched);
   c->partial = part_floats > 0 ? reinterpret_cast<float*>(b + o_part) : nullptr;
   c->tile_done = reinterpret_cast<uint32_t*>(b + o_tiles);
+  c->split_part = reinterpret_cast<float*>(b + o_spart);
   c->x_stage = b + o_xs;
   c->out_stage = b + o_os;
   c->x_stage2 = b + o_xs2;
@@ -557,11 +563,15 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   const int64_t out_vec4 = static_cast<int64_t>(T) * d / 4;
   RouterArgs ra{x, ctx->w_router, ctx->b_router, T, d, c.num_experts, ctx->dchunk, ctx->idx, ctx->gate,
                 ctx->row_of, ctx->hist, ctx->sched, ctx->k, c.gate_mode, c.has_shared_expert, ctx->S, ctx->Ex,
-                fuse && gather_a ? static_cast<float*>(out) : nullptr, ctx->tile_done, d / 128};
+                fuse && gather_a ? static_cast<float*>(out) : nullptr, ctx->tile_done, d / 128, ctx->split_part};
   // large bf16 batches stream x into the router through shared memory by TMA (a per-call map of the
   // caller's buffer); small ones read it straight from global memory
   CUtensorMap tm_xr;
-  if (bf16 && T >= kRouterTmaMinT && d % router_tma_cols() == 0 &&
+  if (bf16 && T > kRouterSplitMinT && nchunks <= kRouterSplitMaxChunks && d % (32 * router_split_factor()) == 0) {
+    // 17..64 tokens: the hidden dimension split over several CTAs per chunk (fewer tokens gain
+    // nothing from it: one CTA's loads already take one or two rounds)
+    if (launch_router_split(ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  } else if (bf16 && T >= kRouterTmaMinT && d % router_tma_cols() == 0 &&
       make_tmap(&tm_xr, x, d, static_cast<uint64_t>(T), kRouterChunk)) {
     if (launch_router_tma(tm_xr, ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   } else if (launch_router(c.dtype, ra, nchunks, s) != cudaSuccess) {

@@ -34,6 +34,8 @@ enum : int32_t {
 
 // Routing summary in device memory.  Written by the last CTA of the router kernel, read by
 // every later stage of the same forward.
+constexpr int kRouterSplitMaxChunks = 2;  // the split router serves batches of up to 64 tokens
+
 struct Sched {
   int32_t counts[kMaxE];           // rows routed to each expert
   int32_t offsets[kMaxE + 1];      // first row of each expert segment (segments padded to 128 rows)
@@ -41,6 +43,7 @@ struct Sched {
   uint32_t ticket;                 // router CTAs finished (reset to 0 by the last one)
   uint32_t grid_sync;              // arrivals at the cooperative decode kernel's grid barriers (reset by the router)
   uint32_t tile_ctr[2];            // next tile of the up / down CTA-pair GEMM (reset by the router)
+  uint32_t split_ticket[kRouterSplitMaxChunks];  // split router: CTAs done per chunk (self-resetting)
   int32_t status;                  // device status word (kStatus* bits)
 };
 
@@ -63,6 +66,7 @@ struct RouterArgs {
   float* zero_out;         // fused combine: out [T, d] fp32 rows of this CTA's tokens cleared, else nullptr
   uint32_t* tile_done;     // cooperative decode kernel's per-tile counters, cleared by the last CTA
   int n_tile_done;
+  float* split_part;       // split router: partial logits [chunks][splits][32][EMAX], or nullptr
 };
 
 struct GatherArgs {
@@ -254,6 +258,8 @@ __device__ __forceinline__ int active_experts(const Sched* sc, int E, int* list)
 cudaError_t launch_router(int dtype, const RouterArgs& a, int nchunks, cudaStream_t s);
 cudaError_t launch_router_tma(const CUtensorMap& tmx, const RouterArgs& a, int nchunks, cudaStream_t s);
 int router_tma_cols();  // the TMA-staged router needs d to be a multiple of this
+cudaError_t launch_router_split(const RouterArgs& a, int nchunks, cudaStream_t s);
+int router_split_factor();  // CTAs per chunk of the split router (d must be a multiple of 32 x this)
 cudaError_t launch_gather(int dtype, const GatherArgs& a, cudaStream_t s);
 cudaError_t launch_combine(int out_dtype, const CombineArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_tc_gemm(int epi, bool gather_a, const CUtensorMap& tmA, const CUtensorMap& tmB,

@@ -133,7 +133,8 @@ __device__ void scan_offsets(const RouterArgs& a, int nchunks) {
 // After the chunk's routing is in s_idx (a __syncthreads() ago): in-chunk ranks, the chunk's expert
 // histogram, and -- in the CTA that finishes last -- the scan of all histograms.  S slots per token
 // (k routed experts, then the shared expert when present); a token names each expert at most once.
-__device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[kMaxSlots], int valid, int chunk_t0) {
+__device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[kMaxSlots], int valid, int chunk_t0,
+                             int chunk = blockIdx.x, int nchunks = gridDim.x) {
   __shared__ int s_last;
   const int Ex = a.Ex, S = a.S;
   if (threadIdx.x < S * kRouterChunk) {
@@ -151,12 +152,12 @@ __device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[kMaxSlots],
     int c = 0;
     for (int u = 0; u < valid; ++u)
       for (int q = 0; q < S; ++q) c += (s_idx[u][q] == (int)threadIdx.x);
-    if (gridDim.x > 1)
-      a.hist[(size_t)blockIdx.x * Ex + threadIdx.x] = c;
+    if (nchunks > 1)
+      a.hist[(size_t)chunk * Ex + threadIdx.x] = c;
     else
       s_cnt[threadIdx.x] = c;
   }
-  if (gridDim.x == 1) {
+  if (nchunks == 1) {
     // one chunk (T <= 32, decode-sized batches): no other CTA to wait for, so the summary comes
     // straight from this CTA's counts; the chunk's first row of each expert is the expert's offset
     __syncthreads();
@@ -184,11 +185,11 @@ __device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[kMaxSlots],
   }
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(&a.sched->ticket, 1u) == gridDim.x - 1);
+  if (threadIdx.x == 0) s_last = (atomicAdd(&a.sched->ticket, 1u) == static_cast<unsigned>(nchunks) - 1u);
   __syncthreads();
   if (s_last) {
     __threadfence();
-    scan_offsets(a, gridDim.x);
+    scan_offsets(a, nchunks);
   }
 }
 
@@ -507,6 +508,129 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_top2_mma_kernel(Rout
   finish_chunk(a, s_idx, valid, chunk_t0);
 }
 
+// Small batches (one or two 32-token chunks, decode): the hidden dimension is split over kRsSplit
+// CTAs per chunk, so every warp's fragment loads fit in one round (a single CTA would need four
+// dependent rounds of HBM loads).  Each CTA sums its warps' slices in order and stores its partial
+// logits; the CTA that finishes a chunk's split last (a per-chunk ticket, reset by that CTA) sums the
+// kRsSplit partials in split order -- deterministic -- and does the top-k and the histogram.
+constexpr int kRsSplit = 8;
+
+template <int NT>
+__global__ void __launch_bounds__(kRouterThreads, 2) router_split_kernel(RouterArgs a) {
+  constexpr int NW = kRouterThreads / 32;
+  constexpr int EMAX = 8 * NT;
+  __shared__ float s_part[NW][16][EMAX];
+  __shared__ int s_idx[kRouterChunk][kMaxSlots];
+  __shared__ int s_lastsplit;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x / kRsSplit, split = blockIdx.x % kRsSplit;
+  const int nchunks = gridDim.x / kRsSplit;
+  const int chunk_t0 = chunk * kRouterChunk;
+  const int T = a.T, d = a.d, E = a.E;
+  const int valid = min(kRouterChunk, T - chunk_t0);
+  const int H = valid > 16 ? 2 : 1;
+  const int S = NW / H;
+  const int h = warp % H, sl = warp / H;
+  const int g = lane >> 2, q = lane & 3;
+  const int r0 = chunk_t0 + 16 * h;
+  const bool v0 = r0 + g < T, v1 = r0 + g + 8 < T;
+  const uint4* x0 = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) + (size_t)(v0 ? r0 + g : 0) * d);
+  const uint4* x1 =
+      reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) + (size_t)(v1 ? r0 + g + 8 : 0) * d);
+  const uint4* wr[NT];
+  bool wv[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    wv[nt] = nt * 8 + g < E;
+    wr[nt] = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.w_router) +
+                                            (size_t)(wv[nt] ? nt * 8 + g : 0) * d);
+  }
+  // this CTA's 32-column blocks, then this warp's share of them
+  const int nblk = d / 32;
+  const int cb0 = (nblk * split) / kRsSplit, cb1 = (nblk * (split + 1)) / kRsSplit;
+  const int kb0 = cb0 + ((cb1 - cb0) * sl) / S, kb1 = cb0 + ((cb1 - cb0) * (sl + 1)) / S;
+  pdl_trigger();
+  pdl_wait();  // x may come from the previous kernel; the workspace from the previous forward
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+  constexpr int UNR = 8;
+  for (int kb = kb0; kb < kb1; kb += UNR) {
+    uint4 A0[UNR], A1[UNR], B[UNR][NT];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int vi = 4 * (kb + u) + q;
+      const bool in = kb + u < kb1;
+      A0[u] = (in && v0) ? __ldg(x0 + vi) : make_uint4(0u, 0u, 0u, 0u);
+      A1[u] = (in && v1) ? __ldg(x1 + vi) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) B[u][nt] = (in && wv[nt]) ? __ldg(wr[nt] + vi) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      if (kb + u < kb1) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          asm volatile(
+              "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+              "{%0,%1,%2,%3};"
+              : "+f"(acc[nt][0]), "+f"(acc[nt][1]), "+f"(acc[nt][2]), "+f"(acc[nt][3])
+              : "r"(A0[u].x), "r"(A1[u].x), "r"(A0[u].y), "r"(A1[u].y), "r"(B[u][nt].x), "r"(B[u][nt].y));
+          asm volatile(
+              "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+              "{%0,%1,%2,%3};"
+              : "+f"(acc[nt][0]), "+f"(acc[nt][1]), "+f"(acc[nt][2]), "+f"(acc[nt][3])
+              : "r"(A0[u].z), "r"(A1[u].z), "r"(A0[u].w), "r"(A1[u].w), "r"(B[u][nt].z), "r"(B[u][nt].w));
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    s_part[warp][g][nt * 8 + 2 * q] = acc[nt][0];
+    s_part[warp][g][nt * 8 + 2 * q + 1] = acc[nt][1];
+    s_part[warp][g + 8][nt * 8 + 2 * q] = acc[nt][2];
+    s_part[warp][g + 8][nt * 8 + 2 * q + 1] = acc[nt][3];
+  }
+  __syncthreads();
+  // this split's partial logits of the chunk's 32 rows, warps' slices summed in order
+  float* part = a.split_part + ((size_t)chunk * kRsSplit + split) * kRouterChunk * EMAX;
+  for (int i = threadIdx.x; i < kRouterChunk * EMAX; i += blockDim.x) {
+    const int r = i / EMAX, e = i - r * EMAX, hh = r / 16, rr = r - 16 * hh;
+    float v = 0.f;
+    if (hh < H) {
+      v = s_part[hh][rr][e];
+      for (int w = 1; w < S; ++w) v += s_part[hh + w * H][rr][e];
+    }
+    part[i] = v;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned before = atomicAdd(&a.sched->split_ticket[chunk], 1u);
+    s_lastsplit = before == kRsSplit - 1;
+    if (s_lastsplit) a.sched->split_ticket[chunk] = 0;  // ready for the next forward
+  }
+  __syncthreads();
+  if (!s_lastsplit) return;
+  __threadfence();
+  if (threadIdx.x < kRouterChunk) {
+    const int t = chunk_t0 + threadIdx.x;
+    const float* base = a.split_part + (size_t)chunk * kRsSplit * kRouterChunk * EMAX + threadIdx.x * EMAX;
+    float L[EMAX];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+      float v = __ldcg(base + e);
+      for (int sp = 1; sp < kRsSplit; ++sp) v += __ldcg(base + (size_t)sp * kRouterChunk * EMAX + e);
+      L[e] = v + ((a.b_router != nullptr && e < E) ? a.b_router[e] : 0.f);
+    }
+    topk_store<EMAX>(a, L, t, s_idx[threadIdx.x]);
+  }
+  __syncthreads();
+  finish_chunk(a, s_idx, valid, chunk_t0, chunk, nchunks);
+}
+
 // Large batches: the same logits GEMM with x streamed through shared memory by TMA.  The CTA's 32
 // token rows arrive in stages of 512 columns (eight 64-column boxes, 128-byte swizzle: 1 KB of
 // every row at a time, which DRAM serves better than shorter pieces) in a kRtStages-deep ring, so
@@ -732,6 +856,14 @@ cudaError_t launch_router_tma(const CUtensorMap& tmx, const RouterArgs& a, int n
   if (a.E <= 8) return pdl_launch(router_tma_kernel<1>, dim3(nchunks), dim3(kRouterThreads), kRtSmem, s, tmx, a);
   return pdl_launch(router_tma_kernel<2>, dim3(nchunks), dim3(kRouterThreads), kRtSmem, s, tmx, a);
 }
+
+// bf16, at most kRouterSplitMaxChunks chunks, d a multiple of 32 * kRsSplit; a.split_part holds
+// [nchunks][kRsSplit][32][EMAX] floats
+cudaError_t launch_router_split(const RouterArgs& a, int nchunks, cudaStream_t s) {
+  if (a.E <= 8) return pdl_launch(router_split_kernel<1>, dim3(nchunks * kRsSplit), dim3(kRouterThreads), 0, s, a);
+  return pdl_launch(router_split_kernel<2>, dim3(nchunks * kRsSplit), dim3(kRouterThreads), 0, s, a);
+}
+int router_split_factor() { return kRsSplit; }
 
 cudaError_t launch_router(int dtype, const RouterArgs& a, int nchunks, cudaStream_t s) {
   if (dtype == 0) {
