@@ -38,6 +38,7 @@ constexpr int PNUM_THREADS_ZERO = 192 + 32 * kZeroWarps;  // + the warps clearin
 constexpr int PNUM_THREADS_GA = 192 + 32 * (kGatherWarps + kForwarders);  // + A gather and forwarder warps
 constexpr uint32_t PTMEM_COLS = 512;
 constexpr int PTQ = 4;  // tile-id queue depth (dynamic tile order)
+constexpr int kPublishAt = 4;  // stage of a tile at which the leader hands out the next tile's index
 // full, empty, tmem_full[2], tmem_empty[2], drain, gfull, tile queue full / empty
 constexpr int PNUM_BARS = 3 * PSTAGES + 5 + 2 * PTQ;
 constexpr int PSMEM_BYTES = 1024 + PSTAGES * PSTAGE_BYTES + PNUM_BARS * 8 + 16 + 4 * (4 * kMaxE + 4 + PTQ);
@@ -230,8 +231,10 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
             stage = 0;
             phase ^= 1u;
           }
-          if (DYN && leader && kb == 0) {  // the next tile, while this tile's first stage loads
-            p_next = fetch();
+          // the next tile: its index requested with this tile's first stage, handed to the pair a few
+          // stages later (the atomic's latency and the cluster-scope release then overlap the copies)
+          if (DYN && leader && kb == 0) p_next = fetch();
+          if (DYN && leader && kb == (num_kb > kPublishAt ? kPublishAt : num_kb - 1)) {
             if (!publish(p_next)) {
               ok = false;
               break;
