@@ -434,43 +434,61 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
   if (!*s_abort) {
     const int f = a.f, f4 = f / 4;
     const size_t rows_total = static_cast<size_t>(E) * a.n_up;
-    for (int w = gtid; w < T * Sl * f4; w += gstride) {
-      const int pair = w / f4, c = (w - pair * f4) * 4;
-      const int t = pair / Sl;
-      const int e = a.idx[pair];
-      float hv[4];
-      if (a.swiglu) {
-        const size_t grow = static_cast<size_t>(e) * a.n_up + 256 * (c / 128) + (c % 128);
-        float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
-        for (int s = 0; s < PU.S; ++s) {
-          const float* P = a.partial + (static_cast<size_t>(s) * n_pad + t) * rows_total;
-          const float4 pg = __ldcg(reinterpret_cast<const float4*>(P + grow));
-          const float4 pu = __ldcg(reinterpret_cast<const float4*>(P + grow + 128));
-          g.x += pg.x; g.y += pg.y; g.z += pg.z; g.w += pg.w;
-          u.x += pu.x; u.y += pu.y; u.z += pu.z; u.w += pu.w;
-        }
-        hv[0] = silu_fast(g.x) * u.x;
-        hv[1] = silu_fast(g.y) * u.y;
-        hv[2] = silu_fast(g.z) * u.z;
-        hv[3] = silu_fast(g.w) * u.w;
-      } else {
-        const size_t grow = static_cast<size_t>(e) * a.n_up + c;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < PU.S; ++s) {
-          const float4 p = __ldcg(reinterpret_cast<const float4*>(a.partial + (static_cast<size_t>(s) * n_pad + t) *
-                                                                                  rows_total + grow));
-          v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
-        }
-        const float* b = a.b1 + static_cast<size_t>(e) * f + c;
-        hv[0] = fmaxf(v.x + b[0], 0.f);
-        hv[1] = fmaxf(v.y + b[1], 0.f);
-        hv[2] = fmaxf(v.z + b[2], 0.f);
-        hv[3] = fmaxf(v.w + b[3], 0.f);
+    // kAU work units per thread and round: their partial-sum loads all in flight before any is used
+    constexpr int kAU = 4;
+    const int n_units = T * Sl * f4;
+    for (int w0 = gtid; w0 < n_units; w0 += kAU * gstride) {
+      int ue[kAU], ut[kAU], uc[kAU];
+      float4 g[kAU], u[kAU];
+#pragma unroll
+      for (int j = 0; j < kAU; ++j) {
+        const int w = w0 + j * gstride;
+        const int pair = w < n_units ? w / f4 : 0;
+        uc[j] = (w - pair * f4) * 4;
+        ut[j] = pair / Sl;
+        ue[j] = w < n_units ? a.idx[pair] : -1;
+        g[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        u[j] = g[j];
       }
-      uint2 o;
-      o.x = pack_bf16(hv[0], hv[1]);
-      o.y = pack_bf16(hv[2], hv[3]);
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.h) + (static_cast<size_t>(e) * n_pad + t) * f + c) = o;
+      for (int s = 0; s < PU.S; ++s) {
+#pragma unroll
+        for (int j = 0; j < kAU; ++j) {
+          if (ue[j] < 0) continue;
+          const float* P = a.partial + (static_cast<size_t>(s) * n_pad + ut[j]) * rows_total;
+          if (a.swiglu) {
+            const size_t grow = static_cast<size_t>(ue[j]) * a.n_up + 256 * (uc[j] / 128) + (uc[j] % 128);
+            const float4 pg = __ldcg(reinterpret_cast<const float4*>(P + grow));
+            const float4 pu = __ldcg(reinterpret_cast<const float4*>(P + grow + 128));
+            g[j].x += pg.x; g[j].y += pg.y; g[j].z += pg.z; g[j].w += pg.w;
+            u[j].x += pu.x; u[j].y += pu.y; u[j].z += pu.z; u[j].w += pu.w;
+          } else {
+            const float4 p = __ldcg(reinterpret_cast<const float4*>(P + static_cast<size_t>(ue[j]) * a.n_up + uc[j]));
+            g[j].x += p.x; g[j].y += p.y; g[j].z += p.z; g[j].w += p.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kAU; ++j) {
+        if (ue[j] < 0) continue;
+        const int e = ue[j], t = ut[j], c = uc[j];
+        float hv[4];
+        if (a.swiglu) {
+          hv[0] = silu_fast(g[j].x) * u[j].x;
+          hv[1] = silu_fast(g[j].y) * u[j].y;
+          hv[2] = silu_fast(g[j].z) * u[j].z;
+          hv[3] = silu_fast(g[j].w) * u[j].w;
+        } else {
+          const float* b = a.b1 + static_cast<size_t>(e) * f + c;
+          hv[0] = fmaxf(g[j].x + b[0], 0.f);
+          hv[1] = fmaxf(g[j].y + b[1], 0.f);
+          hv[2] = fmaxf(g[j].z + b[2], 0.f);
+          hv[3] = fmaxf(g[j].w + b[3], 0.f);
+        }
+        uint2 o;
+        o.x = pack_bf16(hv[0], hv[1]);
+        o.y = pack_bf16(hv[2], hv[3]);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.h) + (static_cast<size_t>(e) * n_pad + t) * f + c) = o;
+      }
     }
     fence_proxy_async_global();  // H is read next by TMA (async proxy)
   }
