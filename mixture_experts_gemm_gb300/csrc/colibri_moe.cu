@@ -104,7 +104,7 @@ constexpr int kNumStages = 5;  // router, gather, up GEMM, down GEMM, combine
 constexpr int kTileCombineMaxT = 4;
 constexpr int kRouterTmaMinT = 1024;  // batches from this size use the TMA-staged router
 constexpr int kRouterSplitMinT = 16;   // batches above this size (and up to 64) use the split router
-// (Mixtral-shaped router stage, GB300: T=32 23.2 -> 16.9 us split; T=16 equal; T=1 9.1 -> 10.5 us)
+// (GB300: Mixtral-shaped router stage at T=32 23.2 -> 16.9 us split; T=16 equal; T=1 9.1 -> 10.5 us)
 
 struct DeviceGuard {
   int prev = -1;
@@ -568,8 +568,8 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   // caller's buffer); small ones read it straight from global memory
   CUtensorMap tm_xr;
   if (bf16 && T > kRouterSplitMinT && nchunks <= kRouterSplitMaxChunks && d % (32 * router_split_factor()) == 0) {
-    // 17..64 tokens: the hidden dimension split over several CTAs per chunk (fewer tokens gain
-    // nothing from it: one CTA's loads already take one or two rounds)
+    // 17..1024 tokens: the hidden dimension split over several CTAs per chunk (fewer tokens gain
+    // nothing from it: one CTA's loads already take one or two rounds; more fill the GPU anyway)
     if (launch_router_split(ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   } else if (bf16 && T >= kRouterTmaMinT && d % router_tma_cols() == 0 &&
       make_tmap(&tm_xr, x, d, static_cast<uint64_t>(T), kRouterChunk)) {

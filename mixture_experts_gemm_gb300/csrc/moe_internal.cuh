@@ -34,7 +34,7 @@ enum : int32_t {
 
 // Routing summary in device memory.  Written by the last CTA of the router kernel, read by
 // every later stage of the same forward.
-constexpr int kRouterSplitMaxChunks = 2;  // the split router serves batches of up to 64 tokens
+constexpr int kRouterSplitMaxChunks = 32;  // the split router serves batches of up to 1024 tokens
 
 struct Sched {
   int32_t counts[kMaxE];           // rows routed to each expert

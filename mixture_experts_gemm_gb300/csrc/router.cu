@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_top2_mma_kernel(Rout
   finish_chunk(a, s_idx, valid, chunk_t0);
 }
 
-// Small batches (one or two 32-token chunks, decode): the hidden dimension is split over kRsSplit
+// Small and medium batches (up to 32 chunks of 32 tokens): the hidden dimension is split over kRsSplit
 // CTAs per chunk, so every warp's fragment loads fit in one round (a single CTA would need four
 // dependent rounds of HBM loads).  Each CTA sums its warps' slices in order and stores its partial
 // logits; the CTA that finishes a chunk's split last (a per-chunk ticket, reset by that CTA) sums the
@@ -552,6 +552,11 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_split_kernel(RouterA
   const int kb0 = cb0 + ((cb1 - cb0) * sl) / S, kb1 = cb0 + ((cb1 - cb0) * (sl + 1)) / S;
   pdl_trigger();
   pdl_wait();  // x may come from the previous kernel; the workspace from the previous forward
+  {
+    // clearing out (when asked): this split's share of the chunk's rows
+    const int r0s = (kRouterChunk * split) / kRsSplit, r1s = min((kRouterChunk * (split + 1)) / kRsSplit, valid);
+    if (r1s > r0s) zero_out_rows(a, chunk_t0 + r0s, r1s - r0s);
+  }
   float acc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
