@@ -15,7 +15,9 @@
 // A pair computes two 128-row M tiles of one expert that share the weight tile; when an expert has
 // an odd number of M tiles, the second CTA of its last pair computes rows past the expert's segment
 // (read as they are or as zeros past the buffer) and stores nothing.  Waits are bounded as in the
-// single-CTA kernel; TMEM is allocated and freed collectively by one warp of each CTA.
+// single-CTA kernel; TMEM is allocated and freed collectively by one warp of each CTA.  Tiles are
+// handed out in index order at run time (see "Tile order" below).  The up projection can carry two
+// more warps that clear the fused combine's output while the mainloop runs.
 //
 // Gathered A (GA, up projection): the A rows come straight from the token rows x through
 // token_of_row (gather_a.cuh); extra warps of each CTA copy them with cp.async and a forwarder

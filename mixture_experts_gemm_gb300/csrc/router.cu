@@ -7,10 +7,15 @@
 // Selection is made on the logits (softmax is monotone); ties go to the lower expert index; the
 // gates are the softmax over the selected pair, g_a = 1 / (1 + exp(L_b - L_a)), g_b = 1 - g_a.
 //
-// The kernel is HBM-bound on reading x (2*T*E*d FLOP against T*d*sizeof(x) bytes): each warp
-// streams 4 token rows with 16-byte loads while W_r sits in shared memory, so every W_r value read
-// from shared memory feeds 4 tokens.  Per-chunk histograms make the dispatch deterministic: atomics
-// only count finished CTAs, and every row index comes from a scan in token order.
+// The work is bound by reading x (2*T*E*d FLOP against T*d*sizeof(x) bytes).  One CTA per 32-token
+// chunk; four kernels share the top-k, histogram and scan code below:
+//   router_top2_kernel      fp32 (and bf16 with d not a multiple of 32): FMA dot products, W_r
+//                           staged in shared memory, each warp streaming 4 token rows;
+//   router_top2_mma_kernel  bf16: mma.sync logits with fragments loaded straight from x;
+//   router_split_kernel     bf16, 17..1024 tokens: d split over 8 CTAs per chunk;
+//   router_tma_kernel       bf16, >= 1024 tokens: x staged through shared memory by TMA.
+// Per-chunk histograms make the dispatch deterministic: atomics only count finished CTAs, and every
+// row index comes from a scan in token order.
 #include "moe_internal.cuh"
 
 namespace colibri {
