@@ -297,6 +297,26 @@ def test_gathered_a_rows_equal_copied_xp(gemm, monkeypatch):
         assert np.array_equal(Hg, Hc), shape.name
 
 
+def test_in_order_tile_handout_equals_static_order(monkeypatch):
+    """The CTA-pair GEMM hands tiles out in index order at run time (a shared counter, a per-pair id
+    queue); every tile is computed the same way in either order, so outputs and H agree bit for bit
+    with the static round-robin order -- also when there are fewer tiles than pairs."""
+    for shape in (testgen.LayerShape("order", 3000, 512, 1024, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True),
+                  testgen.LayerShape("order-few", 130, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")):
+        li = testgen.make_inputs(shape)
+        monkeypatch.delenv("COLIBRI_MOE_TILE_ORDER", raising=False)
+        layer_d, out_d, r, _, _ = _full_check(li)
+        monkeypatch.setenv("COLIBRI_MOE_TILE_ORDER", "static")
+        layer_s, out_s, _, _, _ = _full_check(li)
+        assert np.array_equal(out_d, out_s), shape.name
+        rows = np.sort(r["row_of"].ravel())
+        assert np.array_equal(layer_d.debug_tensor(1).float().cpu().numpy()[rows],
+                              layer_s.debug_tensor(1).float().cpu().numpy()[rows]), shape.name
+        # a second forward on the same context (the router clears the tile counters)
+        out_d2, _ = run(layer_d, x_device(li))
+        assert np.array_equal(out_d, out_d2), shape.name
+
+
 @pytest.mark.parametrize("T", [24, 900])
 def test_forward_replays_from_a_cuda_graph(T):
     """forward allocates nothing and never synchronises, so it can be captured into a CUDA graph; the
