@@ -21,9 +21,8 @@
 // joins the element-wise phase A.  The weight tiles of phase D are requested before the barriers
 // that precede it (they do not depend on phase A), so the HBM stream continues across them.
 //
-// Barriers: one arrival per CTA on a counter in the routing summary (cleared by the router), the
-// arriving thread fences (gpu scope) first and spins with acquire loads, bounded by the wait
-// timeout; H is written through the generic proxy and read by TMA, so its writers fence the proxy
+// Barriers: one arrival per CTA on a counter in the routing summary (cleared by the router), a
+// gpu-scope release, then a spin on acquire loads bounded by the wait timeout; H is written through the generic proxy and read by TMA, so its writers fence the proxy
 // before arriving.  Splits are summed in order: results are deterministic.
 #include "tcgen05_ptx.cuh"
 
@@ -68,13 +67,14 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
   return r != 0;
 }
 
-// Grid-wide barrier number `n` (1, 2, ...): every CTA arrives once; bounded wait.
+// Grid-wide barrier number `n` (1, 2, ...): every CTA arrives once; bounded wait.  The arrival is a
+// gpu-scope release (it covers the CTA's writes, ordered before it by the CTA barrier) and the spin an
+// acquire; the closing CTA barrier orders every thread's later reads after that acquire.
 __device__ __forceinline__ void grid_barrier(Sched* sc, uint32_t n, volatile int* s_abort, uint64_t timeout_ns,
                                              int32_t* status) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(&sc->grid_sync, 1u);
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&sc->grid_sync) : "memory");
     const uint32_t target = n * gridDim.x;
     if (ld_acquire_gpu(&sc->grid_sync) < target) {
       const uint64_t t0 = globaltimer_ns();
@@ -86,7 +86,6 @@ __device__ __forceinline__ void grid_barrier(Sched* sc, uint32_t n, volatile int
         }
       }
     }
-    __threadfence();
   }
   __syncthreads();
 }
