@@ -79,6 +79,7 @@ struct colibri_moe {
   CUtensorMap tm_xp{}, tm_h{}, tm_w13{}, tm_w2{};
   // decode path (T <= decode_max_t): 128-row weight boxes, token boxes of 16/32/48/64 rows
   CUtensorMap tm_w13_dec{}, tm_w2_dec{}, tm_xp_dec[4]{}, tm_h_dec[4]{};
+  CUtensorMap tm_w13_half{};  // 64-row boxes: the cooperative decode kernel's gate/up pairs
   float* partial = nullptr;  // decode partial sums [splits][n_pad][E * rows]
   uint32_t* tile_done = nullptr;  // cooperative decode kernel: items done per down-projection tile
   float* split_part = nullptr;    // split router: partial logits of small batches
@@ -89,6 +90,7 @@ struct colibri_moe {
   bool dynamic_tiles = true; // CTA-pair GEMMs take tiles in index order from a shared counter
   int pair_ctas = 0;         // co-resident CTAs of the pair kernel (persistent grid size)
   bool decode_fused = true;  // decode batches: one cooperative kernel after the router
+  bool direct_h = true;      // ... whose unsplit up projection writes H in its epilogue
   int fused_ctas = 0;        // its grid (one CTA per SM)
   int32_t last_T = -1;
   int32_t last_kernels = 0;  // kernels enqueued by the last forward
@@ -213,6 +215,13 @@ bool env_pair_gemm() {
 
 // Decode-sized batches run the cooperative fused kernel unless COLIBRI_MOE_DECODE_FUSED=0 selects
 // the separate kernels (dispatch, GEMM, activation, GEMM, combine).
+// The cooperative decode kernel's up projection, when unsplit, writes H in its epilogue (no
+// activation phase, one grid barrier fewer) unless COLIBRI_MOE_DECODE_DIRECT_H=0.
+bool env_direct_h() {
+  const char* s = std::getenv("COLIBRI_MOE_DECODE_DIRECT_H");
+  return !(s && s[0] == '0');
+}
+
 bool env_decode_fused() {
   const char* s = std::getenv("COLIBRI_MOE_DECODE_FUSED");
   return !(s && s[0] == '0');
@@ -406,6 +415,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
     if (c->pair_ctas < 2) c->pair_gemm = false;
   }
   c->decode_fused = env_decode_fused() && c->decode_max_t > 0;
+  c->direct_h = env_direct_h();
   if (c->decode_fused) {
     const int co = decode_fused_max_ctas(sms);
     c->fused_ctas = co < sms ? co : sms;
@@ -524,7 +534,8 @@ int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_weights_t* w,
     if (!make_tmap(&ctx->tm_w13, ctx->w13, d, static_cast<uint64_t>(Ex) * ctx->n_up, bn) ||
         !make_tmap(&ctx->tm_w2, ctx->w2, f, static_cast<uint64_t>(Ex) * d, bn) ||
         !make_tmap(&ctx->tm_w13_dec, ctx->w13, d, static_cast<uint64_t>(Ex) * ctx->n_up, kRowTile) ||
-        !make_tmap(&ctx->tm_w2_dec, ctx->w2, f, static_cast<uint64_t>(Ex) * d, kRowTile))
+        !make_tmap(&ctx->tm_w2_dec, ctx->w2, f, static_cast<uint64_t>(Ex) * d, kRowTile) ||
+        !make_tmap(&ctx->tm_w13_half, ctx->w13, d, static_cast<uint64_t>(Ex) * ctx->n_up, kRowTile / 2))
       return COLIBRI_ERR_CUDA;
   }
   ctx->loaded = true;
@@ -589,8 +600,8 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     FusedDecodeArgs fa{ctx->sched, E, d, f, ctx->n_up, T, n_pad, ctx->S, ctx->idx, ctx->gate, ctx->row_of,
                        ctx->tok_of_row, ctx->hist, ctx->rows_alloc, ctx->partial, ctx->b1, ctx->b2, ctx->h, out,
                        c.out_dtype == COLIBRI_DTYPE_BF16 ? 1 : 0, swiglu ? 1 : 0, ctx->timeout_ns,
-                       &ctx->sched->status, ctx->tile_done, T <= kTileCombineMaxT ? 1 : 0};
-    if (launch_decode_fused(ctx->tm_w13_dec, tm_xt, ctx->tm_w2_dec, ctx->tm_h_dec[n_pad / 16 - 1], fa,
+                       &ctx->sched->status, ctx->tile_done, T <= kTileCombineMaxT ? 1 : 0, ctx->direct_h ? 1 : 0};
+    if (launch_decode_fused(ctx->tm_w13_dec, tm_xt, ctx->tm_w2_dec, ctx->tm_h_dec[n_pad / 16 - 1], ctx->tm_w13_half, fa,
                             ctx->fused_ctas, s) != cudaSuccess)
       return COLIBRI_ERR_CUDA;
     mark(3);

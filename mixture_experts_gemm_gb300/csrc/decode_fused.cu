@@ -7,6 +7,10 @@
 //
 //   phase U  P[s][t][e rows] = sum over K split s of W13_e[rows, k] x[t, k]   (tcgen05, TMEM)
 //   phase A  H[e * n_pad + t, :] = act(sum_s P[s][t][e rows])  for every routed (token, expert)
+//            -- or, when phase U runs unsplit (S = 1, the usual case), phase U's epilogue writes H
+//            itself and phase A and its barrier drop out: its weight tiles are then two 64-row
+//            boxes, the gate rows of 64 hidden units and their up rows, so the warps holding the
+//            up values hand them to the warps holding the gates through shared memory
 //   phase D  P[s][t][e rows] = sum over split s of W2_e[rows, k] H[e * n_pad + t, k]
 //   phase C  out[t, :] = sum over t's slots in order of g * (sum_s P[s][t][e rows] (+ b2)): after a
 //            third barrier, or (tile_combine, the smallest batches) for the 128 columns of a down-
@@ -38,8 +42,11 @@ constexpr int FB_SLOT = kDecodeMaxT * FBK * 2;   // 8 KB token tile slot (n_pad 
 constexpr int FNUM_THREADS = 192;
 constexpr uint32_t FTMEM_COLS = 128;             // two accumulators of up to 64 fp32 columns
 constexpr int FNUM_BARS = 2 * FSTAGES + 5;
+constexpr int FHALF = FBM / 2;                   // hidden units per weight tile with SwiGLU (direct H)
+constexpr int FX_CHUNK = 16;                     // token columns per TMEM load
+constexpr int FX_BYTES = 2 * FX_CHUNK * FHALF * 4;  // up values handed over: two buffers of 16 x 64
 constexpr int FSMEM_BYTES =
-    1024 + FSTAGES * (FA_BYTES + FB_SLOT) + FNUM_BARS * 8 + 16 + 8 * kMaxE + 4 * (2 * kMaxE + 4);
+    1024 + FSTAGES * (FA_BYTES + FB_SLOT) + FX_BYTES + FNUM_BARS * 8 + 16 + 8 * kMaxE + 4 * (2 * kMaxE + 4);
 static_assert(FSMEM_BYTES <= 227 * 1024, "fused decode shared memory");
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
@@ -99,6 +106,8 @@ struct Phase {
   int x_step;   // first token row of expert e's operand = e * x_step
   int MT, KB, S, total;
   float* partial;  // [S][n_pad][E * rows]
+  const CUtensorMap* tmWh;  // direct H: the same weights in 64-row boxes, else nullptr
+  bool direct;              // phase U writes H (S == 1)
 };
 
 __device__ __forceinline__ Phase make_phase(const CUtensorMap* tmW, const CUtensorMap* tmX, int K, int rows, int x_step,
@@ -114,6 +123,8 @@ __device__ __forceinline__ Phase make_phase(const CUtensorMap* tmW, const CUtens
   p.S = decode_splits(n_act * p.MT, p.KB, gridDim.x, s_max);
   p.total = n_act * p.MT * p.S;
   p.partial = partial;
+  p.tmWh = nullptr;
+  p.direct = false;
   return p;
 }
 
@@ -145,12 +156,13 @@ struct Ring {
 __global__ void __launch_bounds__(FNUM_THREADS, 1)
     decode_fused_kernel(const __grid_constant__ CUtensorMap tmW13, const __grid_constant__ CUtensorMap tmX,
                         const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmH,
-                        const FusedDecodeArgs a) {
+                        const __grid_constant__ CUtensorMap tmW13h, const FusedDecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + FSTAGES * FA_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + FSTAGES * FB_SLOT);
+  float* xs = reinterpret_cast<float*>(sB + FSTAGES * FB_SLOT);  // [2][16 tokens][64 units] (direct H)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xs) + FX_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + FNUM_BARS);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   unsigned long long* s_mask = reinterpret_cast<unsigned long long*>(tmem_slot + 4);  // tokens routed to e
@@ -182,6 +194,7 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmW2);
     prefetch_tmap(&tmH);
+    prefetch_tmap(&tmW13h);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), FTMEM_COLS);
@@ -213,7 +226,11 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
   const uint32_t b_bytes = static_cast<uint32_t>(n_pad) * FBK * 2;
   const uint32_t idesc = make_idesc_bf16(FBM, n_pad);
 
-  const Phase PU = make_phase(&tmW13, &tmX, a.d, a.n_up, 0, n_act, kDecodeSplitsUp, a.partial);
+  Phase PU = make_phase(&tmW13, &tmX, a.d, a.n_up, 0, n_act, kDecodeSplitsUp, a.partial);
+  if (a.direct_h && PU.S == 1) {
+    PU.tmWh = &tmW13h;
+    PU.direct = true;
+  }
   const Phase PD = make_phase(&tmW2, &tmH, a.f, a.d, n_pad, n_act, kDecodeSplitsDown, a.partial);
 
   // per-role state, carried from phase U to phase D
@@ -224,6 +241,18 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
   int pre = 0;                       // producer: stages of phase D whose weight tile is in flight
   Ring pre_start;
 
+  // The weight tile of item im at K block kb: one 128-row box, or (direct H with SwiGLU) the gate
+  // rows 256*(mt/2) + 64*(mt%2) + [0, 64) and the up rows 128 further on, in two 64-row boxes.
+  auto load_weights = [&](const Phase& P, const Item& im, uint32_t dst, uint32_t bar, int kb) {
+    if (P.direct) {
+      const int r0 = im.e * P.rows + (a.swiglu ? 2 * FBM * (im.mt >> 1) + FHALF * (im.mt & 1) : FBM * im.mt);
+      const int r1 = r0 + (a.swiglu ? FBM : FHALF);
+      tma_load_2d(dst, P.tmWh, bar, kb * FBK, r0);
+      tma_load_2d(dst + FHALF * FBK * 2, P.tmWh, bar, kb * FBK, r1);
+    } else {
+      tma_load_2d(dst, P.tmW, bar, kb * FBK, im.e * P.rows + im.mt * FBM);
+    }
+  };
   // Producer: weight tile + token tile per stage.  Stages [0, pre) of this phase had their weight
   // tile requested earlier (from pre_start on); only their token tile is issued here.
   auto produce = [&](const Phase& P, int n_pre, Ring start) {
@@ -232,7 +261,6 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
     bool ok = true;
     for (int it = blockIdx.x; ok && it < P.total; it += gridDim.x) {
       const Item im = item_of(P, it, s_act);
-      const int w_row = im.e * P.rows + im.mt * FBM;
       const int x_row = im.e * P.x_step;
       for (int kb = im.kb0; kb < im.kb1; ++kb, ++g) {
         const uint32_t fb = full0 + 8 * cur.stage;
@@ -242,7 +270,7 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(fb, FA_BYTES + b_bytes);
-          tma_load_2d(smem_u32(sA + cur.stage * FA_BYTES), P.tmW, fb, kb * FBK, w_row);
+          load_weights(P, im, smem_u32(sA + cur.stage * FA_BYTES), fb, kb);
         }
         armed |= 1u << cur.stage;
         armed_phase = (armed_phase & ~(1u << cur.stage)) | (cur.phase << cur.stage);
@@ -263,7 +291,6 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
     bool ok = true;
     for (int it = blockIdx.x; ok && pre < FSTAGES && it < P.total; it += gridDim.x) {
       const Item im = item_of(P, it, s_act);
-      const int w_row = im.e * P.rows + im.mt * FBM;
       for (int kb = im.kb0; kb < im.kb1 && pre < FSTAGES; ++kb, ++pre) {
         if (!mbar_wait(empty0 + 8 * ring.stage, ring.phase ^ 1u, s_abort, a.timeout_ns)) {
           ok = false;
@@ -271,7 +298,7 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
         }
         const uint32_t fb = full0 + 8 * ring.stage;
         mbar_arrive_expect_tx(fb, FA_BYTES + b_bytes);
-        tma_load_2d(smem_u32(sA + ring.stage * FA_BYTES), P.tmW, fb, kb * FBK, w_row);
+        load_weights(P, im, smem_u32(sA + ring.stage * FA_BYTES), fb, kb);
         ring.next();
       }
     }
@@ -367,29 +394,65 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
   // tile's last item (every active expert, every split) combines that tile's output columns.
   auto epilogue = [&](const Phase& P, bool combine) {
     const int q = warp & 3;
+    const int wr = q * 32 + lane;  // weight row of the tile
     const size_t rows_total = static_cast<size_t>(E) * P.rows;
+    int xb = 0;
     for (int it = blockIdx.x; it < P.total; it += gridDim.x) {
       const Item im = item_of(P, it, s_act);
       const unsigned long long mask = s_mask[im.e];
       bool ok = mbar_wait(tfull0 + 8 * acc, acc_phase, s_abort, a.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
-      if (combine) ok = epilogue_all(ok);  // the named barriers below need all four warps
+      if (combine || (P.direct && a.swiglu)) ok = epilogue_all(ok);  // named barriers below need all four warps
       if (!ok) {
         if (lane == 0 && !*s_abort) atomicOr(a.status, kStatusTimeoutEpilogue);
         if (lane == 0) *s_abort = 1;
         break;
       }
       tc_fence_after();
-      const size_t row = static_cast<size_t>(im.e) * P.rows + im.mt * FBM + q * 32 + lane;
       const uint32_t tbase =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kDecodeMaxT);
-      float* out = P.partial + static_cast<size_t>(im.sp) * n_pad * rows_total + row;
-      for (int c = 0; c < n_pad; c += 16) {
-        uint32_t v[16];
-        tmem_ld16_sync(tbase + c, v);
+      if (P.direct) {
+        // H rows e * n_pad + t of the routed tokens, written here (phase A is skipped)
+        __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(a.h) + static_cast<size_t>(im.e) * n_pad * a.f;
+        for (int c = 0; c < n_pad; c += FX_CHUNK) {
+          uint32_t v[FX_CHUNK];
+          tmem_ld16_sync(tbase + c, v);
+          if (a.swiglu) {
+            // rows 0-63: gates of hidden units 64*mt + [0, 64); rows 64-127: their up values
+            float* x = xs + xb * (FX_CHUNK * FHALF);
+            if (q >= 2) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if ((mask >> (c + j)) & 1ull) out[static_cast<size_t>(c + j) * rows_total] = __uint_as_float(v[j]);
+              for (int j = 0; j < FX_CHUNK; ++j) x[j * FHALF + wr - FHALF] = __uint_as_float(v[j]);
+            }
+            named_barrier_epilogue();
+            if (q < 2) {
+              const int col = im.mt * FHALF + wr;
+#pragma unroll
+              for (int j = 0; j < FX_CHUNK; ++j)
+                if ((mask >> (c + j)) & 1ull)
+                  hrow[static_cast<size_t>(c + j) * a.f + col] =
+                      __float2bfloat16_rn(silu_fast(__uint_as_float(v[j])) * x[j * FHALF + wr]);
+            }
+            xb ^= 1;
+          } else {
+            const int col = im.mt * FBM + wr;
+            const float b = a.b1[static_cast<size_t>(im.e) * a.f + col];
+#pragma unroll
+            for (int j = 0; j < FX_CHUNK; ++j)
+              if ((mask >> (c + j)) & 1ull)
+                hrow[static_cast<size_t>(c + j) * a.f + col] = __float2bfloat16_rn(fmaxf(__uint_as_float(v[j]) + b, 0.f));
+          }
+        }
+      } else {
+        const size_t row = static_cast<size_t>(im.e) * P.rows + im.mt * FBM + wr;
+        float* out = P.partial + static_cast<size_t>(im.sp) * n_pad * rows_total + row;
+        for (int c = 0; c < n_pad; c += 16) {
+          uint32_t v[16];
+          tmem_ld16_sync(tbase + c, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if ((mask >> (c + j)) & 1ull) out[static_cast<size_t>(c + j) * rows_total] = __uint_as_float(v[j]);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -426,11 +489,13 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
     if (lane == 0) mma(PU);
   } else {
     epilogue(PU, false);
+    if (PU.direct) fence_proxy_async_global();  // H is read next by TMA (async proxy)
   }
-  grid_barrier(a.sched, 1, s_abort, a.timeout_ns, a.status);
+  uint32_t nbar = 0;  // grid barriers passed
+  grid_barrier(a.sched, ++nbar, s_abort, a.timeout_ns, a.status);
 
   // ---------------------------------------------------------------- phase A: H rows of routed pairs
-  if (!*s_abort) {
+  if (!PU.direct && !*s_abort) {
     const int f = a.f, f4 = f / 4;
     const size_t rows_total = static_cast<size_t>(E) * a.n_up;
     // kAU work units per thread and round: their partial-sum loads all in flight before any is used
@@ -491,7 +556,7 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
     }
     fence_proxy_async_global();  // H is read next by TMA (async proxy)
   }
-  grid_barrier(a.sched, 2, s_abort, a.timeout_ns, a.status);
+  if (!PU.direct) grid_barrier(a.sched, ++nbar, s_abort, a.timeout_ns, a.status);
 
   // ---------------------------------------------------------------- phase D (+ combine per tile)
   if (warp == 0) {
@@ -503,7 +568,7 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
   }
   if (!a.tile_combine) {
     // ------------------------------------------------------------ phase C: combine after a barrier
-    grid_barrier(a.sched, 3, s_abort, a.timeout_ns, a.status);
+    grid_barrier(a.sched, ++nbar, s_abort, a.timeout_ns, a.status);
     if (!*s_abort) {
       const int d = a.d, d4 = d / 4;
       const size_t rows_total = static_cast<size_t>(E) * d;
@@ -599,7 +664,8 @@ int decode_fused_max_ctas(int num_sms) {
 }
 
 cudaError_t launch_decode_fused(const CUtensorMap& tmW13, const CUtensorMap& tmX, const CUtensorMap& tmW2,
-                                const CUtensorMap& tmH, const FusedDecodeArgs& a, int grid, cudaStream_t s) {
+                                const CUtensorMap& tmH, const CUtensorMap& tmW13h, const FusedDecodeArgs& a, int grid,
+                                cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(FNUM_THREADS);
@@ -612,7 +678,7 @@ cudaError_t launch_decode_fused(const CUtensorMap& tmW13, const CUtensorMap& tmX
   attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_fused_kernel, tmW13, tmX, tmW2, tmH, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_fused_kernel, tmW13, tmX, tmW2, tmH, tmW13h, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -190,6 +190,7 @@ struct FusedDecodeArgs {
   int32_t* status;
   uint32_t* tile_done;      // [d / 128] items finished per down-projection weight tile (self-resetting)
   int tile_combine;         // 1: combine per tile by its last CTA; 0: after a grid barrier
+  int direct_h;             // 1: an unsplit up projection writes H in its epilogue (no phase A)
 };
 
 // fp32 SIMT grouped GEMM operands (row-major, K contiguous)
@@ -280,7 +281,8 @@ cudaError_t launch_decode_act(bool swiglu, const DecodeActArgs& a, cudaStream_t 
 cudaError_t prepare_decode_fused();
 int decode_fused_max_ctas(int num_sms);
 cudaError_t launch_decode_fused(const CUtensorMap& tmW13, const CUtensorMap& tmX, const CUtensorMap& tmW2,
-                                const CUtensorMap& tmH, const FusedDecodeArgs& a, int grid, cudaStream_t s);
+                                const CUtensorMap& tmH, const CUtensorMap& tmW13h, const FusedDecodeArgs& a, int grid,
+                                cudaStream_t s);
 cudaError_t launch_decode_combine(int out_dtype, const DecodeCombineArgs& a, cudaStream_t s);
 int tc_gemm_block_n();
 int tc_gemm_threads();

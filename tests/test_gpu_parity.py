@@ -172,6 +172,58 @@ def test_cooperative_decode_kernel_equals_separate_kernels(case, monkeypatch):
         assert np.array_equal(r_f[k], r_s[k]), k
 
 
+def _decode_splits(items0, kblocks, grid, s_max):
+    """The cooperative decode kernel's K-split rule (smallest split count filling >= 90 % of its waves)."""
+    best, best_num, best_den = 1, -1, 1
+    for S in range(1, min(s_max, kblocks) + 1):
+        items = items0 * S
+        waves = -(-items // grid)
+        if items >= grid and items * 10 >= waves * grid * 9:
+            return S
+        if items * best_den > best_num * waves * grid:
+            best, best_num, best_den = S, items, waves * grid
+    return best
+
+
+@pytest.mark.parametrize("case", ["swiglu-t20", "swiglu-t3", "relu-t20", "k4-shared-t5"])
+def test_cooperative_decode_kernel_writes_h_in_the_up_epilogue(case, monkeypatch):
+    """When the up projection runs unsplit, its epilogue writes H itself (gate rows of 64 hidden units
+    and their up rows in one 128-row tile, the up values handed over through shared memory) and the
+    activation phase and one grid barrier drop out.  H and the output equal the activation-phase
+    form bit for bit, and the separate kernels'.  The shapes give one full wave of unsplit items."""
+    E, k, shared = 4, 2, False
+    if case.startswith("relu"):
+        act, f = testgen.ACT_RELU_BIAS, 4864
+    else:
+        act, f = testgen.ACT_SWIGLU, 2432
+    if case.startswith("k4"):
+        E, k, shared, f = 8, 4, True, 1024
+    T = int(case.rsplit("t", 1)[1])
+    shape = testgen.LayerShape(f"direct-{case}", T, 256, f, E, act, "bf16", top_k=k, shared_expert=shared)
+    li = testgen.make_inputs(shape)
+    layer_d, out_d, r, _, _ = _full_check(li)
+    assert layer_d.last_kernel_count() == 2
+    n_act = int((np.asarray(r["counts"]) > 0).sum())
+    n_up = 2 * f if act == testgen.ACT_SWIGLU else f
+    grid = torch.cuda.get_device_properties(0).multi_processor_count
+    assert _decode_splits(n_act * n_up // 128, 256 // 64, grid, 2) == 1, "the case must run the up GEMM unsplit"
+    monkeypatch.setenv("COLIBRI_MOE_DECODE_DIRECT_H", "0")
+    layer_a, out_a, _, _, _ = _full_check(li)
+    assert np.array_equal(out_d, out_a)
+    rows = []
+    for e in range(len(r["counts"])):
+        rows += [e * ((T + 15) // 16 * 16) + t for t in range(T) if (r["idx"][t] == e).any()]
+    if shared:
+        Es = len(r["counts"]) - 1
+        rows += [Es * ((T + 15) // 16 * 16) + t for t in range(T)]
+    Hd = layer_d.debug_tensor(1).float().cpu().numpy()[rows]
+    Ha = layer_a.debug_tensor(1).float().cpu().numpy()[rows]
+    assert np.array_equal(Hd, Ha)
+    monkeypatch.setenv("COLIBRI_MOE_DECODE_FUSED", "0")
+    _, out_s, _, _, _ = _full_check(li)
+    assert np.array_equal(out_d, out_s)
+
+
 def test_decode_path_relu_bias():
     shape = testgen.LayerShape("decode-relu", 20, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")
     li = testgen.make_inputs(shape)
