@@ -186,6 +186,17 @@ COLIBRI_API int colibri_moe_set_stage_events(colibri_moe_t* ctx, void* const* ev
  * gives up or an index check fails: *status = 0 means none did. */
 COLIBRI_API int colibri_moe_device_status(colibri_moe_t* ctx, int32_t* status);
 
+/* Failure-detection probe (a diagnostic with no counterpart in the articles).  Every wait inside
+ * the layer's kernels is bounded: when one gives up, the kernel sets a bit of the device status
+ * word, stops, drains its own copies and returns, and colibri_moe_device_status reports the bit.
+ * This call enqueues on `stream` (a cudaStream_t, NULL = legacy default stream) one small kernel
+ * that runs the same bounded wait on a barrier nothing arrives on, for timeout_us microseconds
+ * (1 .. 1000000), then sets COLIBRI_STATUS_WAIT_PROBE.  No fault, no hang: the context stays usable.
+ * Returns COLIBRI_ERR_INVALID_ARG for a NULL ctx or a limit out of range, COLIBRI_ERR_CUDA if the
+ * launch fails.  Asynchronous: read the bit with colibri_moe_device_status. */
+#define COLIBRI_STATUS_WAIT_PROBE (1 << 6)
+COLIBRI_API int colibri_moe_probe_wait_timeout(colibri_moe_t* ctx, int32_t timeout_us, void* stream);
+
 /* Routing without any allocation (no counterpart in the articles: an addition for callers that
  * cannot allocate device memory -- code that runs inside a host framework whose memory pool owns
  * the whole GPU, real-time loops where cudaMalloc's implicit synchronisation is not allowed, or

@@ -24,6 +24,7 @@ __all__ = ["MoELayer", "ColibriError", "lib", "LIB_PATH", "DTYPE_F32", "DTYPE_BF
 
 DTYPE_F32, DTYPE_BF16 = 0, 1
 ACT_RELU_BIAS, ACT_SWIGLU = 0, 1
+STATUS_WAIT_PROBE = 1 << 6  # set by probe_wait_timeout when its bounded wait gives up
 GATE_SOFTMAX_SELECTED, GATE_SOFTMAX_ALL = 0, 1
 _GATES = {"selected": GATE_SOFTMAX_SELECTED, "pair": GATE_SOFTMAX_SELECTED, "all": GATE_SOFTMAX_ALL,
           "full": GATE_SOFTMAX_ALL}
@@ -35,7 +36,7 @@ EXPORTED = ("colibri_moe_create", "colibri_moe_load_weights", "colibri_moe_forwa
             "colibri_moe_get_routing", "colibri_moe_debug_buffer", "colibri_moe_num_stages",
             "colibri_moe_forward_host_async", "colibri_moe_host_sync",
             "colibri_moe_last_kernel_count", "colibri_moe_set_stage_events", "colibri_moe_device_status",
-            "colibri_moe_route_noalloc",
+            "colibri_moe_probe_wait_timeout", "colibri_moe_route_noalloc",
             "colibri_moe_destroy", "colibri_moe_strerror")
 
 
@@ -84,6 +85,7 @@ def lib() -> ctypes.CDLL:
             "colibri_moe_last_kernel_count": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
             "colibri_moe_set_stage_events": ([vp, vp, i32], ctypes.c_int),
             "colibri_moe_device_status": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
+            "colibri_moe_probe_wait_timeout": ([vp, i32, vp], ctypes.c_int),
             "colibri_moe_route_noalloc": ([vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp], ctypes.c_int),
             "colibri_moe_destroy": ([vp], None),
             "colibri_moe_strerror": ([ctypes.c_int], ctypes.c_char_p),
@@ -295,6 +297,11 @@ class MoELayer:
         v = ctypes.c_int32()
         _check(lib().colibri_moe_device_status(self._h, ctypes.byref(v)), "colibri_moe_device_status")
         return v.value
+
+    def probe_wait_timeout(self, timeout_us: int, stream=None) -> None:
+        """Enqueue one bounded wait that runs out after timeout_us (sets STATUS_WAIT_PROBE)."""
+        _check(lib().colibri_moe_probe_wait_timeout(self._h, int(timeout_us), _stream_handle(stream)),
+               "colibri_moe_probe_wait_timeout")
 
 
 class _DeviceArray:

@@ -870,6 +870,18 @@ int colibri_moe_set_stage_events(colibri_moe_t* ctx, void* const* events, int32_
   return COLIBRI_OK;
 }
 
+int colibri_moe_probe_wait_timeout(colibri_moe_t* ctx, int32_t timeout_us, void* stream) {
+  if (!ctx || timeout_us < 1 || timeout_us > 1000000) return COLIBRI_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return COLIBRI_ERR_CUDA;
+  if (launch_wait_probe(&ctx->sched->status, static_cast<uint64_t>(timeout_us) * 1000ull,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return COLIBRI_ERR_CUDA;
+  }
+  return COLIBRI_OK;
+}
+
 int colibri_moe_device_status(colibri_moe_t* ctx, int32_t* status) {
   if (!ctx || !status) return COLIBRI_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);

@@ -30,6 +30,7 @@ enum : int32_t {
   kStatusBadRow = 1 << 3,
   kStatusTimeoutGridSync = 1 << 4,
   kStatusTimeoutRouter = 1 << 5,
+  kStatusWaitProbe = 1 << 6,  // the failure-detection probe's wait ran out (as it is meant to)
 };
 
 // Routing summary in device memory.  Written by the last CTA of the router kernel, read by
@@ -284,6 +285,7 @@ cudaError_t launch_decode_fused(const CUtensorMap& tmW13, const CUtensorMap& tmX
                                 const CUtensorMap& tmH, const CUtensorMap& tmW13h, const FusedDecodeArgs& a, int grid,
                                 cudaStream_t s);
 cudaError_t launch_decode_combine(int out_dtype, const DecodeCombineArgs& a, cudaStream_t s);
+cudaError_t launch_wait_probe(int32_t* status, uint64_t timeout_ns, cudaStream_t s);
 int tc_gemm_block_n();
 int tc_gemm_threads();
 

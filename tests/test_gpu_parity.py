@@ -590,6 +590,29 @@ def test_last_kernel_count_matches_the_path(monkeypatch):
     torch.cuda.synchronize()
 
 
+def test_bounded_wait_runs_out_and_the_context_stays_usable():
+    """Failure detection without a fault: the probe runs the kernels' bounded mbarrier wait on a
+    barrier nothing arrives on; after its time limit the wait gives up, the status bit is reported
+    (and cleared by the read), and the same context then runs a forward that matches the oracle."""
+    import time
+    import mixture_experts_gemm_gb300 as moe
+    li = testgen.make_inputs(testgen.LayerShape("probe", 300, 256, 512, 4, testgen.ACT_SWIGLU, "bf16"))
+    layer = make_layer(li)
+    assert layer.device_status() == 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    layer.probe_wait_timeout(20000)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert 0.019 <= waited < 1.0, waited
+    assert layer.device_status() == moe.STATUS_WAIT_PROBE
+    assert layer.device_status() == 0              # reading clears it
+    for bad in (0, -5, 1000001):
+        with pytest.raises(RuntimeError):
+            layer.probe_wait_timeout(bad)
+    _full_check(li, layer=layer)                   # device_status() == 0 asserted inside
+
+
 def test_stage_events_time_every_stage():
     shape = testgen.LayerShape("events", 512, 512, 512, 8, testgen.ACT_SWIGLU, "bf16")
     li = testgen.make_inputs(shape)
