@@ -445,6 +445,31 @@ def test_mixtral_prefill_workload(mixtral):
     assert layer.device_status() == 0
 
 
+@pytest.mark.parametrize("dtype,T,k,shared", [("bf16", 60000, 2, False), ("bf16", 33000, 4, False),
+                                               ("f32", 20000, 2, False)])
+def test_large_batch_many_router_chunks(dtype, T, k, shared):
+    """Tens of thousands of tokens: up to 1875 router chunks of 32 tokens, so the chunk histograms,
+    their scan and the dispatch run far past the benchmark sizes.  Routing checked in full (bit for
+    bit outside near ties), output rows sampled against the oracle (every expert's first and last
+    token, the rarest experts' tokens, random others)."""
+    shape = testgen.LayerShape(f"many-chunks-{dtype}-{T}", T, 256, 256, 16, testgen.ACT_SWIGLU, dtype,
+                               zipf_router_bias=True, top_k=k, shared_expert=shared)
+    li = testgen.make_inputs(shape)
+    layer = make_layer(li)
+    out, r = run(layer, x_device(li))
+    L = oracle.OracleLayer.from_inputs(li)
+    logits = L.router_logits(li.x_f32)
+    idx, gate = L.topk(logits)
+    counts, offs, row_of, _ = L.dispatch(idx)
+    check_routing(r, logits, idx, gate, shape.num_experts, row_of, offs)
+    tokens = sample_tokens(idx, shape.num_experts, 64)
+    ref = L.forward_rows(li.x_f32, idx, gate, tokens)
+    err = rel_err(out[tokens], ref)
+    assert err <= (TOL_F32 if dtype == "f32" else TOL_BF16), err
+    assert np.isfinite(out).all()
+    assert layer.device_status() == 0
+
+
 @pytest.mark.parametrize("T", testgen.DECODE_TOKENS)
 def test_mixtral_decode_workload(mixtral, T):
     li, layer, L = mixtral
