@@ -43,7 +43,14 @@ constexpr int PTQ = 4;  // tile-id queue depth (dynamic tile order)
 constexpr int kPublishAt = 4;  // stage of a tile at which the leader hands out the next tile's index
 // full, empty, tmem_full[2], tmem_empty[2], drain, gfull, tile queue full / empty
 constexpr int PNUM_BARS = 3 * PSTAGES + 5 + 2 * PTQ;
-constexpr int PSMEM_BYTES = 1024 + PSTAGES * PSTAGE_BYTES + PNUM_BARS * 8 + 16 + 4 * (4 * kMaxE + 4 + PTQ);
+// Epilogue staging: each epilogue warp turns its 32 rows x 32 words of a chunk around in shared
+// memory (row stride 36 words: both the row-per-thread writes and the 4-rows-per-instruction reads
+// are free of bank conflicts), so that every global write instruction covers four whole 128-byte row
+// segments instead of 16 bytes of 32 different rows.
+constexpr int PSTG_LD = 36;
+constexpr int PSTG_BYTES = 4 * 32 * PSTG_LD * 4;  // 4 warps x 32 rows x 36 words
+constexpr int PSMEM_BYTES =
+    1024 + PSTAGES * PSTAGE_BYTES + PSTG_BYTES + PNUM_BARS * 8 + 16 + 4 * (4 * kMaxE + 4 + PTQ);
 static_assert(PSMEM_BYTES <= 227 * 1024, "pair GEMM shared memory");
 static_assert(PSTAGES % kForwarders == 0, "a stage keeps its forwarder across ring cycles");
 
@@ -71,7 +78,8 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + PSTAGES * PA_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + PSTAGES * PB_BYTES);
+  uint32_t* s_stage = reinterpret_cast<uint32_t*>(sB + PSTAGES * PB_BYTES);  // epilogue staging
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s_stage) + PSTG_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + PNUM_BARS);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_counts = reinterpret_cast<int*>(tmem_slot + 4);
@@ -395,12 +403,33 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
         break;
       }
       tc_fence_after();
-      const int row = s_offsets[c.e] + (2 * c.pm + static_cast<int>(rank)) * PBM + q * 32 + lane;
-      const bool valid = row < s_offsets[c.e] + s_counts[c.e];
+      const int row0 = s_offsets[c.e] + (2 * c.pm + static_cast<int>(rank)) * PBM + q * 32;  // this warp's rows
+      const int seg_end = s_offsets[c.e] + s_counts[c.e];
+      const bool valid = row0 + lane < seg_end;  // this thread's row (the TMEM lane it reads)
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * PBN);
+      // write-back mapping: lane -> row 4 * i + rr of the warp's 32 (i = 0..7), 16-byte column group cg
+      const int rr = lane >> 3, cg = lane & 7;
+      uint32_t* stg = s_stage + q * (32 * PSTG_LD);
+      uint32_t* stg_mine = stg + lane * PSTG_LD;          // row-per-thread side
+      const uint32_t* stg_wb = stg + rr * PSTG_LD + 4 * cg;  // + 4 * i * PSTG_LD: write-back side
+      // rows of the write-back side that exist: bit i for row 4 * i + rr
+      uint32_t wb_valid = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) wb_valid |= (row0 + 4 * i + rr < seg_end ? 1u : 0u) << i;
+      // a chunk pair of bf16 results (64 columns, 128 bytes per row) from the staging tile to rows of `out`
+      auto write_bf16_rows = [&](__nv_bfloat16* out, int64_t ldo) {
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 val = *reinterpret_cast<const uint4*>(stg_wb + 4 * i * PSTG_LD);
+          if ((wb_valid >> i) & 1u)
+            *reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + 4 * i + rr) * ldo + 8 * cg) = val;
+        }
+        __syncwarp();  // the staging tile is rewritten next
+      };
       if constexpr (EPI == kEpiSwiGLU) {
         // columns [0,128) = gate (B half of the leader), [128,256) = up (B half of the peer)
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(row) * a.ldo + c.n * (PBN / 2);
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + c.n * (PBN / 2);
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t g[32], u[32];
@@ -413,14 +442,13 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
             const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
             pk[i] = pack_bf16(silu_fast(g0) * u0, silu_fast(g1) * u1);
           }
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
+          uint4* dst = reinterpret_cast<uint4*>(stg_mine + 16 * (ch & 1));
 #pragma unroll
-            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          }
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          if (ch & 1) write_bf16_rows(out + (ch - 1) * 32, a.ldo);
         }
       } else if constexpr (EPI == kEpiReluBias) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(row) * a.ldo + c.n * PBN;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + c.n * PBN;
         const float* bias = a.bias + static_cast<size_t>(c.e) * a.out_cols + c.n * PBN;
 #pragma unroll 1
         for (int ch = 0; ch < 8; ++ch) {
@@ -431,59 +459,61 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
           for (int i = 0; i < 16; ++i)
             pk[i] = pack_bf16(fmaxf(__uint_as_float(v[2 * i]) + bias[ch * 32 + 2 * i], 0.f),
                               fmaxf(__uint_as_float(v[2 * i + 1]) + bias[ch * 32 + 2 * i + 1], 0.f));
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
+          uint4* dst = reinterpret_cast<uint4*>(stg_mine + 16 * (ch & 1));
 #pragma unroll
-            for (int w = 0; w < 4; ++w) dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
-          }
+          for (int w = 0; w < 4; ++w) dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+          if (ch & 1) write_bf16_rows(out + (ch - 1) * 32, a.ldo);
         }
-      } else if constexpr (EPI == kEpiCombineF32) {
-        // out[token] += gate * (acc (+ b2)): with two slots and a zeroed output the two reductions give
-        // RN(g0*y0 + g1*y1) in either order, the value the separate combine computes
-        const int tok = valid ? a.token_of_row[row] : 0;
-        const float gr = valid ? a.gate_of_row[row] : 0.f;
-        float* out = static_cast<float*>(a.out) + static_cast<size_t>(tok) * a.ldo + c.n * PBN;
+      } else {
+        // fp32 results: Y rows, or (kEpiCombineF32) out[token] += gate * (acc (+ b2)); with two slots
+        // and a zeroed output the two reductions give RN(g0*y0 + g1*y1) in either order, the value the
+        // separate combine computes
+        constexpr bool kCombine = EPI == kEpiCombineF32;
         const float* bias = a.bias ? a.bias + static_cast<size_t>(c.e) * a.out_cols + c.n * PBN : nullptr;
+        // token and gate of the write-back side's rows (those of row 4 * i + rr sit in lane 4 * i + rr)
+        const int my_tok = kCombine && valid ? __ldcg(a.token_of_row + row0 + lane) : 0;
+        const float my_g = kCombine && valid ? __ldcg(a.gate_of_row + row0 + lane) : 0.f;
+        int tok[8];
+        float gr[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          tok[i] = __shfl_sync(0xffffffffu, my_tok, 4 * i + rr);
+          gr[i] = __shfl_sync(0xffffffffu, my_g, 4 * i + rr);
+        }
 #pragma unroll 1
         for (int ch = 0; ch < PBN / 32; ++ch) {
           uint32_t v[32];
           tmem_ld32_sync(tbase + ch * 32, v);
-          if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(stg_mine);
 #pragma unroll
-            for (int w = 0; w < 8; ++w) {
-              float y[4];
+          for (int w = 0; w < 8; ++w) dst[w] = make_uint4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+          __syncwarp();
+          const int col = ch * 32 + 4 * cg;  // this lane's 4 columns of the chunk
+          float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (bias) b4 = make_float4(bias[col], bias[col + 1], bias[col + 2], bias[col + 3]);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                y[i] = __uint_as_float(v[4 * w + i]);
-                if (bias) y[i] += bias[ch * 32 + 4 * w + i];
-                y[i] = __fmul_rn(gr, y[i]);
+          for (int i = 0; i < 8; ++i) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(stg_wb + 4 * i * PSTG_LD);
+            float y[4] = {__uint_as_float(raw.x), __uint_as_float(raw.y), __uint_as_float(raw.z),
+                          __uint_as_float(raw.w)};
+            if (bias) {
+              y[0] += b4.x;
+              y[1] += b4.y;
+              y[2] += b4.z;
+              y[3] += b4.w;
+            }
+            if ((wb_valid >> i) & 1u) {
+              if constexpr (kCombine) {
+                float* o = static_cast<float*>(a.out) + static_cast<size_t>(tok[i]) * a.ldo + c.n * PBN + col;
+                red_add_v4(o, __fmul_rn(gr[i], y[0]), __fmul_rn(gr[i], y[1]), __fmul_rn(gr[i], y[2]),
+                           __fmul_rn(gr[i], y[3]));
+              } else {
+                float* o = static_cast<float*>(a.out) + static_cast<size_t>(row0 + 4 * i + rr) * a.ldo + c.n * PBN + col;
+                *reinterpret_cast<float4*>(o) = make_float4(y[0], y[1], y[2], y[3]);
               }
-              red_add_v4(out + ch * 32 + 4 * w, y[0], y[1], y[2], y[3]);
             }
           }
-        }
-      } else {
-        float* out = static_cast<float*>(a.out) + static_cast<size_t>(row) * a.ldo + c.n * PBN;
-        const float* bias = a.bias ? a.bias + static_cast<size_t>(c.e) * a.out_cols + c.n * PBN : nullptr;
-#pragma unroll 1
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t v[32];
-          tmem_ld32_sync(tbase + ch * 32, v);
-          if (valid) {
-            float4* dst = reinterpret_cast<float4*>(out + ch * 32);
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-              float4 o = make_float4(__uint_as_float(v[4 * w]), __uint_as_float(v[4 * w + 1]),
-                                     __uint_as_float(v[4 * w + 2]), __uint_as_float(v[4 * w + 3]));
-              if (bias) {
-                o.x += bias[ch * 32 + 4 * w];
-                o.y += bias[ch * 32 + 4 * w + 1];
-                o.z += bias[ch * 32 + 4 * w + 2];
-                o.w += bias[ch * 32 + 4 * w + 3];
-              }
-              dst[w] = o;
-            }
-          }
+          __syncwarp();  // the staging tile is rewritten next
         }
       }
       tc_fence_before();
