@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
       int p = seq_first(sq, true);
       bool ok = sq.ok;
       for (; ok && p >= 0; p = seq_next(sq, p, true), ok = ok && sq.ok) {
-        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, s_abort, a.timeout_ns)) {
+        if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1u, s_abort, a.timeout_ns)) {
           ok = false;
           break;
         }
@@ -518,7 +518,15 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(mapa_shared(tempty0 + 8 * acc, 0));
+      // accumulator free: the leader's barrier; the peer arrives with the default CTA-scope release
+      // (a cluster-scope release costs about a microsecond per arrival; nothing but the tcgen05 loads
+      // fenced above is ordered by it) and the MMA issuer acquires at cluster scope
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(tempty0 + 8 * acc);
+        else
+          mbar_arrive_peer(mapa_shared(tempty0 + 8 * acc, 0));
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
