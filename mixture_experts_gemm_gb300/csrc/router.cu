@@ -183,7 +183,6 @@ __device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[kMaxSlots],
       a.sched->ticket = 0;
       a.sched->grid_sync = 0;
       a.sched->tile_ctr[0] = a.sched->tile_ctr[1] = 0;
-    a.sched->tile_ctr[0] = a.sched->tile_ctr[1] = 0;
       for (int i = 0; i < a.n_tile_done; ++i) a.tile_done[i] = 0;
     }
     return;
