@@ -615,6 +615,32 @@ def test_last_kernel_count_matches_the_path(monkeypatch):
     torch.cuda.synchronize()
 
 
+def test_two_contexts_on_two_streams_concurrently():
+    """Contexts share no device state: two layers (one on the grouped-GEMM path, one on the
+    cooperative decode path) forward on two streams at once, several times over without a host
+    synchronisation in between, and each output equals its own sequential run bit for bit."""
+    la = testgen.make_inputs(testgen.LayerShape("conc-a", 900, 512, 384, 8, testgen.ACT_SWIGLU, "bf16",
+                                                zipf_router_bias=True))
+    lb = testgen.make_inputs(testgen.LayerShape("conc-b", 24, 512, 768, 16, testgen.ACT_SWIGLU, "bf16",
+                                                top_k=4, shared_expert=True))
+    layer_a, layer_b = make_layer(la), make_layer(lb)
+    xa, xb = x_device(la), x_device(lb)
+    ref_a = layer_a.forward(xa).clone()
+    ref_b = layer_b.forward(xb).clone()
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    outs_a = [torch.empty_like(ref_a) for _ in range(4)]
+    outs_b = [torch.empty_like(ref_b) for _ in range(4)]
+    for i in range(4):
+        layer_a.forward(xa, outs_a[i], stream=sa)
+        layer_b.forward(xb, outs_b[i], stream=sb)
+    torch.cuda.synchronize()
+    for i in range(4):
+        assert torch.equal(outs_a[i], ref_a), i
+        assert torch.equal(outs_b[i], ref_b), i
+    assert layer_a.device_status() == 0 and layer_b.device_status() == 0
+
+
 def test_bounded_wait_runs_out_and_the_context_stays_usable():
     """Failure detection without a fault: the probe runs the kernels' bounded mbarrier wait on a
     barrier nothing arrives on; after its time limit the wait gives up, the status bit is reported
