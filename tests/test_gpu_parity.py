@@ -173,12 +173,12 @@ def test_cooperative_decode_kernel_equals_separate_kernels(case, monkeypatch):
 
 
 def _decode_splits(items0, kblocks, grid, s_max):
-    """The cooperative decode kernel's K-split rule (smallest split count filling >= 90 % of its waves)."""
+    """The cooperative decode kernel's K-split rule (smallest split count filling >= 95 % of its waves)."""
     best, best_num, best_den = 1, -1, 1
     for S in range(1, min(s_max, kblocks) + 1):
         items = items0 * S
         waves = -(-items // grid)
-        if items >= grid and items * 10 >= waves * grid * 9:
+        if items >= grid and items * 20 >= waves * grid * 19:
             return S
         if items * best_den > best_num * waves * grid:
             best, best_num, best_den = S, items, waves * grid
