@@ -347,7 +347,7 @@ def main():
         e2e = {"value": whole_job_rate(world, T, k_e2e, el), "unit": UNIT,
                "h2d_bytes_per_step": xh.numel() * xh.element_size(),
                "d2h_bytes_per_step": oh.numel() * oh.element_size(),
-               "mode": "colibri_moe_forward_host_async: copies of step i overlap the forwards of steps i-1, i+1"}
+               "mode": "colibri_moe_forward_host_async: three staging slots; the copies of step i overlap the forwards of the steps around it"}
     clk = clocks.stop()
     status = layer.device_status()
 

@@ -134,9 +134,10 @@ COLIBRI_API int colibri_moe_forward(colibri_moe_t* ctx, const void* x, void* out
 COLIBRI_API int colibri_moe_forward_host(colibri_moe_t* ctx, const void* x_host, void* out_host, int32_t T, void* stream);
 
 /* Pipelined form of forward_host for serving loops (no counterpart in the articles, which run one
- * synchronous batch at a time): returns without waiting.  The context keeps two device staging
+ * synchronous batch at a time): returns without waiting.  The context keeps three device staging
  * slots used in turn and two internal copy streams, so the host->device copy of one call and the
- * device->host copy of the previous one overlap the forwards on `stream`.  The forward is enqueued
+ * device->host copies of earlier ones overlap the forwards on `stream` (a call's input copy waits
+ * only for the result copy of the call three back).  The forward is enqueued
  * on `stream` after this call's input copy; the result copy is ordered after it on an internal
  * stream.  out_host holds the result, and x_host may be reused, once colibri_moe_host_sync returns
  * (until then the copies may still be reading or writing them).  Host buffers should be pinned:

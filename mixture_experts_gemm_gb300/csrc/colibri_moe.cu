@@ -28,6 +28,8 @@ bool pdl_enabled() {
 }
 }  // namespace colibri
 
+constexpr int kHostSlots = 3;  // staging slots of the pipelined host-buffer forward
+
 struct colibri_moe {
   colibri_moe_config_t cfg{};
   int device = 0;
@@ -67,13 +69,14 @@ struct colibri_moe {
   float* gate_of_row = nullptr;
   int32_t* hist = nullptr;
   Sched* sched = nullptr;
-  void* x_stage = nullptr;    // forward_host staging (also slot 0 of the pipelined host path)
-  void* out_stage = nullptr;
-  // pipelined host path (forward_host_async): two staging slots, copy streams and their events
-  void* x_stage2 = nullptr;
-  void* out_stage2 = nullptr;
+  // host-buffer staging: slot 0 serves forward_host; forward_host_async takes the slots in turn,
+  // with two copy streams and per-slot events.  Three slots: a call's copy in waits for the copy out
+  // of the call three back, so copy in, forward and copy out of one call spread over three calls'
+  // time and the copies run at the host link's rate (with two slots that chain set the pace).
+  void* x_stage[kHostSlots] = {};
+  void* out_stage[kHostSlots] = {};
   cudaStream_t h2d = nullptr, d2h = nullptr;
-  cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_done[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr};
+  cudaEvent_t ev_in[kHostSlots] = {}, ev_done[kHostSlots] = {}, ev_free[kHostSlots] = {};
   int slot = 0;
 
   CUtensorMap tm_xp{}, tm_h{}, tm_w13{}, tm_w2{};
@@ -269,7 +272,7 @@ void colibri_moe_destroy(colibri_moe_t* ctx) {
     DeviceGuard g(ctx->device);
     if (ctx->h2d) cudaStreamSynchronize(ctx->h2d);
     if (ctx->d2h) cudaStreamSynchronize(ctx->d2h);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kHostSlots; ++i) {
       if (ctx->ev_in[i]) cudaEventDestroy(ctx->ev_in[i]);
       if (ctx->ev_done[i]) cudaEventDestroy(ctx->ev_done[i]);
       if (ctx->ev_free[i]) cudaEventDestroy(ctx->ev_free[i]);
@@ -359,10 +362,11 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   const size_t o_tiles = carve((d / 128 + 1) * sizeof(uint32_t));
   const size_t o_spart = carve(static_cast<size_t>(kRouterSplitMaxChunks) * router_split_factor() * kRouterChunk *
                                16 * sizeof(float));
-  const size_t o_xs = carve(T * d * c->esize);
-  const size_t o_os = carve(T * d * c->out_esize);
-  const size_t o_xs2 = carve(T * d * c->esize);
-  const size_t o_os2 = carve(T * d * c->out_esize);
+  size_t o_xs[kHostSlots], o_os[kHostSlots];
+  for (int i = 0; i < kHostSlots; ++i) {
+    o_xs[i] = carve(T * d * c->esize);
+    o_os[i] = carve(T * d * c->out_esize);
+  }
   c->ws_bytes = off;
   if (cudaMalloc(&c->ws, c->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -383,13 +387,13 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   c->partial = part_floats > 0 ? reinterpret_cast<float*>(b + o_part) : nullptr;
   c->tile_done = reinterpret_cast<uint32_t*>(b + o_tiles);
   c->split_part = reinterpret_cast<float*>(b + o_spart);
-  c->x_stage = b + o_xs;
-  c->out_stage = b + o_os;
-  c->x_stage2 = b + o_xs2;
-  c->out_stage2 = b + o_os2;
+  for (int i = 0; i < kHostSlots; ++i) {
+    c->x_stage[i] = b + o_xs[i];
+    c->out_stage[i] = b + o_os[i];
+  }
   bool streams_ok = cudaStreamCreateWithFlags(&c->h2d, cudaStreamNonBlocking) == cudaSuccess &&
                     cudaStreamCreateWithFlags(&c->d2h, cudaStreamNonBlocking) == cudaSuccess;
-  for (int i = 0; i < 2 && streams_ok; ++i)
+  for (int i = 0; i < kHostSlots && streams_ok; ++i)
     streams_ok = cudaEventCreateWithFlags(&c->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
                  cudaEventCreateWithFlags(&c->ev_done[i], cudaEventDisableTiming) == cudaSuccess &&
                  cudaEventCreateWithFlags(&c->ev_free[i], cudaEventDisableTiming) == cudaSuccess;
@@ -731,15 +735,18 @@ int colibri_moe_forward_host(colibri_moe_t* ctx, const void* x_host, void* out_h
   const size_t xb = static_cast<size_t>(T) * ctx->cfg.d_model * ctx->esize;
   const size_t ob = static_cast<size_t>(T) * ctx->cfg.d_model * ctx->out_esize;
   // after any pipelined call still copying out of the staging slots
-  if (cudaStreamWaitEvent(s, ctx->ev_free[0], 0) != cudaSuccess ||
-      cudaStreamWaitEvent(s, ctx->ev_free[1], 0) != cudaSuccess ||
-      cudaMemcpyAsync(ctx->x_stage, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+  for (int i = 0; i < kHostSlots; ++i)
+    if (cudaStreamWaitEvent(s, ctx->ev_free[i], 0) != cudaSuccess) {
+      cudaGetLastError();
+      return COLIBRI_ERR_CUDA;
+    }
+  if (cudaMemcpyAsync(ctx->x_stage[0], x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
     cudaGetLastError();
     return COLIBRI_ERR_CUDA;
   }
-  int rc = enqueue_forward(ctx, ctx->x_stage, ctx->out_stage, T, s);
+  int rc = enqueue_forward(ctx, ctx->x_stage[0], ctx->out_stage[0], T, s);
   if (rc) return rc;
-  if (cudaMemcpyAsync(out_host, ctx->out_stage, ob, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+  if (cudaMemcpyAsync(out_host, ctx->out_stage[0], ob, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess) {
     cudaGetLastError();
     return COLIBRI_ERR_CUDA;
@@ -761,11 +768,11 @@ int colibri_moe_forward_host_async(colibri_moe_t* ctx, const void* x_host, void*
   if (!g.ok) return COLIBRI_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int k = ctx->slot;
-  void* xs = k ? ctx->x_stage2 : ctx->x_stage;
-  void* os = k ? ctx->out_stage2 : ctx->out_stage;
+  void* xs = ctx->x_stage[k];
+  void* os = ctx->out_stage[k];
   const size_t xb = static_cast<size_t>(T) * ctx->cfg.d_model * ctx->esize;
   const size_t ob = static_cast<size_t>(T) * ctx->cfg.d_model * ctx->out_esize;
-  // slot k is free once the call two back has copied its result out (its forward read x before)
+  // slot k is free once the call kHostSlots back has copied its result out (its forward read x before)
   if (cudaStreamWaitEvent(ctx->h2d, ctx->ev_free[k], 0) != cudaSuccess ||
       cudaMemcpyAsync(xs, x_host, xb, cudaMemcpyHostToDevice, ctx->h2d) != cudaSuccess ||
       cudaEventRecord(ctx->ev_in[k], ctx->h2d) != cudaSuccess || cudaStreamWaitEvent(s, ctx->ev_in[k], 0) != cudaSuccess) {
@@ -780,7 +787,7 @@ int colibri_moe_forward_host_async(colibri_moe_t* ctx, const void* x_host, void*
     cudaGetLastError();
     return COLIBRI_ERR_CUDA;
   }
-  ctx->slot = k ^ 1;
+  ctx->slot = (k + 1) % kHostSlots;
   return COLIBRI_OK;
 }
 
