@@ -488,6 +488,38 @@ def test_mixtral_deterministic(mixtral):
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("T", [8192, 1, 4, 32])
+def test_mixtral_many_forwards_bit_identical(mixtral, T):
+    """Races between the kernels' roles (accumulator hand-over across the CTA pair, the tile queue,
+    grid barriers, the epilogue hand-over of the decode kernel) would show as outputs that differ
+    from run to run: 40 back-to-back forwards (12 at the prefill size), each equal to the first."""
+    li, layer, L = mixtral
+    x = x_device(li, T)
+    first = layer.forward(x).clone()
+    outs = [torch.empty_like(first) for _ in range(12 if T > 64 else 40)]
+    for o in outs:
+        layer.forward(x, o)
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        assert torch.equal(o, first), i
+    assert layer.device_status() == 0
+
+
+@pytest.mark.parametrize("name", ["skewed-16e", "1.3b-8e"])
+def test_workload_many_forwards_bit_identical(name):
+    li = testgen.make_inputs(testgen.CONFIGS[name])
+    layer = make_layer(li)
+    x = x_device(li)
+    first = layer.forward(x).clone()
+    outs = [torch.empty_like(first) for _ in range(40)]
+    for o in outs:
+        layer.forward(x, o)
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        assert torch.equal(o, first), i
+    assert layer.device_status() == 0
+
+
 # ------------------------------------------------------------------ edge cases and the boundary
 def test_zero_router_gives_empty_experts_and_ties():
     shape = testgen.LayerShape("zero-router", 200, 256, 256, 8, testgen.ACT_SWIGLU, "bf16")
