@@ -80,8 +80,8 @@ struct colibri_moe {
   int slot = 0;
 
   CUtensorMap tm_xp{}, tm_h{}, tm_w13{}, tm_w2{};
-  // decode path (T <= decode_max_t): 128-row weight boxes, token boxes of 16/32/48/64 rows
-  CUtensorMap tm_w13_dec{}, tm_w2_dec{}, tm_xp_dec[4]{}, tm_h_dec[4]{};
+  // decode path (T <= decode_max_t): 128-row weight boxes, token boxes of 16, 32, ..., 128 rows
+  CUtensorMap tm_w13_dec{}, tm_w2_dec{}, tm_xp_dec[kDecodeMaxT / 16]{}, tm_h_dec[kDecodeMaxT / 16]{};
   CUtensorMap tm_w13_half{};  // 64-row boxes: the cooperative decode kernel's gate/up pairs
   float* partial = nullptr;  // decode partial sums [splits][n_pad][E * rows]
   uint32_t* tile_done = nullptr;  // cooperative decode kernel: items done per down-projection tile
@@ -230,13 +230,17 @@ bool env_decode_fused() {
   return !(s && s[0] == '0');
 }
 
-int env_decode_max_t() {
+// Batches of up to this many tokens take the decode path: 128 for experts of at least 2^25 weights
+// per matrix (d_model x d_ff; at the Mixtral shape the cooperative kernel wins up to 128 tokens),
+// else 64 (with smaller experts the grouped GEMMs catch up between 64 and 96 tokens).
+// COLIBRI_MOE_DECODE_MAX_T overrides (0 .. kDecodeMaxT; 0 turns the decode path off).
+int env_decode_max_t(int64_t d, int64_t f) {
   const char* s = std::getenv("COLIBRI_MOE_DECODE_MAX_T");
   if (s) {
     long v = std::strtol(s, nullptr, 10);
     if (v >= 0 && v <= kDecodeMaxT) return static_cast<int>(v);
   }
-  return kDecodeMaxT;
+  return d * f >= (int64_t{1} << 25) ? kDecodeMaxT : kDecodeSepMaxT;
 }
 
 uint64_t env_timeout_ns() {
@@ -351,7 +355,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   const size_t o_hist = carve(static_cast<size_t>(c->nchunks_max) * Ex * 4);
   const size_t o_sched = carve(sizeof(Sched));
   // decode partial sums: bf16 layers whose batches can be decode-sized
-  c->decode_max_t = cfg->dtype == COLIBRI_DTYPE_BF16 ? env_decode_max_t() : 0;
+  c->decode_max_t = cfg->dtype == COLIBRI_DTYPE_BF16 ? env_decode_max_t(d, f) : 0;
   if (c->decode_max_t > T) c->decode_max_t = static_cast<int>(T);
   const int64_t npad_max = (c->decode_max_t + 15) / 16 * 16;
   const int64_t part_floats = c->decode_max_t > 0
@@ -428,7 +432,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   if (cfg->dtype == COLIBRI_DTYPE_BF16) {
     bool ok = make_tmap(&c->tm_xp, c->xp, d, c->rows_alloc, kRowTile) &&
               make_tmap(&c->tm_h, c->h, f, c->rows_alloc, kRowTile);
-    for (int i = 0; ok && i < 4; ++i)
+    for (int i = 0; ok && i < kDecodeMaxT / 16; ++i)
       ok = make_tmap(&c->tm_xp_dec[i], c->xp, d, c->rows_alloc, 16 * (i + 1)) &&
            make_tmap(&c->tm_h_dec[i], c->h, f, c->rows_alloc, 16 * (i + 1));
     if (!ok) {
@@ -561,7 +565,8 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
 
   // Two slots with an fp32 output on the prefill path: the down GEMM adds g * y straight into out
   // (cleared first); two fp32 additions onto zero give the same value in either order.
-  const bool decode = bf16 && T <= ctx->decode_max_t;
+  // (the separate decode kernels serve up to kDecodeSepMaxT tokens, the cooperative kernel more)
+  const bool decode = bf16 && T <= ctx->decode_max_t && (ctx->decode_fused || T <= kDecodeSepMaxT);
   const bool fuse = bf16 && !decode && ctx->fuse_combine && ctx->S == 2 && c.out_dtype == COLIBRI_DTYPE_F32;
   // bf16 prefill: the up GEMM gathers its A rows from x through token_of_row instead of reading a
   // materialised Xp; the dispatch kernel then only writes the row bookkeeping.

@@ -1,4 +1,4 @@
-// Decode-sized batches (T <= 64) in one cooperative kernel: up projection, activation, down
+// Decode-sized batches (T <= 128) in one cooperative kernel: up projection, activation, down
 // projection and combine, separated by grid-wide barriers instead of kernel boundaries.
 //
 // What is computed is the separate-kernel decode path's (gemm_decode.cu: the Compute stage of
@@ -20,7 +20,7 @@
 //
 // The token operand of phase U is x itself (all n_pad >= T token rows of the batch, rows past T
 // read as zeros by TMA), so no dispatch copy is needed: a column t of expert e's accumulator is
-// kept only when t was routed to e (a 64-bit token mask per expert).  One persistent CTA per SM,
+// kept only when t was routed to e (a 128-bit token mask per expert).  One persistent CTA per SM,
 // the warp roles of the decode GEMM (TMA producer, MMA issuer, 4 epilogue warps); every thread
 // joins the element-wise phase A.  The weight tiles of phase D are requested before the barriers
 // that precede it (they do not depend on phase A), so the HBM stream continues across them.
@@ -36,17 +36,19 @@ namespace {
 using namespace ptx;
 
 constexpr int FBM = 128, FBK = 64, FUMMA_K = 16;
-constexpr int FSTAGES = 8;
+// The ring: FSTAGES_MAX stages of a 16 KB weight tile and an 8 KB token slot (n_pad <= 64), or six
+// stages with a 16 KB token slot for 65..128 tokens.
+constexpr int FSTAGES_MAX = 8;
+constexpr int FRING_BYTES = 192 * 1024;
 constexpr int FA_BYTES = FBM * FBK * 2;          // 16 KB weight tile
-constexpr int FB_SLOT = kDecodeMaxT * FBK * 2;   // 8 KB token tile slot (n_pad rows used)
 constexpr int FNUM_THREADS = 192;
-constexpr uint32_t FTMEM_COLS = 128;             // two accumulators of up to 64 fp32 columns
-constexpr int FNUM_BARS = 2 * FSTAGES + 5;
+constexpr uint32_t FTMEM_COLS = 2 * kDecodeMaxT;  // two accumulators of up to 128 fp32 columns
+constexpr int FNUM_BARS = 2 * FSTAGES_MAX + 5;
 constexpr int FHALF = FBM / 2;                   // hidden units per weight tile with SwiGLU (direct H)
 constexpr int FX_CHUNK = 16;                     // token columns per TMEM load
 constexpr int FX_BYTES = 2 * FX_CHUNK * FHALF * 4;  // up values handed over: two buffers of 16 x 64
 constexpr int FSMEM_BYTES =
-    1024 + FSTAGES * (FA_BYTES + FB_SLOT) + FX_BYTES + FNUM_BARS * 8 + 16 + 8 * kMaxE + 4 * (2 * kMaxE + 4);
+    1024 + FRING_BYTES + FX_BYTES + FNUM_BARS * 8 + 16 + 16 * kMaxE + 4 * (2 * kMaxE + 4);
 static_assert(FSMEM_BYTES <= 227 * 1024, "fused decode shared memory");
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
@@ -145,8 +147,9 @@ __device__ __forceinline__ Item item_of(const Phase& p, int it, const int* s_act
 struct Ring {
   int stage = 0;
   uint32_t phase = 0;
+  int n = FSTAGES_MAX;  // stages in the ring
   __device__ __forceinline__ void next() {
-    if (++stage == FSTAGES) {
+    if (++stage == n) {
       stage = 0;
       phase ^= 1u;
     }
@@ -159,27 +162,31 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
                         const __grid_constant__ CUtensorMap tmW13h, const FusedDecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + FSTAGES * FA_BYTES;
-  float* xs = reinterpret_cast<float*>(sB + FSTAGES * FB_SLOT);  // [2][16 tokens][64 units] (direct H)
+  float* xs = reinterpret_cast<float*>(smem + FRING_BYTES);  // [2][16 tokens][64 units] (direct H)
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xs) + FX_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + FNUM_BARS);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  unsigned long long* s_mask = reinterpret_cast<unsigned long long*>(tmem_slot + 4);  // tokens routed to e
-  int* s_act = reinterpret_cast<int*>(s_mask + kMaxE);
+  // tokens routed to e: bit t of the 128-bit mask s_mask[2e] | s_mask[2e + 1] << 64
+  unsigned long long* s_mask = reinterpret_cast<unsigned long long*>(tmem_slot + 4);
+  int* s_act = reinterpret_cast<int*>(s_mask + 2 * kMaxE);
   int* s_nact = s_act + kMaxE;
   volatile int* s_last = s_nact + 1;  // this CTA completed the current weight tile (phase D)
 
   const uint32_t full0 = smem_u32(bars);
-  const uint32_t empty0 = smem_u32(bars + FSTAGES);
-  const uint32_t tfull0 = smem_u32(bars + 2 * FSTAGES);
-  const uint32_t tempty0 = smem_u32(bars + 2 * FSTAGES + 2);
-  const uint32_t drain = smem_u32(bars + 2 * FSTAGES + 4);
+  const uint32_t empty0 = smem_u32(bars + FSTAGES_MAX);
+  const uint32_t tfull0 = smem_u32(bars + 2 * FSTAGES_MAX);
+  const uint32_t tempty0 = smem_u32(bars + 2 * FSTAGES_MAX + 2);
+  const uint32_t drain = smem_u32(bars + 2 * FSTAGES_MAX + 4);
+  // ring geometry: stage s holds the weight tile at +0 and the token tile at +16 KB
+  const int stride = a.n_pad <= 64 ? FA_BYTES + 8 * 1024 : FA_BYTES + 16 * 1024;
+  const int nst = FRING_BYTES / stride;  // 8 or 6
+  auto stage_a = [&](int st) { return smem_u32(smem + st * stride); };
+  auto stage_b = [&](int st) { return smem_u32(smem + st * stride + FA_BYTES); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E, T = a.T, Sl = a.S, n_pad = a.n_pad;
   if (warp == 0 && lane == 0) {
-    for (int s = 0; s < FSTAGES; ++s) {
+    for (int s = 0; s < FSTAGES_MAX; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
@@ -200,18 +207,26 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
     tmem_alloc(smem_u32(tmem_slot), FTMEM_COLS);
     tmem_relinquish();
   }
-  if (threadIdx.x < kMaxE) s_mask[threadIdx.x] = 0ull;
+  if (threadIdx.x < 2 * kMaxE) s_mask[threadIdx.x] = 0ull;
   pdl_trigger();
   pdl_wait();  // routing (idx, gates, counts) comes from the router
-  // every routing load of this thread in flight at once (T * S <= 320 slots, E <= 17 counts)
+  // every routing load of this thread in flight at once (T * S <= 640 slots, E <= 17 counts)
+  constexpr int kSlotLoads = 4;
+  static_assert(kSlotLoads * FNUM_THREADS >= kDecodeMaxT * kMaxSlots, "routing slots per thread");
   const int n_slots = T * Sl;
-  const int i0 = threadIdx.x, i1 = threadIdx.x + FNUM_THREADS;
-  const int e0 = i0 < n_slots ? a.idx[i0] : -1;
-  const int e1 = i1 < n_slots ? a.idx[i1] : -1;
+  int ev[kSlotLoads];
+#pragma unroll
+  for (int u = 0; u < kSlotLoads; ++u) {
+    const int i = threadIdx.x + u * FNUM_THREADS;
+    ev[u] = i < n_slots ? a.idx[i] : -1;
+  }
   const int cnt = threadIdx.x < E ? a.sched->counts[threadIdx.x] : 0;
   __syncthreads();  // masks cleared
-  if (e0 >= 0 && e0 < E) atomicOr(&s_mask[e0], 1ull << (i0 / Sl));
-  if (e1 >= 0 && e1 < E) atomicOr(&s_mask[e1], 1ull << (i1 / Sl));
+#pragma unroll
+  for (int u = 0; u < kSlotLoads; ++u) {
+    const int i = threadIdx.x + u * FNUM_THREADS, t = i / Sl;
+    if (ev[u] >= 0 && ev[u] < E) atomicOr(&s_mask[2 * ev[u] + (t >> 6)], 1ull << (t & 63));
+  }
   if (warp == 0) {  // active experts in index order, from the counts
     const unsigned act = __ballot_sync(0xffffffffu, lane < E && cnt > 0);
     if (lane < E && cnt > 0) s_act[__popc(act & ((1u << lane) - 1u))] = lane;
@@ -235,6 +250,7 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
 
   // per-role state, carried from phase U to phase D
   Ring ring;                         // producer and MMA issuer: shared-memory ring position
+  ring.n = nst;
   int acc = 0;                       // MMA issuer and epilogue: TMEM accumulator in use
   uint32_t acc_phase = 0;
   uint32_t armed = 0, armed_phase = 0;  // producer: stages with copies issued (last phase of each)
@@ -270,11 +286,11 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(fb, FA_BYTES + b_bytes);
-          load_weights(P, im, smem_u32(sA + cur.stage * FA_BYTES), fb, kb);
+          load_weights(P, im, stage_a(cur.stage), fb, kb);
         }
         armed |= 1u << cur.stage;
         armed_phase = (armed_phase & ~(1u << cur.stage)) | (cur.phase << cur.stage);
-        tma_load_2d(smem_u32(sB + cur.stage * FB_SLOT), P.tmX, fb, kb * FBK, x_row);
+        tma_load_2d(stage_b(cur.stage), P.tmX, fb, kb * FBK, x_row);
         cur.next();
       }
     }
@@ -289,16 +305,16 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
     pre_start = ring;
     pre = 0;
     bool ok = true;
-    for (int it = blockIdx.x; ok && pre < FSTAGES && it < P.total; it += gridDim.x) {
+    for (int it = blockIdx.x; ok && pre < nst && it < P.total; it += gridDim.x) {
       const Item im = item_of(P, it, s_act);
-      for (int kb = im.kb0; kb < im.kb1 && pre < FSTAGES; ++kb, ++pre) {
+      for (int kb = im.kb0; kb < im.kb1 && pre < nst; ++kb, ++pre) {
         if (!mbar_wait(empty0 + 8 * ring.stage, ring.phase ^ 1u, s_abort, a.timeout_ns)) {
           ok = false;
           break;
         }
         const uint32_t fb = full0 + 8 * ring.stage;
         mbar_arrive_expect_tx(fb, FA_BYTES + b_bytes);
-        load_weights(P, im, smem_u32(sA + ring.stage * FA_BYTES), fb, kb);
+        load_weights(P, im, stage_a(ring.stage), fb, kb);
         ring.next();
       }
     }
@@ -323,8 +339,8 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(sA + ring.stage * FA_BYTES);
-        const uint32_t b_addr = smem_u32(sB + ring.stage * FB_SLOT);
+        const uint32_t a_addr = stage_a(ring.stage);
+        const uint32_t b_addr = stage_b(ring.stage);
 #pragma unroll
         for (int k = 0; k < FBK / FUMMA_K; ++k)
           umma_bf16(d_tmem, sw128_desc(a_addr + k * FUMMA_K * 2), sw128_desc(b_addr + k * FUMMA_K * 2), idesc,
@@ -399,7 +415,9 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
     int xb = 0;
     for (int it = blockIdx.x; it < P.total; it += gridDim.x) {
       const Item im = item_of(P, it, s_act);
-      const unsigned long long mask = s_mask[im.e];
+      const unsigned long long mlo = s_mask[2 * im.e], mhi = s_mask[2 * im.e + 1];
+      // token columns c .. c + 15 of the mask (16-column chunks never straddle its two words)
+      auto mask16 = [&](int c) -> unsigned long long { return c < 64 ? mlo >> c : mhi >> (c - 64); };
       bool ok = mbar_wait(tfull0 + 8 * acc, acc_phase, s_abort, a.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (combine || (P.direct && a.swiglu)) ok = epilogue_all(ok);  // named barriers below need all four warps
@@ -429,7 +447,7 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
               const int col = im.mt * FHALF + wr;
 #pragma unroll
               for (int j = 0; j < FX_CHUNK; ++j)
-                if ((mask >> (c + j)) & 1ull)
+                if ((mask16(c) >> j) & 1ull)
                   hrow[static_cast<size_t>(c + j) * a.f + col] =
                       __float2bfloat16_rn(silu_fast(__uint_as_float(v[j])) * x[j * FHALF + wr]);
             }
@@ -439,7 +457,7 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
             const float b = a.b1[static_cast<size_t>(im.e) * a.f + col];
 #pragma unroll
             for (int j = 0; j < FX_CHUNK; ++j)
-              if ((mask >> (c + j)) & 1ull)
+              if ((mask16(c) >> j) & 1ull)
                 hrow[static_cast<size_t>(c + j) * a.f + col] = __float2bfloat16_rn(fmaxf(__uint_as_float(v[j]) + b, 0.f));
           }
         }
@@ -451,7 +469,7 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
           tmem_ld16_sync(tbase + c, v);
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if ((mask >> (c + j)) & 1ull) out[static_cast<size_t>(c + j) * rows_total] = __uint_as_float(v[j]);
+            if ((mask16(c) >> j) & 1ull) out[static_cast<size_t>(c + j) * rows_total] = __uint_as_float(v[j]);
         }
       }
       tc_fence_before();
@@ -627,7 +645,7 @@ __global__ void __launch_bounds__(FNUM_THREADS, 1)
   // ---------------------------------------------------------------- teardown
   if (warp == 0 && lane == 0) {
     // copies issued but never consumed (only after a timeout) land before the CTA leaves
-    for (int s = 0; s < FSTAGES; ++s)
+    for (int s = 0; s < nst; ++s)
       if (armed & (1u << s)) {
         volatile int never = 0;
         mbar_wait(full0 + 8 * s, (armed_phase >> s) & 1u, &never, a.timeout_ns);

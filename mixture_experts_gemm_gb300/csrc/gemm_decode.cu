@@ -25,7 +25,7 @@ using namespace ptx;
 constexpr int DBM = 128, DBK = 64, DUMMA_K = 16;
 constexpr int DSTAGES = 8;
 constexpr int DA_BYTES = DBM * DBK * 2;      // 16 KB weight tile
-constexpr int DB_SLOT = kDecodeMaxT * DBK * 2;  // 8 KB token-tile slot (n_pad rows used)
+constexpr int DB_SLOT = kDecodeSepMaxT * DBK * 2;  // 8 KB token-tile slot (n_pad rows used)
 constexpr int DNUM_THREADS = 192;
 constexpr uint32_t DTMEM_COLS = 128;           // two accumulators of up to 64 fp32 columns
 constexpr int DNUM_BARS = 2 * DSTAGES + 5;
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(DNUM_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kDecodeMaxT);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kDecodeSepMaxT);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, phase, s_abort, a.timeout_ns)) {
             ok = false;
@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(DNUM_THREADS, 1)
       tc_fence_after();
       const size_t row = static_cast<size_t>(e) * a.n_per_expert + mt * DBM + q * 32 + lane;
       const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kDecodeMaxT);
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kDecodeSepMaxT);
       float* P = a.partial + static_cast<size_t>(sp) * n_pad * rows_total + row;
       for (int c = 0; c < n_pad; c += 16) {
         uint32_t v[16];

@@ -18,7 +18,8 @@ constexpr int kRowTile = 128;        // expert row segments start on multiples o
 constexpr int kRouterChunk = 32;     // tokens per router CTA (4 per warp)
 constexpr int kRouterThreads = 256;
 constexpr int kRouterMaxSmem = 96 * 1024;  // W_r columns staged per router pass (dynamic smem)
-constexpr int kDecodeMaxT = 64;            // batches up to this many tokens take the decode path
+constexpr int kDecodeMaxT = 128;           // most tokens of a decode-path batch (cooperative kernel)
+constexpr int kDecodeSepMaxT = 64;         // most tokens of a batch on the separate decode kernels
 constexpr int kDecodeSplitsUp = 2;         // most K splits of the decode up projection
 constexpr int kDecodeSplitsDown = 8;       // most K splits of the decode down projection
 
@@ -169,12 +170,12 @@ struct DecodeCombineArgs {
   int S;
 };
 
-// Cooperative decode kernel (T <= 64): up projection, activation, down projection, combine.
+// Cooperative decode kernel (T <= 128): up projection, activation, down projection, combine.
 struct FusedDecodeArgs {
   Sched* sched;
   int E;                    // scheduled experts (routed + shared)
   int d, f, n_up;           // model width, hidden width, up-projection weight rows per expert
-  int T, n_pad, S;          // tokens, token columns (16..64, >= T), slots per token
+  int T, n_pad, S;          // tokens, token columns (16..128, >= T), slots per token
   const int32_t* idx;       // [T, S] from the router
   const float* gate;        // [T, S]
   int32_t* row_of;          // [T, S] in: rank in chunk, out: row of the dispatch layout

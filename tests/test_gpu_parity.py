@@ -224,6 +224,34 @@ def test_cooperative_decode_kernel_writes_h_in_the_up_epilogue(case, monkeypatch
     assert np.array_equal(out_d, out_s)
 
 
+@pytest.mark.parametrize("case", ["t65", "t100", "t128", "relu-t90", "k4-shared-t100", "direct-t128"])
+def test_cooperative_decode_kernel_up_to_128_tokens(case, monkeypatch):
+    """COLIBRI_MOE_DECODE_MAX_T up to 128: the cooperative kernel with token tiles of 80..128 rows
+    (16 KB token slots, six ring stages, 128-column accumulators, a 128-bit token mask per expert):
+    against the oracle and against the grouped-GEMM path on the same inputs."""
+    monkeypatch.setenv("COLIBRI_MOE_DECODE_MAX_T", "128")
+    T = int(case.rsplit("t", 1)[1])
+    if case.startswith("relu"):
+        shape = testgen.LayerShape("coop128-relu", T, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")
+    elif case.startswith("k4"):
+        shape = testgen.LayerShape("coop128-k4s", T, 512, 384, 8, testgen.ACT_SWIGLU, "bf16",
+                                   zipf_router_bias=True, top_k=4, shared_expert=True)
+    elif case.startswith("direct"):
+        shape = testgen.LayerShape("coop128-direct", T, 256, 2432, 4, testgen.ACT_SWIGLU, "bf16")
+    else:
+        shape = testgen.LayerShape("coop128", T, 512, 384, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True)
+    li = testgen.make_inputs(shape)
+    layer_c, out_c, r_c, _, _ = _full_check(li)
+    assert layer_c.last_kernel_count() == 2
+    monkeypatch.setenv("COLIBRI_MOE_DECODE_MAX_T", "64")
+    _, out_p, r_p, _, _ = _full_check(li)
+    for k in ("idx", "counts", "offsets", "row_of"):
+        assert np.array_equal(r_c[k], r_p[k]), k
+    assert rel_err(out_c, out_p) <= TOL_BF16
+    out_c2, _ = run(layer_c, x_device(li))
+    assert np.array_equal(out_c, out_c2)
+
+
 def test_decode_path_relu_bias():
     shape = testgen.LayerShape("decode-relu", 20, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")
     li = testgen.make_inputs(shape)
