@@ -35,7 +35,7 @@ STAGES = ["router", "gather", "gemm_up", "gemm_down", "combine"]
 # stands (profiles/gemm_pair_mixtral_prefill.md); None where no capture of the current kernel exists.
 DOM_EVERY = 8  # the dominant kernel is timed with events on every 8th step of the timed region
 NCU_TRAFFIC = {("mixtral-prefill", 8192, "gemm_up", "2sm"): 2.619e9, ("mixtral-prefill", 8192, "gemm_down", "2sm"): 3.022e9,
-               ("mixtral-decode", 1, "gemm_up", "decode"): 0.7096e9, ("mixtral-decode", 16, "gemm_up", "decode"): 2.8338e9}
+               ("mixtral-decode", 1, "gemm_up", "decode"): 0.7092e9, ("mixtral-decode", 16, "gemm_up", "decode"): 2.8339e9}
 
 
 def log(*a):
