@@ -498,6 +498,24 @@ def test_large_batch_many_router_chunks(dtype, T, k, shared):
     assert layer.device_status() == 0
 
 
+def test_decode_limit_follows_the_expert_size(mixtral):
+    """Default decode limit: 128 tokens for experts of >= 2^25 weights per matrix (the Mixtral
+    shape), 64 for smaller ones, where the grouped GEMMs are as fast from ~64-96 tokens on."""
+    li, layer, L = mixtral
+    for T, kernels in ((100, 2), (128, 2), (129, 4)):
+        out, r = run(layer, x_device(li, T))
+        assert layer.last_kernel_count() == kernels, T
+    x129 = li.x_f32[:129]
+    idx, gate = L.topk(L.router_logits(x129))
+    tokens = sample_tokens(idx, li.shape.num_experts, 16)
+    ref = L.forward_rows(x129, idx, gate, tokens)
+    assert rel_err(out[tokens], ref) <= TOL_BF16
+    small = testgen.make_inputs(testgen.LayerShape("limit-small", 100, 512, 384, 8, testgen.ACT_SWIGLU, "bf16"))
+    layer_s = make_layer(small)
+    run(layer_s, x_device(small))
+    assert layer_s.last_kernel_count() == 4
+
+
 @pytest.mark.parametrize("T", testgen.DECODE_TOKENS)
 def test_mixtral_decode_workload(mixtral, T):
     li, layer, L = mixtral
