@@ -35,7 +35,8 @@ STAGES = ["router", "gather", "gemm_up", "gemm_down", "combine"]
 # stands (profiles/gemm_pair_mixtral_prefill.md); None where no capture of the current kernel exists.
 DOM_EVERY = 8  # the dominant kernel is timed with events on every 8th step of the timed region
 NCU_TRAFFIC = {("mixtral-prefill", 8192, "gemm_up", "2sm"): 2.619e9, ("mixtral-prefill", 8192, "gemm_down", "2sm"): 3.022e9,
-               ("mixtral-decode", 1, "gemm_up", "decode"): 0.7092e9, ("mixtral-decode", 16, "gemm_up", "decode"): 2.8339e9}
+               ("mixtral-decode", 1, "gemm_up", "decode"): 0.7092e9, ("mixtral-decode", 16, "gemm_up", "decode"): 2.8339e9,
+               ("1.3b-8e", 512, "gemm_up", "2sm"): 0.3913e9}
 
 
 def log(*a):
@@ -388,8 +389,10 @@ def main():
             byts = n_w * (n_up + 1) * shape.d_model * shape.d_ff * es
         ach = byts / dur / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        path = "decode" if layer.last_kernel_count() == 2 else \
+            ("1sm" if os.environ.get("COLIBRI_MOE_GEMM") == "1sm" else "2sm")
         roof = {"bound": "hbm", "kernel": STAGES[dominant], "achieved": ach, "peak": peak, "unit": "GB/s",
-                "frac": ach / peak, "traffic": NCU_TRAFFIC.get((shape.name, T, STAGES[dominant], "decode")),
+                "frac": ach / peak, "traffic": NCU_TRAFFIC.get((shape.name, T, STAGES[dominant], path)),
                 "peak_source": f"{peak_src} copy", "algorithmic_bytes_per_launch": byts,
                 "step_frac_of_hbm": alg["bytes"] / (ms_per_step / 1e3) / 1e9 / peak, "timing": timed_note}
 
