@@ -1,8 +1,8 @@
 // fp32 grouped expert GEMM on the SIMT FMA pipes (the fp32 dtype path).
 //
 // tcgen05 has no fp32-input kind and TF32 (10-bit mantissa) cannot hold fp32 parity, so fp32
-// layers run here: one CTA per (expert, 32-row slice of a 128-row tile, 64-column tile), 256
-// threads with a 2x4 register tile each (slices past the expert's rows exit at once, so the work
+// layers run here: one CTA per (expert, 32-row slice of a 128-row tile, 32-column tile), 256
+// threads with a 2x2 register tile each (slices past the expert's rows exit at once, so the work
 // follows the real row count), K staged through shared memory 32 at a time; the global loads of the next K
 // slab are issued into registers before the current slab is multiplied, so their latency overlaps
 // the FMAs (these layers are small: latency, not FMA throughput, sets their time).  Each expert is
@@ -14,9 +14,10 @@
 namespace colibri {
 namespace {
 
-constexpr int SBM = 32, SBN = 64, SBK = 32;
+constexpr int SBM = 32, SBN = 32, SBK = 32;
 constexpr int kSlices = kRowTile / SBM;  // row slices per 128-row tile
 constexpr int TM = SBM / 16;             // rows per thread
+constexpr int TN = SBN / 16;             // columns per thread
 constexpr int kLoadsA = SBM * SBK / 256, kLoadsB = SBN * SBK / 256;  // per thread per K slab
 
 template <int EPI>
@@ -45,11 +46,11 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
   const float* __restrict__ B3 = kSwiGLU ? a.b3 + (size_t)e * a.N * a.K : nullptr;
 
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  float acc[TM][4], acc3[TM][4];
+  float acc[TM][TN], acc3[TM][TN];
 #pragma unroll
   for (int i = 0; i < TM; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = acc3[i][j] = 0.f;
+    for (int j = 0; j < TN; ++j) acc[i][j] = acc3[i][j] = 0.f;
 
   float ra[kLoadsA], rb[kLoadsB], rb3[kSwiGLU ? kLoadsB : 1];
   auto load_slab = [&](int k0) {
@@ -84,18 +85,18 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
     if (k0 + SBK < a.K) load_slab(k0 + SBK);  // in flight while this slab is multiplied
 #pragma unroll
     for (int kk = 0; kk < SBK; ++kk) {
-      float af[TM], bf[4], bf3[4];
+      float af[TM], bf[TN], bf3[TN];
 #pragma unroll
       for (int i = 0; i < TM; ++i) af[i] = As[kk][ty * TM + i];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        bf[j] = Bs[kk][tx * 4 + j];
-        if constexpr (kSwiGLU) bf3[j] = B3s[kk][tx * 4 + j];
+      for (int j = 0; j < TN; ++j) {
+        bf[j] = Bs[kk][tx * TN + j];
+        if constexpr (kSwiGLU) bf3[j] = B3s[kk][tx * TN + j];
       }
 #pragma unroll
       for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < TN; ++j) {
           acc[i][j] = fmaf(af[i], bf[j], acc[i][j]);
           if constexpr (kSwiGLU) acc3[i][j] = fmaf(af[i], bf3[j], acc3[i][j]);
         }
@@ -107,8 +108,8 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
     const int r = row0 + ty * TM + i;
     if (r >= seg_end) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int col = n0 + tx * 4 + j;
+    for (int j = 0; j < TN; ++j) {
+      const int col = n0 + tx * TN + j;
       if (col >= a.N) continue;
       float v = acc[i][j];
       if constexpr (EPI == kEpiSwiGLU) {
