@@ -65,15 +65,19 @@ __device__ void scan_offsets(const RouterArgs& a, int nchunks) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (nchunks + NTH - 1) / NTH;
   const int c0 = min(tid * per, nchunks), c1 = min(c0 + per, nchunks);
-  int sum[kMaxE];
+  int sum[kMaxE], first[kMaxE];  // first: the counts of chunk c0, kept for the second pass
 #pragma unroll
-  for (int e = 0; e < kMaxE; ++e) sum[e] = 0;
+  for (int e = 0; e < kMaxE; ++e) sum[e] = first[e] = 0;
   for (int c = c0; c < c1; ++c) {
     int v[kMaxE];
 #pragma unroll
     for (int e = 0; e < kMaxE; ++e) v[e] = e < E ? __ldcg(&a.hist[(size_t)c * E + e]) : 0;
 #pragma unroll
     for (int e = 0; e < kMaxE; ++e) sum[e] += v[e];
+    if (c == c0) {
+#pragma unroll
+      for (int e = 0; e < kMaxE; ++e) first[e] = v[e];
+    }
   }
   int excl[kMaxE];
 #pragma unroll
@@ -125,7 +129,7 @@ __device__ void scan_offsets(const RouterArgs& a, int nchunks) {
   for (int c = c0; c < c1; ++c) {
     int v[kMaxE];
 #pragma unroll
-    for (int e = 0; e < kMaxE; ++e) v[e] = e < E ? __ldcg(&a.hist[(size_t)c * E + e]) : 0;
+    for (int e = 0; e < kMaxE; ++e) v[e] = c == c0 ? first[e] : (e < E ? __ldcg(&a.hist[(size_t)c * E + e]) : 0);
 #pragma unroll
     for (int e = 0; e < kMaxE; ++e)
       if (e < E) {
@@ -141,22 +145,34 @@ __device__ void scan_offsets(const RouterArgs& a, int nchunks) {
 __device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[kMaxSlots], int valid, int chunk_t0,
                              int chunk = blockIdx.x, int nchunks = gridDim.x) {
   __shared__ int s_last;
+  // The chunk's (token, slot) entries in token-major order, one per thread of the first warps.  An
+  // entry's rank is the number of earlier entries naming its expert (no token names an expert twice,
+  // so these are the earlier tokens' rows of that expert): the warp's equal-expert lanes below it,
+  // plus the earlier warps' counts of that expert.
+  __shared__ int s_wcnt[kMaxSlots][kMaxE];  // entries of warp w naming expert e
   const int Ex = a.Ex, S = a.S;
-  if (threadIdx.x < S * kRouterChunk) {
-    const int tt = threadIdx.x / S, s = threadIdx.x - tt * S;
-    if (tt < valid) {
-      const int e = s_idx[tt][s];
-      int r = 0;
-      for (int u = 0; u < tt; ++u)
-        for (int q = 0; q < S; ++q) r += (s_idx[u][q] == e);
-      a.rank[(size_t)S * (chunk_t0 + tt) + s] = r;
-    }
+  const int n = valid * S, nw = (n + 31) >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int e_ent = -1;
+  unsigned same = 0;
+  if (warp < nw) {
+    const int i = threadIdx.x;
+    e_ent = i < n ? s_idx[i / S][i - (i / S) * S] : -1;
+    same = __match_any_sync(0xffffffffu, e_ent);
+    if (lane < Ex) s_wcnt[warp][lane] = 0;
+    __syncwarp();
+    if (e_ent >= 0 && (same & ((1u << lane) - 1u)) == 0) s_wcnt[warp][e_ent] = __popc(same);
+  }
+  __syncthreads();
+  if (e_ent >= 0) {
+    int r = __popc(same & ((1u << lane) - 1u));
+    for (int w = 0; w < warp; ++w) r += s_wcnt[w][e_ent];
+    a.rank[(size_t)S * chunk_t0 + threadIdx.x] = r;
   }
   __shared__ int s_cnt[kMaxE];
   if (threadIdx.x < Ex) {
     int c = 0;
-    for (int u = 0; u < valid; ++u)
-      for (int q = 0; q < S; ++q) c += (s_idx[u][q] == (int)threadIdx.x);
+    for (int w = 0; w < nw; ++w) c += s_wcnt[w][threadIdx.x];
     if (nchunks > 1)
       a.hist[(size_t)chunk * Ex + threadIdx.x] = c;
     else
@@ -624,17 +640,25 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_split_kernel(RouterA
   __syncthreads();
   if (!s_lastsplit) return;
   __threadfence();
+  // every thread sums (row, expert) logits over the splits in split order, into s_part's space
+  float(*s_logit)[EMAX] = reinterpret_cast<float(*)[EMAX]>(&s_part[0][0][0]);
+  const float* base = a.split_part + (size_t)chunk * kRsSplit * kRouterChunk * EMAX;
+  for (int i = threadIdx.x; i < kRouterChunk * EMAX; i += blockDim.x) {
+    float p[kRsSplit];
+#pragma unroll
+    for (int sp = 0; sp < kRsSplit; ++sp) p[sp] = __ldcg(base + (size_t)sp * kRouterChunk * EMAX + i);
+    float v = p[0];
+#pragma unroll
+    for (int sp = 1; sp < kRsSplit; ++sp) v += p[sp];
+    const int e = i % EMAX;
+    s_logit[i / EMAX][e] = v + ((a.b_router != nullptr && e < E) ? a.b_router[e] : 0.f);
+  }
+  __syncthreads();
   if (threadIdx.x < kRouterChunk) {
-    const int t = chunk_t0 + threadIdx.x;
-    const float* base = a.split_part + (size_t)chunk * kRsSplit * kRouterChunk * EMAX + threadIdx.x * EMAX;
     float L[EMAX];
 #pragma unroll
-    for (int e = 0; e < EMAX; ++e) {
-      float v = __ldcg(base + e);
-      for (int sp = 1; sp < kRsSplit; ++sp) v += __ldcg(base + (size_t)sp * kRouterChunk * EMAX + e);
-      L[e] = v + ((a.b_router != nullptr && e < E) ? a.b_router[e] : 0.f);
-    }
-    topk_store<EMAX>(a, L, t, s_idx[threadIdx.x]);
+    for (int e = 0; e < EMAX; ++e) L[e] = s_logit[threadIdx.x][e];
+    topk_store<EMAX>(a, L, chunk_t0 + threadIdx.x, s_idx[threadIdx.x]);
   }
   __syncthreads();
   finish_chunk(a, s_idx, valid, chunk_t0, chunk, nchunks);
