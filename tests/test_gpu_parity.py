@@ -118,11 +118,13 @@ def test_small_bf16_swiglu(T):
     _full_check(li)
 
 
-@pytest.mark.parametrize("T,d", [(1040, 512), (1057, 512), (1100, 1024), (1100, 768)])
+@pytest.mark.parametrize("T,d", [(1040, 512), (1057, 512), (1100, 1024), (1100, 768), (1100, 4096), (1500, 3584),
+                                 (5000, 1536)])
 def test_tma_router_ragged_last_chunk(T, d):
     """Batches of >= 1024 tokens with d a multiple of 512 stream x into the router by TMA: a last
-    chunk of 16, 17 or 12 valid rows (rows past T read as zeros), and a d that is not a multiple of
-    512 (the global-load router instead) must all route exactly as the oracle."""
+    chunk of 16, 1, 12, 28 or 8 valid rows (rows past T read as zeros), and a d that is not a multiple
+    of 512 (the global-load router instead) must all route exactly as the oracle; d = 4096 and 3584
+    wrap around the three-stage ring several times, T = 5000 has more chunks than the GPU has SMs."""
     shape = testgen.LayerShape("tma-router", T, d, 256, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True)
     _full_check(testgen.make_inputs(shape))
 
