@@ -273,6 +273,21 @@ __device__ __forceinline__ void topk_store(const RouterArgs& a, const float (&L)
   }
 }
 
+// The warps' partial logit tiles (warp w holds half w % H of the chunk's rows over hidden slice
+// w / H) summed in slice order, plus the router bias, for the first nrows rows: every thread takes
+// some (row, expert) sums, then a __syncthreads().
+template <int EMAX>
+__device__ __forceinline__ void sum_slices(const RouterArgs& a, const float (*s_part)[16][EMAX],
+                                           float (*s_logit)[EMAX], int H, int S, int nrows) {
+  for (int i = threadIdx.x; i < nrows * EMAX; i += blockDim.x) {
+    const int r = i / EMAX, e = i - r * EMAX, hh = r >> 4, rr = r & 15;
+    float v = s_part[hh][rr][e];
+    for (int w = 1; w < S; ++w) v += s_part[hh + w * H][rr][e];
+    s_logit[r][e] = v + ((a.b_router != nullptr && e < a.E) ? a.b_router[e] : 0.f);
+  }
+  __syncthreads();
+}
+
 // Fused combine: the down projection adds both expert outputs into out, so this CTA's token rows
 // start at zero.  Issued before the logits work, the stores drain while the loads wait on memory.
 __device__ __forceinline__ void zero_out_rows(const RouterArgs& a, int chunk_t0, int valid) {
@@ -511,18 +526,13 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_top2_mma_kernel(Rout
     s_part[warp][g + 8][nt * 8 + 2 * q + 1] = acc[nt][3];
   }
   __syncthreads();
-  if (threadIdx.x < kRouterChunk) {
-    const int tt = threadIdx.x, hh = tt >> 4, r = tt & 15;
-    if (tt < valid) {
-      float L[EMAX];
+  __shared__ float s_logit[kRouterChunk][EMAX];
+  sum_slices<EMAX>(a, s_part, s_logit, H, S, valid);
+  if (threadIdx.x < valid) {
+    float L[EMAX];
 #pragma unroll
-      for (int e = 0; e < EMAX; ++e) {
-        float v = s_part[hh][r][e];
-        for (int s2 = 1; s2 < S; ++s2) v += s_part[hh + s2 * H][r][e];
-        L[e] = v + ((a.b_router != nullptr && e < E) ? a.b_router[e] : 0.f);
-      }
-      topk_store<EMAX>(a, L, chunk_t0 + tt, s_idx[tt]);
-    }
+    for (int e = 0; e < EMAX; ++e) L[e] = s_logit[threadIdx.x][e];
+    topk_store<EMAX>(a, L, chunk_t0 + threadIdx.x, s_idx[threadIdx.x]);
   }
   __syncthreads();
   finish_chunk(a, s_idx, valid, chunk_t0);
@@ -835,16 +845,14 @@ __global__ void __launch_bounds__(kRouterThreads, 2)
     s_part[warp][g + 8][nt * 8 + 2 * q + 1] = acc[nt][3];
   }
   __syncthreads();
-  if (sl == 0 && lane < 16) {
-    const int t = chunk_t0 + 16 * h + lane;
+  // the summed logits go to the first ring slot: every stage has landed and been read
+  float(*s_logit)[EMAX] = reinterpret_cast<float(*)[EMAX]>(stg);
+  sum_slices<EMAX>(a, s_part, s_logit, H, S, 16 * H);
+  if (threadIdx.x < 16 * H) {
     float L[EMAX];
 #pragma unroll
-    for (int e = 0; e < EMAX; ++e) {
-      float v = s_part[h][lane][e];
-      for (int w = 1; w < S; ++w) v += s_part[h + w * H][lane][e];
-      L[e] = v + ((a.b_router != nullptr && e < E) ? a.b_router[e] : 0.f);
-    }
-    topk_store<EMAX>(a, L, t, s_idx[16 * h + lane]);
+    for (int e = 0; e < EMAX; ++e) L[e] = s_logit[threadIdx.x][e];
+    topk_store<EMAX>(a, L, chunk_t0 + threadIdx.x, s_idx[threadIdx.x]);
   }
   __syncthreads();
   finish_chunk(a, s_idx, valid, chunk_t0);
