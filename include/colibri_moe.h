@@ -172,8 +172,9 @@ COLIBRI_API int colibri_moe_debug_buffer(colibri_moe_t* ctx, int32_t which, void
  * (the combine, when fused into the down GEMM). */
 COLIBRI_API int colibri_moe_num_stages(const colibri_moe_t* ctx, int32_t* n_stages);
 
-/* *n = the number of kernels the most recent forward (or forward_host) enqueued: 4 on the bf16
- * prefill path with the combine fused into the down GEMM, 5 with a separate combine, 2 on the
+/* *n = the number of kernels the most recent forward (or forward_host) enqueued: 4 on the grouped
+ * GEMM path (bf16 prefill or fp32) with the combine fused into the down GEMM (two slots, fp32
+ * output), 5 with a separate combine, 2 on the
  * decode path (by default T <= 128 for experts of at least 2^25 weights per matrix, else T <= 64:
  * the router and one cooperative kernel), 6 on the separate
  * decode kernels (COLIBRI_MOE_DECODE_FUSED=0, T <= 64); 0 before the first forward and after a

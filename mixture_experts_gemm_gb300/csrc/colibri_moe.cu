@@ -191,7 +191,8 @@ int check_config(const colibri_moe_config_t* c) {
   return COLIBRI_OK;
 }
 
-// Two-slot fp32 layers fuse the combine into the down GEMM unless COLIBRI_MOE_FUSED_COMBINE=0.
+// Layers with two slots and an fp32 output fuse the combine into the down GEMM (tcgen05 or SIMT)
+// unless COLIBRI_MOE_FUSED_COMBINE=0.
 bool env_fuse_combine() {
   const char* s = std::getenv("COLIBRI_MOE_FUSED_COMBINE");
   return !(s && s[0] == '0');
@@ -567,7 +568,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   // (cleared first); two fp32 additions onto zero give the same value in either order.
   // (the separate decode kernels serve up to kDecodeSepMaxT tokens, the cooperative kernel more)
   const bool decode = bf16 && T <= ctx->decode_max_t && (ctx->decode_fused || T <= kDecodeSepMaxT);
-  const bool fuse = bf16 && !decode && ctx->fuse_combine && ctx->S == 2 && c.out_dtype == COLIBRI_DTYPE_F32;
+  const bool fuse = !decode && ctx->fuse_combine && ctx->S == 2 && c.out_dtype == COLIBRI_DTYPE_F32;
   // bf16 prefill: the up GEMM gathers its A rows from x through token_of_row instead of reading a
   // materialised Xp; the dispatch kernel then only writes the row bookkeeping.
   const bool gather_a = bf16 && !decode && ctx->gather_a;
@@ -578,12 +579,14 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
                             make_tmap(&tm_xt, x, d, static_cast<uint64_t>(T), static_cast<uint32_t>((T + 15) / 16 * 16));
   mark(0);
   // With the combine fused, out is cleared before the down GEMM adds into it: by extra warps of the
-  // (tensor-bound) up GEMM, or by the router on the gathered-A path whose extra warps gather.
+  // (tensor-bound) up GEMM, or by the router on the gathered-A path whose extra warps gather and on
+  // the fp32 (SIMT) path.
   float4* const clear_in_gemm = fuse && !gather_a ? static_cast<float4*>(out) : nullptr;
   const int64_t out_vec4 = static_cast<int64_t>(T) * d / 4;
   RouterArgs ra{x, ctx->w_router, ctx->b_router, T, d, c.num_experts, ctx->dchunk, ctx->idx, ctx->gate,
                 ctx->row_of, ctx->hist, ctx->sched, ctx->k, c.gate_mode, c.has_shared_expert, ctx->S, ctx->Ex,
-                fuse && gather_a ? static_cast<float*>(out) : nullptr, ctx->tile_done, d / 128, ctx->split_part};
+                fuse && (gather_a || !bf16) ? static_cast<float*>(out) : nullptr, ctx->tile_done, d / 128,
+                ctx->split_part};
   // large bf16 batches stream x into the router through shared memory by TMA (a per-call map of the
   // caller's buffer); small ones read it straight from global memory
   CUtensorMap tm_xr;
@@ -692,7 +695,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
       return COLIBRI_ERR_CUDA;
     mark(3);
     SimtGemmArgs dn{ctx->sched, E, f, d, static_cast<const float*>(ctx->h), static_cast<const float*>(ctx->w2),
-                    nullptr, ctx->b2, ctx->y};
+                    nullptr, ctx->b2, ctx->y, ctx->tok_of_row, ctx->gate_of_row, fuse ? static_cast<float*>(out) : nullptr};
     if (launch_simt_gemm(kEpiStoreF32, dn, static_cast<int>(max_mtiles), s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   }
   mark(4);

@@ -8,7 +8,9 @@
 // the FMAs (these layers are small: latency, not FMA throughput, sets their time).  Each expert is
 // an affine layer out = in W^T (+ b) with W stored [out, in] (hnwysp.cn/news/30485 3.2), two layers per expert
 // W1 | b1 | W2 | b2 (m.nxbn.cn/news/48047 3.1), the activation applied in the epilogue
-// (m.nxbn.cn 2.1: matmul and activation fused per expert).
+// (m.nxbn.cn 2.1: matmul and activation fused per expert).  With two slots and an fp32 output the
+// down projection's epilogue also does the combine (m.nxbn.cn 3.3): g * y added onto the cleared
+// output row of the row's token.
 #include "moe_internal.cuh"
 
 namespace colibri {
@@ -118,6 +120,10 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
         v = fmaxf(v + a.bias[(size_t)e * a.N + col], 0.f);
       } else {
         if (a.bias) v += a.bias[(size_t)e * a.N + col];
+        if (a.comb_out) {  // two slots added onto zero: the sum is the same in either order
+          atomicAdd(&a.comb_out[(size_t)a.token_of_row[r] * a.N + col], __fmul_rn(a.gate_of_row[r], v));
+          continue;
+        }
       }
       a.out[(size_t)r * a.N + col] = v;
     }

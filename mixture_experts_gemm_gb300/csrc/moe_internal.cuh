@@ -204,6 +204,11 @@ struct SimtGemmArgs {
   const float* b3;          // [E * N, K]  W_up for SwiGLU, else nullptr
   const float* bias;        // [E, N] or nullptr
   float* out;               // [rows, N]
+  // fused combine (store epilogue, two slots, fp32 out): comb_out[token_of_row[r]] += gate_of_row[r] * y[r]
+  // onto rows the router cleared, instead of writing out
+  const int* token_of_row = nullptr;
+  const float* gate_of_row = nullptr;
+  float* comb_out = nullptr;
 };
 
 // Programmatic dependent launch: a kernel launched with pdl_launch may start (and run its prologue)

@@ -351,6 +351,20 @@ def test_fused_combine_equals_separate_combine(gemm, monkeypatch):
     assert np.array_equal(out_f, out_s)
 
 
+@pytest.mark.parametrize("T", [64, 1000])
+def test_fused_combine_fp32_simt_equals_separate_combine(T, monkeypatch):
+    """fp32 layers (SIMT GEMMs), two slots: the router clears the output and the down GEMM's epilogue
+    adds g*y into it, bit for bit the separate combine kernel's result; 4 launches instead of 5."""
+    shape = testgen.LayerShape("fused-fp32", T, 256, 512, 4, testgen.ACT_RELU_BIAS, "f32", zipf_router_bias=True)
+    li = testgen.make_inputs(shape)
+    layer, out_f, _, _, _ = _full_check(li)
+    assert layer.last_kernel_count() == 4
+    monkeypatch.setenv("COLIBRI_MOE_FUSED_COMBINE", "0")
+    layer2, out_s, _, _, _ = _full_check(li)
+    assert layer2.last_kernel_count() == 5
+    assert np.array_equal(out_f, out_s)
+
+
 @pytest.mark.parametrize("gemm", ["2sm", "1sm"])
 def test_gathered_a_rows_equal_copied_xp(gemm, monkeypatch):
     """The up GEMM reading its A rows from x through token_of_row (cp.async gather warps) multiplies the same
