@@ -3,9 +3,10 @@
 // tcgen05 has no fp32-input kind and TF32 (10-bit mantissa) cannot hold fp32 parity, so fp32
 // layers run here: one CTA per (expert, 32-row slice of a 128-row tile, 32-column tile), 256
 // threads with a 2x2 register tile each (slices past the expert's rows exit at once, so the work
-// follows the real row count), K staged through shared memory 32 at a time; the global loads of the next K
-// slab are issued into registers before the current slab is multiplied, so their latency overlaps
-// the FMAs (these layers are small: latency, not FMA throughput, sets their time).  Each expert is
+// follows the real row count), K staged through shared memory 32 at a time by cp.async in a ring of
+// three to five slabs, so several slabs' load latencies overlap each other and the FMAs (these layers
+// are small: latency, not FMA throughput, sets their time).  Every output sums its products in
+// ascending k, as a plain loop would.  Each expert is
 // an affine layer out = in W^T (+ b) with W stored [out, in] (hnwysp.cn/news/30485 3.2), two layers per expert
 // W1 | b1 | W2 | b2 (m.nxbn.cn/news/48047 3.1), the activation applied in the epilogue
 // (m.nxbn.cn 2.1: matmul and activation fused per expert).  With two slots and an fp32 output the
@@ -17,17 +18,28 @@ namespace colibri {
 namespace {
 
 constexpr int SBM = 32, SBN = 32, SBK = 32;
+constexpr int SLD = SBK + 1;             // shared row stride in words: a warp's column reads hit 16 banks
 constexpr int kSlices = kRowTile / SBM;  // row slices per 128-row tile
 constexpr int TM = SBM / 16;             // rows per thread
 constexpr int TN = SBN / 16;             // columns per thread
 constexpr int kLoadsA = SBM * SBK / 256, kLoadsB = SBN * SBK / 256;  // per thread per K slab
 
+// 4-byte asynchronous copy global -> shared; an invalid element is zero-filled (no bytes read)
+__device__ __forceinline__ void cp_async4(float* dst, const float* src, bool valid) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(src), "r"(valid ? 4 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 template <int EPI>
 __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
   constexpr bool kSwiGLU = EPI == kEpiSwiGLU;
-  __shared__ float As[SBK][SBM + 4];
-  __shared__ float Bs[SBK][SBN + 4];
-  __shared__ float B3s[kSwiGLU ? SBK : 1][SBN + 4];
+  constexpr int NS = kSwiGLU ? 3 : 5;  // K slabs in flight (shared memory stays under 48 KB)
+  constexpr int NB = kSwiGLU ? 2 : 1;  // weight tiles per slab (gate and up for SwiGLU)
+  __shared__ float As[NS][SBM][SLD];
+  __shared__ float Bs[NS][NB][SBN][SLD];
   const Sched* sc = a.sched;
   const int n_tiles = (a.N + SBN - 1) / SBN;
   const int tile = blockIdx.x / kSlices, slice = blockIdx.x % kSlices;
@@ -54,46 +66,48 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
 #pragma unroll
     for (int j = 0; j < TN; ++j) acc[i][j] = acc3[i][j] = 0.f;
 
-  float ra[kLoadsA], rb[kLoadsB], rb3[kSwiGLU ? kLoadsB : 1];
-  auto load_slab = [&](int k0) {
+  // slab ks (K columns ks*SBK ...) into ring slot st, rows as stored (no transpose); a warp writes
+  // 32 consecutive words of one row
+  auto load_slab = [&](int st, int k0) {
 #pragma unroll
     for (int i = 0; i < kLoadsA; ++i) {
       const int id = tid + i * 256, r = id / SBK, k = id % SBK;
-      ra[i] = (k0 + k < a.K) ? A[(size_t)(row0 + r) * a.K + k0 + k] : 0.f;
+      const bool in = k0 + k < a.K;
+      cp_async4(&As[st][r][k], in ? A + (size_t)(row0 + r) * a.K + k0 + k : A, in);
     }
 #pragma unroll
     for (int i = 0; i < kLoadsB; ++i) {
       const int id = tid + i * 256, c = id / SBK, k = id % SBK;
       const bool in = (n0 + c < a.N) && (k0 + k < a.K);
-      rb[i] = in ? B[(size_t)(n0 + c) * a.K + k0 + k] : 0.f;
-      if constexpr (kSwiGLU) rb3[i] = in ? B3[(size_t)(n0 + c) * a.K + k0 + k] : 0.f;
+      const size_t off = (size_t)(n0 + c) * a.K + k0 + k;
+      cp_async4(&Bs[st][0][c][k], in ? B + off : B, in);
+      if constexpr (kSwiGLU) cp_async4(&Bs[st][NB - 1][c][k], in ? B3 + off : B3, in);
     }
   };
-  load_slab(0);
-  for (int k0 = 0; k0 < a.K; k0 += SBK) {
-    __syncthreads();  // every thread is done with the previous slab
+  const int nslab = (a.K + SBK - 1) / SBK;
 #pragma unroll
-    for (int i = 0; i < kLoadsA; ++i) {
-      const int id = tid + i * 256;
-      As[id % SBK][id / SBK] = ra[i];
+  for (int st = 0; st < NS - 1; ++st) {
+    if (st < nslab) load_slab(st, st * SBK);
+    cp_async_commit();
+  }
+  for (int ks = 0; ks < nslab; ++ks) {
+    cp_async_wait<NS - 2>();  // this thread's copies of slab ks have landed
+    __syncthreads();          // everyone's have, and every thread is done with slab ks - 1's slot
+    {
+      const int nx = ks + NS - 1;
+      if (nx < nslab) load_slab(nx % NS, nx * SBK);
+      cp_async_commit();
     }
-#pragma unroll
-    for (int i = 0; i < kLoadsB; ++i) {
-      const int id = tid + i * 256;
-      Bs[id % SBK][id / SBK] = rb[i];
-      if constexpr (kSwiGLU) B3s[id % SBK][id / SBK] = rb3[i];
-    }
-    __syncthreads();
-    if (k0 + SBK < a.K) load_slab(k0 + SBK);  // in flight while this slab is multiplied
+    const int st = ks % NS;
 #pragma unroll
     for (int kk = 0; kk < SBK; ++kk) {
       float af[TM], bf[TN], bf3[TN];
 #pragma unroll
-      for (int i = 0; i < TM; ++i) af[i] = As[kk][ty * TM + i];
+      for (int i = 0; i < TM; ++i) af[i] = As[st][ty * TM + i][kk];
 #pragma unroll
       for (int j = 0; j < TN; ++j) {
-        bf[j] = Bs[kk][tx * TN + j];
-        if constexpr (kSwiGLU) bf3[j] = B3s[kk][tx * TN + j];
+        bf[j] = Bs[st][0][tx * TN + j][kk];
+        if constexpr (kSwiGLU) bf3[j] = Bs[st][NB - 1][tx * TN + j][kk];
       }
 #pragma unroll
       for (int i = 0; i < TM; ++i)
@@ -104,6 +118,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
         }
     }
   }
+  cp_async_wait<0>();  // no copy in flight when the CTA leaves (the trailing groups are empty)
 
 #pragma unroll
   for (int i = 0; i < TM; ++i) {
