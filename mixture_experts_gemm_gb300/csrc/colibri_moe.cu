@@ -108,7 +108,7 @@ constexpr int kNumStages = 5;  // router, gather, up GEMM, down GEMM, combine
 // measured on GB300 at the Mixtral shape: T=1 2 us faster, T=4 even, T >= 16 slower.
 constexpr int kTileCombineMaxT = 4;
 constexpr int kRouterTmaMinT = 1024;  // batches from this size use the TMA-staged router
-constexpr int kRouterSplitMinT = 16;   // batches above this size (and up to 64) use the split router
+constexpr int kRouterSplitMinT = 16;   // batches above this size (up to 32 chunks: 1024 tokens) use the split router
 // (GB300: Mixtral-shaped router stage at T=32 23.2 -> 16.9 us split; T=16 equal; T=1 9.1 -> 10.5 us)
 
 struct DeviceGuard {
