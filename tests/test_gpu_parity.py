@@ -315,6 +315,16 @@ def test_routing_variants_and_shared_expert_bf16(T, k, mode, shared):
         assert np.array_equal(tok[off[-1]:off[-1] + T], np.arange(T))
 
 
+@pytest.mark.parametrize("T", [20, 500, 1100])
+def test_most_experts_top4_and_shared_expert(T):
+    """The limits at once: 16 routed experts + the shared one (17 scheduled), top-4, so 5 slots per
+    token and up to 160 (token, slot) entries per router chunk over 5 warps; one chunk (T=20, the
+    decode kernels), 16 chunks (the split router) and 35 chunks (the TMA-staged router)."""
+    shape = testgen.LayerShape("max-e16-k4-s", T, 512, 384, 16, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True,
+                               top_k=4, gate_mode=0, shared_expert=True)
+    _full_check(testgen.make_inputs(shape))
+
+
 @pytest.mark.parametrize("k,mode,shared", [(1, 0, True), (3, 1, True), (4, 0, False)])
 def test_routing_variants_fp32(k, mode, shared):
     shape = testgen.LayerShape("var-f32", 64, 256, 512, 4, testgen.ACT_RELU_BIAS, "f32", top_k=k, gate_mode=mode,
