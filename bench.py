@@ -292,6 +292,7 @@ def main():
         layer.forward_ptr(x.data_ptr(), out.data_ptr(), T, sh)
     torch.cuda.synchronize(dev)
     stage_ms = np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(n_st)] for evs in prof_sets])
+    step_ms_prof = np.array([evs[0].elapsed_time(evs[n_st]) for evs in prof_sets])
     dominant = int(np.argmax(stage_ms.mean(axis=0)))
 
     # 2) the timed region: K back-to-back forwards; events around the dominant kernel on every
@@ -419,6 +420,17 @@ def main():
         "roofline": roof,
         "stages_us": {n: float(v * 1e3) for n, v in zip(STAGES, mean_stage)},
         "stages_note": "stage split from a separate 50-step pass with an event at every stage boundary",
+        "spread_us": {
+            "step_p10": float(np.percentile(step_ms_prof, 10) * 1e3),
+            "step_p50": float(np.percentile(step_ms_prof, 50) * 1e3),
+            "step_p90": float(np.percentile(step_ms_prof, 90) * 1e3),
+            "dominant_p10": float(np.percentile(dom_ms, 10) * 1e3),
+            "dominant_p50": float(np.percentile(dom_ms, 50) * 1e3),
+            "dominant_p90": float(np.percentile(dom_ms, 90) * 1e3),
+            "note": "step: per-step times of the stage pass, whose events end the programmatic-launch overlap "
+                    "between kernels, so they run above ms_per_step (by a few microseconds per kernel: about "
+                    "1 % at the Mixtral prefill, up to half on the smallest layer); dominant: the kernel timed "
+                    "for the roofline, inside the timed region"},
         "e2e": e2e,
         "gpu_launches": args.steps * layer.last_kernel_count(),
         "clocks": clk,

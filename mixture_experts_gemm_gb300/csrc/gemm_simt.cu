@@ -18,16 +18,18 @@ namespace colibri {
 namespace {
 
 constexpr int SBM = 32, SBN = 32, SBK = 32;
-constexpr int SLD = SBK + 1;             // shared row stride in words: a warp's column reads hit 16 banks
+// Shared rows of 36 words: 16-byte aligned for the 16-byte copies and loads, and the 16-byte column
+// reads of 8 consecutive rows (a quarter warp) land in 8 different 16-byte bank groups.
+constexpr int SLD = SBK + 4;
 constexpr int kSlices = kRowTile / SBM;  // row slices per 128-row tile
-constexpr int TM = SBM / 16;             // rows per thread
-constexpr int TN = SBN / 16;             // columns per thread
-constexpr int kLoadsA = SBM * SBK / 256, kLoadsB = SBN * SBK / 256;  // per thread per K slab
+constexpr int TM = SBM / 16;             // rows per thread: ty * TM + i
+constexpr int TN = SBN / 16;             // columns per thread: tx + 16 * j
+static_assert(SBM * SBK / 4 == 256 && SBN * SBK / 4 == 256, "one 16-byte copy per thread and tile");
 
-// 4-byte asynchronous copy global -> shared; an invalid element is zero-filled (no bytes read)
-__device__ __forceinline__ void cp_async4(float* dst, const float* src, bool valid) {
+// 16-byte asynchronous copy global -> shared; an invalid piece is zero-filled (no bytes read)
+__device__ __forceinline__ void cp_async16(float* dst, const float* src, bool valid) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(src), "r"(valid ? 4 : 0) : "memory");
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -38,8 +40,8 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
   constexpr bool kSwiGLU = EPI == kEpiSwiGLU;
   constexpr int NS = kSwiGLU ? 3 : 5;  // K slabs in flight (shared memory stays under 48 KB)
   constexpr int NB = kSwiGLU ? 2 : 1;  // weight tiles per slab (gate and up for SwiGLU)
-  __shared__ float As[NS][SBM][SLD];
-  __shared__ float Bs[NS][NB][SBN][SLD];
+  __shared__ __align__(16) float As[NS][SBM][SLD];
+  __shared__ __align__(16) float Bs[NS][NB][SBN][SLD];
   const Sched* sc = a.sched;
   const int n_tiles = (a.N + SBN - 1) / SBN;
   const int tile = blockIdx.x / kSlices, slice = blockIdx.x % kSlices;
@@ -66,23 +68,17 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
 #pragma unroll
     for (int j = 0; j < TN; ++j) acc[i][j] = acc3[i][j] = 0.f;
 
-  // slab ks (K columns ks*SBK ...) into ring slot st, rows as stored (no transpose); a warp writes
-  // 32 consecutive words of one row
+  // slab ks (K columns k0 = ks*SBK ...) into ring slot st, rows as stored (no transpose): thread tid
+  // copies 4 consecutive k of row tid / 8 of each tile (K is a multiple of 8, so a piece is wholly
+  // inside or wholly past K)
   auto load_slab = [&](int st, int k0) {
-#pragma unroll
-    for (int i = 0; i < kLoadsA; ++i) {
-      const int id = tid + i * 256, r = id / SBK, k = id % SBK;
-      const bool in = k0 + k < a.K;
-      cp_async4(&As[st][r][k], in ? A + (size_t)(row0 + r) * a.K + k0 + k : A, in);
-    }
-#pragma unroll
-    for (int i = 0; i < kLoadsB; ++i) {
-      const int id = tid + i * 256, c = id / SBK, k = id % SBK;
-      const bool in = (n0 + c < a.N) && (k0 + k < a.K);
-      const size_t off = (size_t)(n0 + c) * a.K + k0 + k;
-      cp_async4(&Bs[st][0][c][k], in ? B + off : B, in);
-      if constexpr (kSwiGLU) cp_async4(&Bs[st][NB - 1][c][k], in ? B3 + off : B3, in);
-    }
+    const int r = tid >> 3, k = (tid & 7) * 4;
+    const bool ink = k0 + k < a.K;
+    cp_async16(&As[st][r][k], ink ? A + (size_t)(row0 + r) * a.K + k0 + k : A, ink);
+    const bool in = ink && n0 + r < a.N;
+    const size_t off = (size_t)(n0 + r) * a.K + k0 + k;
+    cp_async16(&Bs[st][0][r][k], in ? B + off : B, in);
+    if constexpr (kSwiGLU) cp_async16(&Bs[st][NB - 1][r][k], in ? B3 + off : B3, in);
   };
   const int nslab = (a.K + SBK - 1) / SBK;
 #pragma unroll
@@ -100,21 +96,29 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
     }
     const int st = ks % NS;
 #pragma unroll
-    for (int kk = 0; kk < SBK; ++kk) {
-      float af[TM], bf[TN], bf3[TN];
+    for (int k4 = 0; k4 < SBK; k4 += 4) {  // four k per 16-byte load, taken in ascending k
+      float4 af[TM], bf[TN], bf3[TN];
 #pragma unroll
-      for (int i = 0; i < TM; ++i) af[i] = As[st][ty * TM + i][kk];
+      for (int i = 0; i < TM; ++i) af[i] = *reinterpret_cast<const float4*>(&As[st][ty * TM + i][k4]);
 #pragma unroll
       for (int j = 0; j < TN; ++j) {
-        bf[j] = Bs[st][0][tx * TN + j][kk];
-        if constexpr (kSwiGLU) bf3[j] = Bs[st][NB - 1][tx * TN + j][kk];
+        bf[j] = *reinterpret_cast<const float4*>(&Bs[st][0][tx + 16 * j][k4]);
+        if constexpr (kSwiGLU) bf3[j] = *reinterpret_cast<const float4*>(&Bs[st][NB - 1][tx + 16 * j][k4]);
       }
 #pragma unroll
       for (int i = 0; i < TM; ++i)
 #pragma unroll
         for (int j = 0; j < TN; ++j) {
-          acc[i][j] = fmaf(af[i], bf[j], acc[i][j]);
-          if constexpr (kSwiGLU) acc3[i][j] = fmaf(af[i], bf3[j], acc3[i][j]);
+          acc[i][j] = fmaf(af[i].x, bf[j].x, acc[i][j]);
+          acc[i][j] = fmaf(af[i].y, bf[j].y, acc[i][j]);
+          acc[i][j] = fmaf(af[i].z, bf[j].z, acc[i][j]);
+          acc[i][j] = fmaf(af[i].w, bf[j].w, acc[i][j]);
+          if constexpr (kSwiGLU) {
+            acc3[i][j] = fmaf(af[i].x, bf3[j].x, acc3[i][j]);
+            acc3[i][j] = fmaf(af[i].y, bf3[j].y, acc3[i][j]);
+            acc3[i][j] = fmaf(af[i].z, bf3[j].z, acc3[i][j]);
+            acc3[i][j] = fmaf(af[i].w, bf3[j].w, acc3[i][j]);
+          }
         }
     }
   }
@@ -126,7 +130,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs a) {
     if (r >= seg_end) continue;
 #pragma unroll
     for (int j = 0; j < TN; ++j) {
-      const int col = n0 + tx * TN + j;
+      const int col = n0 + tx + 16 * j;
       if (col >= a.N) continue;
       float v = acc[i][j];
       if constexpr (EPI == kEpiSwiGLU) {
