@@ -361,7 +361,7 @@ def test_fused_combine_equals_separate_combine(gemm, monkeypatch):
     assert np.array_equal(out_f, out_s)
 
 
-@pytest.mark.parametrize("T", [64, 1000])
+@pytest.mark.parametrize("T", [20, 64, 1000, 3000])
 def test_fused_combine_fp32_simt_equals_separate_combine(T, monkeypatch):
     """fp32 layers (SIMT GEMMs), two slots: the router clears the output and the down GEMM's epilogue
     adds g*y into it, bit for bit the separate combine kernel's result; 4 launches instead of 5."""
