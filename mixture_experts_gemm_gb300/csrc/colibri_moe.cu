@@ -108,8 +108,9 @@ constexpr int kNumStages = 5;  // router, gather, up GEMM, down GEMM, combine
 // measured on GB300 at the Mixtral shape: T=1 2 us faster, T=4 even, T >= 16 slower.
 constexpr int kTileCombineMaxT = 4;
 constexpr int kRouterTmaMinT = 1024;  // batches from this size use the TMA-staged router
-constexpr int kRouterSplitMinT = 16;   // batches above this size (up to 32 chunks: 1024 tokens) use the split router
-// (GB300: Mixtral-shaped router stage at T=32 23.2 -> 16.9 us split; T=16 equal; T=1 9.1 -> 10.5 us)
+constexpr int kRouterSplitMinT = 8;    // batches above this size (up to 32 chunks: 1024 tokens) use the split router
+// (GB300, Mixtral-shaped decode steps: T=32 router stage 23.2 -> 16.9 us split; with the warp-match
+// tail, T=16 432.7 -> 429.1 us per step split, T=1 and T=4 the same either way)
 
 struct DeviceGuard {
   int prev = -1;
@@ -591,7 +592,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   // caller's buffer); small ones read it straight from global memory
   CUtensorMap tm_xr;
   if (bf16 && T > kRouterSplitMinT && nchunks <= kRouterSplitMaxChunks && d % (32 * router_split_factor()) == 0) {
-    // 17..1024 tokens: the hidden dimension split over several CTAs per chunk (fewer tokens gain
+    // 9..1024 tokens: the hidden dimension split over several CTAs per chunk (fewer tokens gain
     // nothing from it: one CTA's loads already take one or two rounds; more fill the GPU anyway)
     if (launch_router_split(ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   } else if (bf16 && T >= kRouterTmaMinT && d % router_tma_cols() == 0 &&

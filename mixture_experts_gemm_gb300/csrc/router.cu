@@ -12,7 +12,7 @@
 //   router_top2_kernel      fp32 (and bf16 with d not a multiple of 32): FMA dot products, W_r
 //                           staged in shared memory, each warp streaming 4 token rows;
 //   router_top2_mma_kernel  bf16: mma.sync logits with fragments loaded straight from x;
-//   router_split_kernel     bf16, 17..1024 tokens: d split over 8 CTAs per chunk;
+//   router_split_kernel     bf16, 9..1024 tokens: d split over 8 CTAs per chunk;
 //   router_tma_kernel       bf16, >= 1024 tokens: x staged through shared memory by TMA.
 // Per-chunk histograms make the dispatch deterministic: atomics only count finished CTAs, and every
 // row index comes from a scan in token order.
