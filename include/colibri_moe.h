@@ -54,8 +54,9 @@ extern "C" {
 /* ---- status codes (m.nxbn.cn 5.1: -1 size exceeded, -2 out of memory, -3 corrupt weights) ---- */
 #define COLIBRI_OK 0
 #define COLIBRI_ERR_INVALID_ARG (-1)  /* NULL pointer, T < 0 or T > max_tokens, host pointer where a
-                                         device pointer is required, aliasing x/out, top_k != 2,
-                                         num_experts outside 2..16, bad enum value */
+                                         device pointer is required, aliasing x/out, top_k outside
+                                         1..4 or above num_experts, num_experts outside 2..16, bad
+                                         enum value */
 #define COLIBRI_ERR_OOM (-2)          /* a device allocation failed */
 #define COLIBRI_ERR_BAD_WEIGHTS (-3)  /* a required weight or bias pointer is NULL, or one is given
                                          that the activation does not use */
