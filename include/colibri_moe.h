@@ -164,9 +164,10 @@ COLIBRI_API int colibri_moe_get_routing(colibri_moe_t* ctx, int32_t* idx, float*
  *           2: Y, expert outputs before the combine [rows, d] (fp32);
  *           3: token_of_row [rows] (int32).
  * Only rows inside an expert's segment [offsets[e], offsets[e] + counts[e]) of the last forward
- * hold defined values; padding rows hold stale data.  Xp is not written by the cooperative decode kernel or
- * with COLIBRI_MOE_GATHER=fused (the GEMM reads x in place), Y not when the combine is fused into
- * the down GEMM.  *ptr receives the device address and *rows the allocated row count (may be NULL). */
+ * hold defined values; padding rows hold stale data.  Xp is not written by the cooperative decode
+ * kernel or with COLIBRI_MOE_GATHER=fused (the GEMM reads x in place), Y not when the combine is
+ * fused into the down GEMM.  *ptr receives the device address and *rows the allocated row count
+ * (may be NULL). */
 COLIBRI_API int colibri_moe_debug_buffer(colibri_moe_t* ctx, int32_t which, void** ptr, int64_t* rows);
 
 /* Number of timed pipeline stages of forward (router, dispatch, up GEMM, down GEMM, combine), for
