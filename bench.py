@@ -28,11 +28,16 @@ sys.path.insert(0, os.path.join(ROOT, "tests"))
 METRIC = "MoE-layer tokens/s at Mixtral-8x7B shape; % of bf16 tensor peak / HBM BW"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_BF16_TFLOPS = 2250.0  # GB300 dense bf16 tensor rate, datasheet (no sparsity)
+NOMINAL_HBM_GBS = 7900.0      # GB300 HBM3e, datasheet
+# a timed region shorter than this is a burst: the GPU has not yet settled at its power cap, so a
+# contraction is compared with the burst cuBLAS rate; longer regions with the sustained one
+SUSTAINED_AFTER_S = 1.0
 STAGES = ["router", "gather", "gemm_up", "gemm_down", "combine"]
 # (the cooperative decode kernel runs inside the "gemm_up" stage: up GEMM, activation, down GEMM and
 # combine in one launch, the other stages empty)
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture of the kernel as it now
-# stands (profiles/gemm_pair_mixtral_prefill.md); None where no capture of the current kernel exists.
+# stands; None where no capture of the current kernel exists.
 DOM_EVERY = 8  # the dominant kernel is timed with events on every 8th step of the timed region
 NCU_TRAFFIC = {("mixtral-prefill", 8192, "gemm_up", "2sm"): 2.619e9, ("mixtral-prefill", 8192, "gemm_down", "2sm"): 3.022e9,
                ("mixtral-decode", 1, "gemm_up", "decode"): 0.7092e9, ("mixtral-decode", 16, "gemm_up", "decode"): 2.8339e9,
@@ -57,6 +62,8 @@ def parse_args():
     p.add_argument("--top-k", type=int, default=None, help="routed experts per token (default: the workload's, 2)")
     p.add_argument("--gate-mode", type=int, default=None, help="0 softmax over the selected experts, 1 full softmax")
     p.add_argument("--shared-expert", action="store_true", help="add an always-on shared expert")
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip the decode sweep and the other workloads' step times that follow the main line")
     return p.parse_args()
 
 
@@ -221,6 +228,78 @@ def run_reference(args, shape, T):
 
 
 # ---------------------------------------------------------------------------------------- GPU arm
+def time_forwards(layer, x_ptr, out_ptr, T, stream, steps, warmup):
+    """ms per forward over `steps` back-to-back forwards, CUDA events on the launching stream."""
+    import torch
+    for _ in range(max(3, warmup)):
+        layer.forward_ptr(x_ptr, out_ptr, T, stream.cuda_stream)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        layer.forward_ptr(x_ptr, out_ptr, T, stream.cuda_stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def decode_sweep(layer, shape, x, out, stream, hbm_gbs, steps):
+    """The decode-shaped layer: the same weights, the first T rows of the batch, T in 1, 4, 16, 32.
+    HBM fraction over the bytes of the distinct experts the batch activates (each read once)."""
+    import testgen
+    res = {}
+    for Td in testgen.DECODE_TOKENS:
+        ms = time_forwards(layer, x.data_ptr(), out.data_ptr(), Td, stream, steps, 10)
+        counts = layer.get_routing(Td)["counts"].cpu().numpy()
+        active = int((counts > 0).sum())
+        wbytes = active * algorithmic(shape, Td)["w_bytes_expert"]
+        res[str(Td)] = {"us_per_step": ms * 1e3, "tokens_per_s": Td / (ms / 1e3), "active_experts": active,
+                        "weight_bytes": wbytes, "hbm_gbs": wbytes / (ms / 1e3) / 1e9,
+                        "hbm_frac": wbytes / (ms / 1e3) / 1e9 / hbm_gbs, "steps": steps,
+                        "kernels_per_step": layer.last_kernel_count()}
+    return res
+
+
+def other_workloads(peaks, steps, device):
+    """Step time of the benchmark's other layers (each with its own seeded weights), for the record."""
+    import torch
+    import testgen
+    from moe_check import host_weights, x_device
+    import mixture_experts_gemm_gb300 as moe
+    stream = torch.cuda.current_stream(device)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    res = {}
+    for name in ("tiny-moe-4e2r", "1.3b-8e", "skewed-16e"):
+        s = testgen.CONFIGS[name]
+        li = testgen.make_inputs(s, want_f32=s.dtype == "f32")
+        layer = moe.MoELayer(s.d_model, s.d_ff, s.num_experts, s.T, dtype=s.dtype,
+                             act="swiglu" if s.act == testgen.ACT_SWIGLU else "relu_bias",
+                             has_router_bias=s.zipf_router_bias, out_dtype="f32", device=device, top_k=s.top_k,
+                             gate_mode=s.gate_mode, shared_expert=s.shared_expert)
+        layer.load_weights(**host_weights(li))
+        x = x_device(li).to(device)
+        out = torch.empty((s.T, s.d_model), dtype=torch.float32, device=device)
+        ms = time_forwards(layer, x.data_ptr(), out.data_ptr(), s.T, stream, steps, 10)
+        counts = layer.get_routing(s.T)["counts"].cpu().numpy()
+        alg = algorithmic(s, s.T, int((counts > 0).sum()))
+        sec = ms / 1e3
+        r = {"workload": workload_desc(s, s.T), "us_per_step": ms * 1e3, "tokens_per_s": s.T / sec,
+             "tflops": alg["flops"] / sec / 1e12, "steps": steps, "kernels_per_step": layer.last_kernel_count()}
+        if s.dtype == "bf16":
+            r["hbm_frac_over_weights"] = alg["bytes"] / sec / 1e9 / hbm
+            r["tensor_frac_of_burst"] = alg["flops"] / sec / 1e12 / burst
+            r["bound"] = "hbm" if alg["flops"] / alg["bytes"] < burst * 1e12 / (hbm * 1e9) else "tensor"
+        else:
+            r["bound"] = "latency (weights fit in L2; fp32 SIMT path)"
+        res[name] = r
+        layer.close()
+        del x, out
+        torch.cuda.empty_cache()
+    return res
+
+
 def main():
     args = parse_args()
     import dataclasses
@@ -328,7 +407,7 @@ def main():
 
     # end to end through the C ABI with host buffers (pinned): every step copies its x host->device,
     # runs the forward and copies out device->host; forward_host_async overlaps one step's copies
-    # with the neighbouring steps' forwards (two staging slots), host_sync ends the timed region
+    # with the neighbouring steps' forwards (three staging slots), host_sync ends the timed region
     e2e = None
     if not args.no_e2e:
         if shape.dtype == "bf16":
@@ -371,14 +450,24 @@ def main():
     if shape.dtype == "bf16" and tensor_bound and dominant in (2, 3):
         fl = alg["flops_up"] if dominant == 2 else alg["flops_down"]
         ach = fl / dur / 1e12
-        # timed inside a seconds-long loop of steps: the sustained (power-capped) peak applies
-        peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
         burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        # the peak that fits the timed region: the burst rate for a region shorter than a second (the
+        # GPU has not settled at its power cap yet), the sustained rate for a longer loop
+        region_s = ms_total / 1e3
+        long_region = region_s >= SUSTAINED_AFTER_S
+        peak = sustained if long_region else burst
         gemm = "1sm" if os.environ.get("COLIBRI_MOE_GEMM") == "1sm" else "2sm"
         roof = {"bound": "tensor", "kernel": STAGES[dominant], "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                 "frac": ach / peak, "traffic": NCU_TRAFFIC.get((shape.name, T, STAGES[dominant], gemm)),
-                "peak_source": f"{peak_src} bf16 sustained", "frac_of_burst": ach / burst,
-                "algorithmic_flops_per_launch": fl, "timing": timed_note}
+                "peak_source": (f"{peak_src} bf16 {'sustained' if long_region else 'burst'}: timed region "
+                                f"{region_s:.3f} s {'>=' if long_region else '<'} {SUSTAINED_AFTER_S:.0f} s"),
+                "frac_of_burst": ach / burst, "frac_of_sustained": ach / sustained,
+                "frac_of_nominal": ach / NOMINAL_BF16_TFLOPS,
+                "nominal_note": f"frac_of_nominal: against the {NOMINAL_BF16_TFLOPS:.0f} TFLOP/s dense bf16 datasheet rate",
+                "algorithmic_flops_per_launch": fl, "dominant_ms": dur * 1e3, "timing": timed_note,
+                "layer_tflops": alg["flops"] / (ms_per_step / 1e3) / 1e12,
+                "layer_frac": alg["flops"] / (ms_per_step / 1e3) / 1e12 / peak}
     else:
         # weight streaming: bytes of the distinct active experts' weights this stage reads
         n_up = 2 if shape.act == 1 else 1
@@ -395,10 +484,20 @@ def main():
         roof = {"bound": "hbm", "kernel": STAGES[dominant], "achieved": ach, "peak": peak, "unit": "GB/s",
                 "frac": ach / peak, "traffic": NCU_TRAFFIC.get((shape.name, T, STAGES[dominant], path)),
                 "peak_source": f"{peak_src} copy", "algorithmic_bytes_per_launch": byts,
+                "dominant_ms": dur * 1e3, "frac_of_nominal": ach / NOMINAL_HBM_GBS,
                 "step_frac_of_hbm": alg["bytes"] / (ms_per_step / 1e3) / 1e9 / peak, "timing": timed_note}
 
     roof["layer_flop_per_byte"] = alg["flops"] / alg["bytes"]
     roof["ridge_flop_per_byte"] = ridge
+
+    extra = {}
+    if not args.no_extra and world == 1 and args.impl == "ours":
+        peaks_x, _ = load_peaks()
+        n_x = max(50, min(args.steps, 200))
+        if shape.name == "mixtral-prefill" and shape.top_k == 2 and not shape.shared_expert and shape.gate_mode == 0:
+            extra["decode"] = decode_sweep(layer, shape, x, out, stream,
+                                           float(peaks_x.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])), n_x)
+        extra["workloads"] = other_workloads(peaks_x, n_x, dev)
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -427,16 +526,22 @@ def main():
             "dominant_p10": float(np.percentile(dom_ms, 10) * 1e3),
             "dominant_p50": float(np.percentile(dom_ms, 50) * 1e3),
             "dominant_p90": float(np.percentile(dom_ms, 90) * 1e3),
-            "note": "step: per-step times of the stage pass, whose events end the programmatic-launch overlap "
-                    "between kernels, so they run above ms_per_step (by a few microseconds per kernel: about "
-                    "1 % at the Mixtral prefill, up to half on the smallest layer); dominant: the kernel timed "
-                    "for the roofline, inside the timed region"},
+            "note": "step: per-step times of the stage pass (50 steps with an event at every stage boundary, "
+                    "which ends the programmatic-launch overlap between kernels: a few microseconds per kernel; "
+                    "it runs before the timed region, so at a cooler clock it can also come out below "
+                    "ms_per_step); dominant: the kernel timed for the roofline, inside the timed region"},
         "e2e": e2e,
         "gpu_launches": args.steps * layer.last_kernel_count(),
         "clocks": clk,
         "cpu_baseline": cpu,
         "device_status": status,
     }
+    if extra:
+        line["decode"] = extra.get("decode")
+        line["workloads"] = extra.get("workloads")
+        line["extra_note"] = ("decode: the Mixtral-shaped layer's weights on the first T rows of the batch, HBM "
+                              "fraction over the distinct active experts' weights; workloads: the other layers' "
+                              "step times; both timed after the main region, CUDA events around back-to-back steps")
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -150,8 +150,9 @@ COLIBRI_API int colibri_moe_forward_host_async(colibri_moe_t* ctx, const void* x
 /* Waits until every copy of earlier forward_host_async calls has completed. */
 COLIBRI_API int colibri_moe_host_sync(colibri_moe_t* ctx);
 
-/* Routing of the most recent forward, copied into caller DEVICE buffers on `stream` (any may be
- * NULL): idx[T,k] int32 (slot 0 = highest logit), gate[T,k] fp32, counts[E] int32 (routed
+/* Routing of the most recent forward -- the routing dump the articles' engine offers as a debug
+ * function to call after a forward (zskr.cn 5.2, colibri_dump_routing) -- copied into caller
+ * DEVICE buffers on `stream` (any may be NULL): idx[T,k] int32 (slot 0 = highest logit), gate[T,k] fp32, counts[E] int32 (routed
  * experts), offsets[E+1] int32 (row where each routed expert's segment starts; segments padded to
  * 128 rows; offsets[E] is where the shared expert's rows start when there is one), row_of[T,k]
  * int32 (row of token t's slot s; row_of - offsets[e] is t's rank among e's tokens). */
@@ -209,8 +210,12 @@ COLIBRI_API int colibri_moe_probe_wait_timeout(colibri_moe_t* ctx, int32_t timeo
  * cannot allocate device memory -- code that runs inside a host framework whose memory pool owns
  * the whole GPU, real-time loops where cudaMalloc's implicit synchronisation is not allowed, or
  * deployments with a fixed device-memory budget set at start-up).  It computes, from device
- * buffers on the CURRENT device, exactly what colibri_moe_get_routing reports after a forward of
- * the same x and router weights: idx[T,2], gate[T,2], counts[E], offsets[E+1], row_of[T,2].
+ * buffers on the CURRENT device, the routing colibri_moe_get_routing reports after a forward of
+ * the same x and router weights (top-2, gates summing to 1): idx[T,2], gate[T,2], counts[E],
+ * offsets[E+1], row_of[T,2].  Its router kernel may sum the logits in another order than the one
+ * forward picks for the same T, so the two agree on every token whose fp64 logit gaps (first to
+ * second and second to third expert) are at least 1e-5, with gates within 1e-5; a token closer to
+ * a tie may be routed either way (and counts, offsets and rows follow its choice).
  *   x [T, d_model] and w_router [E, d_model] in `dtype` (16-byte aligned), b_router [E] fp32 or NULL.
  * It needs no context.  Its scratch (per-chunk histograms and the routing summary) is a fixed
  * __device__ array of about 137 KB inside the library, present on every GPU that loads the library
@@ -219,16 +224,20 @@ COLIBRI_API int colibri_moe_probe_wait_timeout(colibri_moe_t* ctx, int32_t timeo
  * set-up, no allocation); make that first call before any stream capture.  Every call on a device
  * shares the one array, and each call clears the part that must start at zero: calls that overlap
  * on the GPU (different streams, or concurrent host threads) race and give wrong results.
- * Asynchronous on `stream`; it calls no cudaMalloc, cudaFree or allocating library routine. */
+ * Asynchronous on `stream`; it calls no cudaMalloc, cudaFree or allocating library routine.  It
+ * has no context and so no device status word: a bounded wait that gives up inside its router
+ * kernel is not reported (the routing it returns is then undefined). */
 COLIBRI_API int colibri_moe_route_noalloc(const void* x, const void* w_router, const float* b_router, int32_t T,
                                           int32_t d_model, int32_t num_experts, int32_t dtype, int32_t* idx,
                                           float* gate, int32_t* counts, int32_t* offsets, int32_t* row_of,
                                           void* stream);
 
-/* Frees everything the context owns.  NULL-safe. */
+/* Frees everything the context owns (the articles' colibri_free, the release call every program
+ * must make once it is done: zskr.cn 4.3, m.nxbn.cn 4.3).  NULL-safe. */
 COLIBRI_API void colibri_moe_destroy(colibri_moe_t* ctx);
 
-/* Static string for a status code. */
+/* Static text for one of the status codes above (the int codes of m.nxbn.cn 3.3 and 5.1); unknown
+ * codes get a generic string.  Never NULL. */
 COLIBRI_API const char* colibri_moe_strerror(int code);
 
 #ifdef __cplusplus

@@ -3,15 +3,17 @@
 Some callers cannot call cudaMalloc (a host framework's memory pool owns the GPU, a real-time loop
 cannot take cudaMalloc's implicit synchronisation, or the device-memory budget is fixed at
 start-up).  This entry point keeps its scratch in a fixed array inside the library instead; its
-results must equal the routing the context-based forward reports, call after call.
+results must equal the oracle's routing and the routing the context-based forward reports, call
+after call, from a single token up to the largest batch the fixed array holds.
 """
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 import testgen
-from moe_check import make_layer, torch_from_bits, x_device
+from moe_check import NEAR_TIE, check_routing, make_layer, torch_from_bits, x_device
 
 pytestmark = pytest.mark.gpu
 
@@ -33,35 +35,63 @@ def _route_noalloc(lib, x, wr, br, T, shape, dtype_code, stream):
     return rc, out
 
 
-@pytest.mark.parametrize("shape", [
+_CASES = [
+    # forward routes these 1000 tokens with the split router, route_noalloc with the plain one
     testgen.LayerShape("noalloc-bf16", 1000, 512, 256, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True),
     testgen.LayerShape("noalloc-f32", 77, 256, 512, 4, testgen.ACT_RELU_BIAS, "f32"),
-])
-def test_route_noalloc_matches_forward_routing(cuda_lib, shape):
+    # one 32-token chunk (its summary written by the chunk itself) and a single token
+    testgen.LayerShape("noalloc-one-chunk-e16", 32, 256, 256, 16, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True),
+    testgen.LayerShape("noalloc-t1", 1, 256, 256, 8, testgen.ACT_SWIGLU, "bf16"),
+    # the largest batch: every histogram row of the fixed scratch array in use
+    testgen.LayerShape("noalloc-max-t", 65536, 256, 256, 16, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True),
+]
+
+
+@pytest.mark.parametrize("shape", _CASES, ids=[c.name for c in _CASES])
+def test_route_noalloc_matches_oracle_and_forward_routing(cuda_lib, shape):
+    """Two calls in a row: each equals the oracle's routing (bit for bit outside near ties, gates
+    within 1e-5) and the routing the context-based forward reports; the second equals the first."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import mixture_experts_gemm_gb300 as moe
     lib = moe.lib()
     li = testgen.make_inputs(shape)
-    T = shape.T
+    T, E = shape.T, shape.num_experts
+    L = oracle.OracleLayer.from_inputs(li)
+    logits = L.router_logits(li.x_f32)
+    o_idx, o_gate = L.topk(logits)
+    _, o_offs, o_row_of, _ = L.dispatch(o_idx)
+    tie = oracle.near_tie_tokens(logits, NEAR_TIE)
+
     layer = make_layer(li)
     x = x_device(li)
     layer.forward(x)
-    ref = {k: v.cpu() for k, v in layer.get_routing(T).items()}
+    ref = {k: v.cpu().numpy() for k, v in layer.get_routing(T).items()}
     torch.cuda.synchronize()
+    layer.close()
+
     bf = shape.dtype == "bf16"
     wr = (torch_from_bits(li.w_router_bits) if bf else torch.from_numpy(li.w_router_f32)).cuda()
     br = None if li.b_router is None else torch.from_numpy(li.b_router).cuda()
     stream = torch.cuda.current_stream().cuda_stream
+    first = None
     for call in range(2):
         rc, got = _route_noalloc(lib, x, wr, br, T, shape, 1 if bf else 0, stream)
         assert rc == 0, moe.strerror(rc)
         torch.cuda.synchronize()
-        got = {k: v.cpu() for k, v in got.items()}
-        for k in ("idx", "counts", "offsets", "row_of"):
-            assert torch.equal(got[k], ref[k]), (call, k)
-        np.testing.assert_allclose(got["gate"].numpy(), ref["gate"].numpy(), rtol=0, atol=1e-5)
-    layer.close()
+        got = {k: v.cpu().numpy() for k, v in got.items()}
+        check_routing(got, logits, o_idx, o_gate, E, o_row_of, o_offs)
+        # the existing entry point's routing: the same decisions wherever rounding cannot flip one
+        assert np.array_equal(got["idx"][~tie], ref["idx"][~tie]), call
+        np.testing.assert_allclose(got["gate"], ref["gate"], rtol=0, atol=1e-5)
+        if not tie.any():
+            for k in ("idx", "counts", "offsets", "row_of"):
+                assert np.array_equal(got[k], ref[k]), (call, k)
+        if first is None:
+            first = got
+        else:
+            for k in got:
+                assert np.array_equal(got[k], first[k]), k
 
 
 def test_route_noalloc_rejects_oversize_batches(cuda_lib):
