@@ -261,13 +261,14 @@ def decode_sweep(layer, shape, x, out, stream, hbm_gbs, steps):
     return res
 
 
-def other_workloads(peaks, steps, device):
+def other_workloads(peaks, steps, device: int):
     """Step time of the benchmark's other layers (each with its own seeded weights), for the record."""
     import torch
     import testgen
     from moe_check import host_weights, x_device
     import mixture_experts_gemm_gb300 as moe
-    stream = torch.cuda.current_stream(device)
+    dev = torch.device("cuda", device)
+    stream = torch.cuda.current_stream(dev)
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     res = {}
@@ -279,8 +280,8 @@ def other_workloads(peaks, steps, device):
                              has_router_bias=s.zipf_router_bias, out_dtype="f32", device=device, top_k=s.top_k,
                              gate_mode=s.gate_mode, shared_expert=s.shared_expert)
         layer.load_weights(**host_weights(li))
-        x = x_device(li).to(device)
-        out = torch.empty((s.T, s.d_model), dtype=torch.float32, device=device)
+        x = x_device(li).to(dev)
+        out = torch.empty((s.T, s.d_model), dtype=torch.float32, device=dev)
         ms = time_forwards(layer, x.data_ptr(), out.data_ptr(), s.T, stream, steps, 10)
         counts = layer.get_routing(s.T)["counts"].cpu().numpy()
         alg = algorithmic(s, s.T, int((counts > 0).sum()))
@@ -497,7 +498,7 @@ def main():
         if shape.name == "mixtral-prefill" and shape.top_k == 2 and not shape.shared_expert and shape.gate_mode == 0:
             extra["decode"] = decode_sweep(layer, shape, x, out, stream,
                                            float(peaks_x.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])), n_x)
-        extra["workloads"] = other_workloads(peaks_x, n_x, dev)
+        extra["workloads"] = other_workloads(peaks_x, n_x, local)
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
