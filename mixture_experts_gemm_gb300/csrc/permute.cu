@@ -23,21 +23,24 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherArgs a, in
   const int t = gw / wpt, part = gw - t * wpt;
   pdl_wait();
   pdl_trigger();  // after the wait: the next kernel may then read what the router wrote before waiting
-  if (t >= a.T) return;
+  const bool valid = t < a.T;
   const int chunk = t / kRouterChunk;
   const int S = a.S;
   int r[kMaxSlots];
-  bool ok = true;
+  bool ok = valid;
 #pragma unroll
   for (int s = 0; s < kMaxSlots; ++s) {
     r[s] = 0;
-    if (s < S) {
+    if (valid && s < S) {
       const int e = a.idx[(size_t)S * t + s];
       r[s] = a.chunk_base[(size_t)chunk * a.E + e] + a.row_of[(size_t)S * t + s];
       ok = ok && r[s] >= 0 && r[s] < a.rows_alloc;
     }
   }
-  __syncwarp();
+  // the wpt warps of a token (all in this CTA) have read its in-chunk ranks before the first warp
+  // overwrites them with rows below
+  __syncthreads();
+  if (!valid) return;
   if (lane == 0 && part == 0) {
     if (ok) {
       for (int s = 0; s < S; ++s) {
