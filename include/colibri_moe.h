@@ -232,6 +232,59 @@ COLIBRI_API int colibri_moe_route_noalloc(const void* x, const void* w_router, c
                                           float* gate, int32_t* counts, int32_t* offsets, int32_t* row_of,
                                           void* stream);
 
+/* ---- expert parallelism: the experts of one layer split over ep_size GPUs ----
+ * The articles run the whole layer on one device; these calls split its Dispatch and Compute stages
+ * (zskr.cn 2.1) across GPUs, one process (and one context) per GPU, with the caller's communicator
+ * moving rows between them.  Rank r owns experts [r*El, (r+1)*El), El = E / ep_size; it routes its
+ * own tokens over all E experts and runs the expert FFN for every token routed to its experts:
+ *
+ *   ep_dispatch(x, T) -> send_rows [T*k, d], send_counts [E]     rows grouped by expert, so rank q's
+ *                                                                rows are one contiguous block
+ *   all-to-all of send_counts (El per peer) -> recv_counts [ep_size, El]   (host copy for the call below)
+ *   all-to-all of the rows (split sizes = per-peer sums of the counts) -> recv_rows
+ *   ep_experts(recv_rows, recv_counts) -> y_rows [R, d] fp32     same order as recv_rows
+ *   all-to-all of y_rows back (the split sizes swapped) -> y_back [T*k, d] fp32
+ *   ep_combine(y_back) -> out [T, d]                              gate-weighted sum in slot order
+ *
+ * Every call is asynchronous on `stream`, allocates nothing and synchronises nothing; the caller
+ * orders them with its exchanges.  The result equals colibri_moe_forward's for the same weights,
+ * bit for bit wherever forward runs the grouped GEMMs (batches above its decode-path limit). */
+
+/* Context of rank ep_rank of an expert-parallel layer.  cfg describes the whole layer (num_experts =
+ * E across all ranks, max_tokens = most tokens one rank routes per step); E must be a multiple of
+ * ep_size (1..E); no shared expert.  max_recv_rows bounds the rows one ep_experts call may receive
+ * (at most ep_size * max_tokens * top_k; the workspace holds that many expert rows).  The context
+ * holds the router weights and its own experts' weights only: load_weights reads entries
+ * [ep_rank*El, (ep_rank+1)*El) of the per-expert arrays and ignores (may be NULL) the others.
+ * colibri_moe_forward / forward_host / forward_host_async return COLIBRI_ERR_UNSUPPORTED on it.
+ * Errors: COLIBRI_ERR_INVALID_ARG (bad rank, size, or E not divisible), COLIBRI_ERR_UNSUPPORTED
+ * (shared expert), and those of colibri_moe_create. */
+COLIBRI_API int colibri_moe_ep_create(const colibri_moe_config_t* cfg, int32_t ep_rank, int32_t ep_size,
+                                      int32_t max_recv_rows, int device, colibri_moe_t** out);
+
+/* Source side, before the exchange: routes x [T, d] (device, config.dtype, T <= max_tokens) over all
+ * E experts and writes send_rows [T*k, d] (device, config.dtype): row i holds a token routed to the
+ * expert whose block contains i, experts in ascending order, each expert's tokens in ascending token
+ * order (the dispatch order of zskr.cn 3.2, without padding).  send_counts [E] (device int32) gets
+ * the rows per expert.  The routing is kept for ep_combine (and get_routing, whose row_of then gives
+ * each (token, slot)'s row of send_rows).  x, send_rows and send_counts must not overlap; x and
+ * send_rows 16-byte aligned.  T == 0 zeroes send_counts. */
+COLIBRI_API int colibri_moe_ep_dispatch(colibri_moe_t* ctx, const void* x, int32_t T, void* send_rows,
+                                        int32_t* send_counts, void* stream);
+
+/* Expert side: recv_counts is a HOST int32 array [ep_size, El]: the rows source p sent for local
+ * expert j.  recv_rows [R, d] (device, config.dtype, R = the sum of recv_counts <= max_recv_rows) are
+ * the received rows in source order, each source's rows grouped by local expert.  Writes y_rows
+ * [R, d] (device fp32): each row's expert output y_e(x) (no gate), in the order of recv_rows.
+ * Runs the grouped up GEMM (activation fused) and down GEMM over the local experts. */
+COLIBRI_API int colibri_moe_ep_experts(colibri_moe_t* ctx, const void* recv_rows, const int32_t* recv_counts,
+                                       void* y_rows, void* stream);
+
+/* Source side, after the exchange back: y_back [T*k, d] (device fp32) holds the expert outputs of
+ * send_rows' rows in the same order; out [T, d] (device, config.out_dtype) = sum over the token's
+ * slots of gate * y_back[row], in slot order in fp32 (m.nxbn.cn 3.3), T from the last ep_dispatch. */
+COLIBRI_API int colibri_moe_ep_combine(colibri_moe_t* ctx, const float* y_back, void* out, void* stream);
+
 /* Frees everything the context owns (the articles' colibri_free, the release call every program
  * must make once it is done: zskr.cn 4.3, m.nxbn.cn 4.3).  NULL-safe. */
 COLIBRI_API void colibri_moe_destroy(colibri_moe_t* ctx);

@@ -37,6 +37,7 @@ EXPORTED = ("colibri_moe_create", "colibri_moe_load_weights", "colibri_moe_forwa
             "colibri_moe_forward_host_async", "colibri_moe_host_sync",
             "colibri_moe_last_kernel_count", "colibri_moe_set_stage_events", "colibri_moe_device_status",
             "colibri_moe_probe_wait_timeout", "colibri_moe_route_noalloc",
+            "colibri_moe_ep_create", "colibri_moe_ep_dispatch", "colibri_moe_ep_experts", "colibri_moe_ep_combine",
             "colibri_moe_destroy", "colibri_moe_strerror")
 
 
@@ -87,6 +88,11 @@ def lib() -> ctypes.CDLL:
             "colibri_moe_device_status": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
             "colibri_moe_probe_wait_timeout": ([vp, i32, vp], ctypes.c_int),
             "colibri_moe_route_noalloc": ([vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp], ctypes.c_int),
+            "colibri_moe_ep_create": ([ctypes.POINTER(Config), i32, i32, i32, ctypes.c_int, ctypes.POINTER(vp)],
+                                      ctypes.c_int),
+            "colibri_moe_ep_dispatch": ([vp, vp, i32, vp, vp, vp], ctypes.c_int),
+            "colibri_moe_ep_experts": ([vp, vp, vp, vp, vp], ctypes.c_int),
+            "colibri_moe_ep_combine": ([vp, vp, vp, vp], ctypes.c_int),
             "colibri_moe_destroy": ([vp], None),
             "colibri_moe_strerror": ([ctypes.c_int], ctypes.c_char_p),
         }
@@ -135,19 +141,34 @@ def _stream_handle(stream) -> Optional[int]:
 
 
 class MoELayer:
-    """One MoE layer instance (a ``colibri_moe_t`` context) on one GPU."""
+    """One MoE layer instance (a ``colibri_moe_t`` context) on one GPU.
+
+    With ``ep_size`` > 0 the context is rank ``ep_rank`` of an expert-parallel layer (the experts
+    split over ep_size GPUs): it holds experts [ep_rank*El, (ep_rank+1)*El) and runs ep_dispatch /
+    ep_experts / ep_combine (see ``ep.py`` for the exchange between them) instead of forward."""
 
     def __init__(self, d_model: int, d_ff: int, num_experts: int, max_tokens: int, dtype="bf16", act="swiglu",
                  has_router_bias: bool = False, out_dtype="f32", device: int = 0, top_k: int = 2,
-                 gate_mode="selected", shared_expert: bool = False):
+                 gate_mode="selected", shared_expert: bool = False, ep_rank: int = 0, ep_size: int = 0,
+                 max_recv_rows: Optional[int] = None):
         self.cfg = Config(d_model, d_ff, num_experts, top_k, max_tokens,
                           _DTYPES[dtype] if isinstance(dtype, str) else int(dtype),
                           _ACTS[act] if isinstance(act, str) else int(act), int(bool(has_router_bias)),
                           _DTYPES[out_dtype] if isinstance(out_dtype, str) else int(out_dtype),
                           _GATES[gate_mode] if isinstance(gate_mode, str) else int(gate_mode), int(bool(shared_expert)))
         self.device = device
+        self.ep_rank, self.ep_size = int(ep_rank), int(ep_size)
+        self._ep_T = None
         self._h = ctypes.c_void_p()
-        _check(lib().colibri_moe_create(ctypes.byref(self.cfg), device, ctypes.byref(self._h)), "colibri_moe_create")
+        if self.ep_size > 0:
+            if max_recv_rows is None:
+                max_recv_rows = self.ep_size * max_tokens * top_k
+            self.max_recv_rows = int(max_recv_rows)
+            _check(lib().colibri_moe_ep_create(ctypes.byref(self.cfg), self.ep_rank, self.ep_size, self.max_recv_rows,
+                                               device, ctypes.byref(self._h)), "colibri_moe_ep_create")
+        else:
+            _check(lib().colibri_moe_create(ctypes.byref(self.cfg), device, ctypes.byref(self._h)),
+                   "colibri_moe_create")
         self._keep = []
 
     # -------------------------------------------------------------- properties
@@ -245,6 +266,56 @@ class MoELayer:
                                              _ptr(r["offsets"]), _ptr(r["row_of"]), _stream_handle(stream)),
                "colibri_moe_get_routing")
         return r
+
+    # -------------------------------------------------------------- expert parallelism
+    @property
+    def local_experts(self) -> int:
+        """El: experts this rank holds (E / ep_size), or E for an ordinary context."""
+        return self.cfg.num_experts // self.ep_size if self.ep_size else self.cfg.num_experts
+
+    def ep_dispatch(self, x, send_rows=None, send_counts=None, stream=None):
+        """Route x[T, d] over all experts; returns (send_rows [T*k, d], send_counts [E] int32), CUDA tensors,
+        rows grouped by expert (rank q's rows are one contiguous block)."""
+        import torch
+        T, d, k = x.shape[0], self.cfg.d_model, self.cfg.top_k
+        if send_rows is None:
+            send_rows = torch.empty((T * k, d), dtype=x.dtype, device=x.device)
+        if send_counts is None:
+            send_counts = torch.empty(self.cfg.num_experts, dtype=torch.int32, device=x.device)
+        _check(lib().colibri_moe_ep_dispatch(self._h, _ptr(x), T, _ptr(send_rows), _ptr(send_counts),
+                                             _stream_handle(stream)), "colibri_moe_ep_dispatch")
+        self._ep_T = T
+        return send_rows, send_counts
+
+    def ep_experts(self, recv_rows, recv_counts, y_rows=None, stream=None):
+        """Expert FFN of the rows this rank received.  recv_counts: HOST int32 [ep_size, El] (numpy or
+        torch); returns y_rows [R, d] fp32 (CUDA), in the order of recv_rows."""
+        import numpy as np
+        import torch
+        rc = np.ascontiguousarray(np.asarray(recv_counts.cpu() if hasattr(recv_counts, "cpu") else recv_counts,
+                                             dtype=np.int32))
+        if rc.size != self.ep_size * self.local_experts:
+            raise ValueError(f"recv_counts must hold ep_size x El = {self.ep_size} x {self.local_experts} entries")
+        R = int(rc.sum())
+        if y_rows is None:
+            y_rows = torch.empty((R, self.cfg.d_model), dtype=torch.float32, device=torch.device("cuda", self.device))
+        _check(lib().colibri_moe_ep_experts(self._h, _ptr(recv_rows) if R else None, rc.ctypes.data,
+                                            _ptr(y_rows) if R else None, _stream_handle(stream)),
+               "colibri_moe_ep_experts")
+        return y_rows
+
+    def ep_combine(self, y_back, out=None, stream=None):
+        """out[T, d] = gate-weighted sum of the returned expert outputs (T of the last ep_dispatch)."""
+        import torch
+        if self._ep_T is None:
+            raise ColibriError(-5, "colibri_moe_ep_combine")
+        if out is None:
+            odt = torch.float32 if self.cfg.out_dtype == DTYPE_F32 else torch.bfloat16
+            out = torch.empty((self._ep_T, self.cfg.d_model), dtype=odt, device=torch.device("cuda", self.device))
+        _check(lib().colibri_moe_ep_combine(self._h, _ptr(y_back) if self._ep_T else None,
+                                            _ptr(out) if self._ep_T else None, _stream_handle(stream)),
+               "colibri_moe_ep_combine")
+        return out
 
     def debug_buffer(self, which: int):
         p = ctypes.c_void_p()

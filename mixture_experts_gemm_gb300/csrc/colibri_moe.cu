@@ -7,6 +7,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -95,6 +96,14 @@ struct colibri_moe {
   bool decode_fused = true;  // decode batches: one cooperative kernel after the router
   bool direct_h = true;      // ... whose unsplit up projection writes H in its epilogue
   int fused_ctas = 0;        // its grid (one CTA per SM)
+  // expert parallelism (colibri_moe_ep_create): the context routes over all E experts but holds the
+  // weights of experts [ep_first, ep_first + n_arena) only
+  int ep_size = 0;           // 0: an ordinary context
+  int ep_rank = 0;
+  int ep_first = 0;
+  int n_arena = 0;           // experts in the weight arena: Ex, or the local experts of an EP context
+  int64_t ep_max_rows = 0;   // most rows one ep_experts call may receive
+  Sched* ep_sched = nullptr; // schedule of the local experts' GEMMs (ep_experts)
   int32_t last_T = -1;
   int32_t last_kernels = 0;  // kernels enqueued by the last forward
   std::vector<cudaEvent_t> events;
@@ -291,11 +300,21 @@ void colibri_moe_destroy(colibri_moe_t* ctx) {
   delete ctx;
 }
 
-int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_t** out) {
+}  // extern "C"
+
+// Ordinary context (ep_size == 0) or the context of rank ep_rank of an expert-parallel layer.
+static int create_impl(const colibri_moe_config_t* cfg, int device, int ep_rank, int ep_size, int64_t ep_max_rows,
+                       colibri_moe_t** out) {
   if (!out) return COLIBRI_ERR_INVALID_ARG;
   *out = nullptr;
   int rc = check_config(cfg);
   if (rc) return rc;
+  if (ep_size > 0) {
+    if (ep_size > cfg->num_experts || cfg->num_experts % ep_size || ep_rank < 0 || ep_rank >= ep_size ||
+        ep_max_rows <= 0 || ep_max_rows > (int64_t{1} << 26))
+      return COLIBRI_ERR_INVALID_ARG;
+    if (cfg->has_shared_expert) return COLIBRI_ERR_UNSUPPORTED;
+  }
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
     cudaGetLastError();
@@ -329,7 +348,16 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   c->S = cfg->top_k + cfg->has_shared_expert;
   c->Ex = static_cast<int>(E) + cfg->has_shared_expert;
   const int64_t S = c->S, Ex = c->Ex;
-  c->rows_alloc = ((S * T + (kRowTile - 1) * Ex) + kRowTile - 1) / kRowTile * kRowTile;
+  c->ep_size = ep_size;
+  c->ep_rank = ep_rank;
+  c->n_arena = ep_size > 0 ? static_cast<int>(E / ep_size) : c->Ex;
+  c->ep_first = ep_size > 0 ? ep_rank * c->n_arena : 0;
+  c->ep_max_rows = ep_size > 0 ? ep_max_rows : 0;
+  // Xp / H / Y rows: every slot of max_tokens tokens, or the rows an expert rank may receive, plus
+  // up to 127 padding rows per expert segment
+  const int64_t gemm_rows = ep_size > 0 ? ep_max_rows : S * T;
+  const int64_t gemm_experts = ep_size > 0 ? c->n_arena : Ex;
+  c->rows_alloc = ((gemm_rows + (kRowTile - 1) * gemm_experts) + kRowTile - 1) / kRowTile * kRowTile;
   c->nchunks_max = static_cast<int>((T + kRouterChunk - 1) / kRouterChunk);
   {
     // W_r columns staged per router pass: at most 96 KB of shared memory
@@ -356,8 +384,10 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   const size_t o_gor = carve(c->rows_alloc * 4);
   const size_t o_hist = carve(static_cast<size_t>(c->nchunks_max) * Ex * 4);
   const size_t o_sched = carve(sizeof(Sched));
-  // decode partial sums: bf16 layers whose batches can be decode-sized
-  c->decode_max_t = cfg->dtype == COLIBRI_DTYPE_BF16 ? env_decode_max_t(d, f) : 0;
+  const size_t o_ep_sched = ep_size > 0 ? carve(sizeof(Sched)) : 0;
+  // decode partial sums: bf16 layers whose batches can be decode-sized (an expert rank always runs
+  // the grouped GEMMs: its rows come from every source)
+  c->decode_max_t = (cfg->dtype == COLIBRI_DTYPE_BF16 && ep_size == 0) ? env_decode_max_t(d, f) : 0;
   if (c->decode_max_t > T) c->decode_max_t = static_cast<int>(T);
   const int64_t npad_max = (c->decode_max_t + 15) / 16 * 16;
   const int64_t part_floats = c->decode_max_t > 0
@@ -369,9 +399,9 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   const size_t o_spart = carve(static_cast<size_t>(kRouterSplitMaxChunks) * router_split_factor() * kRouterChunk *
                                16 * sizeof(float));
   size_t o_xs[kHostSlots], o_os[kHostSlots];
-  for (int i = 0; i < kHostSlots; ++i) {
-    o_xs[i] = carve(T * d * c->esize);
-    o_os[i] = carve(T * d * c->out_esize);
+  for (int i = 0; i < kHostSlots; ++i) {  // (an expert-parallel context has no host-buffer forward)
+    o_xs[i] = carve(ep_size > 0 ? 0 : T * d * c->esize);
+    o_os[i] = carve(ep_size > 0 ? 0 : T * d * c->out_esize);
   }
   c->ws_bytes = off;
   if (cudaMalloc(&c->ws, c->ws_bytes) != cudaSuccess) {
@@ -390,6 +420,7 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   c->gate_of_row = reinterpret_cast<float*>(b + o_gor);
   c->hist = reinterpret_cast<int32_t*>(b + o_hist);
   c->sched = reinterpret_cast<Sched*>(b + o_sched);
+  c->ep_sched = ep_size > 0 ? reinterpret_cast<Sched*>(b + o_ep_sched) : nullptr;
   c->partial = part_floats > 0 ? reinterpret_cast<float*>(b + o_part) : nullptr;
   c->tile_done = reinterpret_cast<uint32_t*>(b + o_tiles);
   c->split_part = reinterpret_cast<float*>(b + o_spart);
@@ -446,10 +477,26 @@ int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_
   return COLIBRI_OK;
 }
 
+extern "C" {
+
+int colibri_moe_create(const colibri_moe_config_t* cfg, int device, colibri_moe_t** out) {
+  return create_impl(cfg, device, 0, 0, 0, out);
+}
+
+int colibri_moe_ep_create(const colibri_moe_config_t* cfg, int32_t ep_rank, int32_t ep_size, int32_t max_recv_rows,
+                          int device, colibri_moe_t** out) {
+  if (ep_size < 1) {
+    if (out) *out = nullptr;
+    return COLIBRI_ERR_INVALID_ARG;
+  }
+  return create_impl(cfg, device, ep_rank, ep_size, max_recv_rows, out);
+}
+
 int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_weights_t* w, void* stream) {
   if (!ctx || !w) return COLIBRI_ERR_INVALID_ARG;
   const colibri_moe_config_t& c = ctx->cfg;
-  const int E = c.num_experts, Ex = ctx->Ex;
+  const int E = c.num_experts, Ex = ctx->n_arena;  // experts held in the arena
+  const int first = ctx->ep_first;                  // arena expert e is expert first + e
   const bool swiglu = c.act == COLIBRI_ACT_SWIGLU;
   const bool shared = c.has_shared_expert != 0;
   // presence checks: every tensor the activation needs, and none it does not use
@@ -457,7 +504,7 @@ int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_weights_t* w,
   if ((c.has_router_bias != 0) != (w->b_router != nullptr)) return COLIBRI_ERR_BAD_WEIGHTS;
   if (swiglu && (!w->w3 || w->b1 || w->b2)) return COLIBRI_ERR_BAD_WEIGHTS;
   if (!swiglu && (w->w3 || !w->b1 || !w->b2)) return COLIBRI_ERR_BAD_WEIGHTS;
-  for (int e = 0; e < E; ++e) {
+  for (int e = first; e < first + (ctx->ep_size > 0 ? Ex : E); ++e) {  // an expert rank reads its own only
     if (!w->w1[e] || !w->w2[e]) return COLIBRI_ERR_BAD_WEIGHTS;
     if (swiglu && !w->w3[e]) return COLIBRI_ERR_BAD_WEIGHTS;
     if (!swiglu && (!w->b1[e] || !w->b2[e])) return COLIBRI_ERR_BAD_WEIGHTS;
@@ -512,12 +559,13 @@ int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_weights_t* w,
   const size_t mat = f * d * es;  // bytes of one [f, d] matrix
   // arena expert e < E: routed expert e; e == E: the shared expert
   for (int e = 0; ok && e < Ex; ++e) {
-    const bool sh = e == E;
-    const void* W1 = sh ? w->ws1 : w->w1[e];
-    const void* W3 = sh ? w->ws3 : (swiglu ? w->w3[e] : nullptr);
-    const void* W2 = sh ? w->ws2 : w->w2[e];
-    const float* B1 = sh ? w->bs1 : (swiglu ? nullptr : w->b1[e]);
-    const float* B2 = sh ? w->bs2 : (swiglu ? nullptr : w->b2[e]);
+    const bool sh = ctx->ep_size == 0 && e == E;
+    const int src = first + e;
+    const void* W1 = sh ? w->ws1 : w->w1[src];
+    const void* W3 = sh ? w->ws3 : (swiglu ? w->w3[src] : nullptr);
+    const void* W2 = sh ? w->ws2 : w->w2[src];
+    const float* B1 = sh ? w->bs1 : (swiglu ? nullptr : w->b1[src]);
+    const float* B2 = sh ? w->bs2 : (swiglu ? nullptr : w->b2[src]);
     char* w13e = static_cast<char*>(ctx->w13) + static_cast<size_t>(e) * ctx->n_up * d * es;
     if (swiglu && c.dtype == COLIBRI_DTYPE_BF16) {
       // gate rows [128j, 128j+128) -> arena rows [256j, 256j+128); up rows -> [256j+128, 256j+256)
@@ -549,6 +597,28 @@ int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_weights_t* w,
       return COLIBRI_ERR_CUDA;
   }
   ctx->loaded = true;
+  return COLIBRI_OK;
+}
+
+// The router variant for this batch.  Large bf16 batches stream x into the router through shared
+// memory by TMA (a per-call map of the caller's buffer); small ones read it straight from global
+// memory.
+static int enqueue_router(const colibri_moe_t* ctx, const RouterArgs& ra, const void* x, int32_t T, int nchunks,
+                          cudaStream_t s) {
+  const colibri_moe_config_t& c = ctx->cfg;
+  const bool bf16 = c.dtype == COLIBRI_DTYPE_BF16;
+  const int d = c.d_model;
+  CUtensorMap tm_xr;
+  if (bf16 && T > kRouterSplitMinT && nchunks <= kRouterSplitMaxChunks && d % (32 * router_split_factor()) == 0) {
+    // 9..1024 tokens: the hidden dimension split over several CTAs per chunk (fewer tokens gain
+    // nothing from it: one CTA's loads already take one or two rounds; more fill the GPU anyway)
+    if (launch_router_split(ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  } else if (bf16 && T >= kRouterTmaMinT && d % router_tma_cols() == 0 &&
+             make_tmap(&tm_xr, x, d, static_cast<uint64_t>(T), kRouterChunk)) {
+    if (launch_router_tma(tm_xr, ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  } else if (launch_router(c.dtype, ra, nchunks, s) != cudaSuccess) {
+    return COLIBRI_ERR_CUDA;
+  }
   return COLIBRI_OK;
 }
 
@@ -588,19 +658,8 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
                 ctx->row_of, ctx->hist, ctx->sched, ctx->k, c.gate_mode, c.has_shared_expert, ctx->S, ctx->Ex,
                 fuse && (gather_a || !bf16) ? static_cast<float*>(out) : nullptr, ctx->tile_done, d / 128,
                 ctx->split_part};
-  // large bf16 batches stream x into the router through shared memory by TMA (a per-call map of the
-  // caller's buffer); small ones read it straight from global memory
-  CUtensorMap tm_xr;
-  if (bf16 && T > kRouterSplitMinT && nchunks <= kRouterSplitMaxChunks && d % (32 * router_split_factor()) == 0) {
-    // 9..1024 tokens: the hidden dimension split over several CTAs per chunk (fewer tokens gain
-    // nothing from it: one CTA's loads already take one or two rounds; more fill the GPU anyway)
-    if (launch_router_split(ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
-  } else if (bf16 && T >= kRouterTmaMinT && d % router_tma_cols() == 0 &&
-      make_tmap(&tm_xr, x, d, static_cast<uint64_t>(T), kRouterChunk)) {
-    if (launch_router_tma(tm_xr, ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
-  } else if (launch_router(c.dtype, ra, nchunks, s) != cudaSuccess) {
-    return COLIBRI_ERR_CUDA;
-  }
+  const int rrc = enqueue_router(ctx, ra, x, T, nchunks, s);
+  if (rrc) return rrc;
   mark(1);
   GatherArgs ga{x, ctx->idx, ctx->row_of, ctx->hist, T, d, E, ctx->S, ctx->rows_alloc,
                 gather_a ? nullptr : ctx->xp, ctx->tok_of_row, ctx->sched, ctx->gate,
@@ -712,6 +771,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
 
 int colibri_moe_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t T, void* stream) {
   if (!ctx) return COLIBRI_ERR_INVALID_ARG;
+  if (ctx->ep_size > 0) return COLIBRI_ERR_UNSUPPORTED;  // an expert rank: ep_dispatch / ep_experts / ep_combine
   if (T < 0 || T > ctx->cfg.max_tokens) return COLIBRI_ERR_INVALID_ARG;
   if (!ctx->loaded) return COLIBRI_ERR_STATE;
   if (T == 0) {
@@ -731,6 +791,7 @@ int colibri_moe_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t T,
 
 int colibri_moe_forward_host(colibri_moe_t* ctx, const void* x_host, void* out_host, int32_t T, void* stream) {
   if (!ctx) return COLIBRI_ERR_INVALID_ARG;
+  if (ctx->ep_size > 0) return COLIBRI_ERR_UNSUPPORTED;  // an expert rank: ep_dispatch / ep_experts / ep_combine
   if (T < 0 || T > ctx->cfg.max_tokens) return COLIBRI_ERR_INVALID_ARG;
   if (!ctx->loaded) return COLIBRI_ERR_STATE;
   if (T == 0) {
@@ -766,6 +827,7 @@ int colibri_moe_forward_host(colibri_moe_t* ctx, const void* x_host, void* out_h
 int colibri_moe_forward_host_async(colibri_moe_t* ctx, const void* x_host, void* out_host, int32_t T,
                                    void* stream) {
   if (!ctx) return COLIBRI_ERR_INVALID_ARG;
+  if (ctx->ep_size > 0) return COLIBRI_ERR_UNSUPPORTED;
   if (T < 0 || T > ctx->cfg.max_tokens) return COLIBRI_ERR_INVALID_ARG;
   if (!ctx->loaded) return COLIBRI_ERR_STATE;
   if (T == 0) {
@@ -808,6 +870,177 @@ int colibri_moe_host_sync(colibri_moe_t* ctx) {
     cudaGetLastError();
     return COLIBRI_ERR_CUDA;
   }
+  return COLIBRI_OK;
+}
+
+// ------------------------------------------------------------------------- expert parallelism
+
+int colibri_moe_ep_dispatch(colibri_moe_t* ctx, const void* x, int32_t T, void* send_rows, int32_t* send_counts,
+                            void* stream) {
+  if (!ctx) return COLIBRI_ERR_INVALID_ARG;
+  if (ctx->ep_size == 0) return COLIBRI_ERR_UNSUPPORTED;
+  if (T < 0 || T > ctx->cfg.max_tokens) return COLIBRI_ERR_INVALID_ARG;
+  if (!ctx->loaded) return COLIBRI_ERR_STATE;
+  if (!send_counts || !is_device_ptr(send_counts, ctx->device)) return COLIBRI_ERR_INVALID_ARG;
+  const colibri_moe_config_t& c = ctx->cfg;
+  const int E = c.num_experts, d = c.d_model, k = ctx->k;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return COLIBRI_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    if (cudaMemsetAsync(send_counts, 0, E * sizeof(int32_t), s) != cudaSuccess) {
+      cudaGetLastError();
+      return COLIBRI_ERR_CUDA;
+    }
+    ctx->last_T = 0;
+    ctx->last_kernels = 0;
+    return COLIBRI_OK;
+  }
+  if (!x || !send_rows) return COLIBRI_ERR_INVALID_ARG;
+  const size_t xb = static_cast<size_t>(T) * d * ctx->esize;
+  const size_t sb = static_cast<size_t>(T) * k * d * ctx->esize;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(send_rows)) & 15) return COLIBRI_ERR_INVALID_ARG;
+  if (overlap(x, xb, send_rows, sb) || overlap(send_counts, E * sizeof(int32_t), send_rows, sb))
+    return COLIBRI_ERR_INVALID_ARG;
+  if (!is_device_ptr(x, ctx->device) || !is_device_ptr(send_rows, ctx->device)) return COLIBRI_ERR_INVALID_ARG;
+  const int nchunks = (T + kRouterChunk - 1) / kRouterChunk;
+  RouterArgs ra{x, ctx->w_router, ctx->b_router, T, d, E, ctx->dchunk, ctx->idx, ctx->gate, ctx->row_of, ctx->hist,
+                ctx->sched, k, c.gate_mode, 0, k, E, nullptr, ctx->tile_done, d / 128, ctx->split_part};
+  const int rc = enqueue_router(ctx, ra, x, T, nchunks, s);
+  if (rc) return rc;
+  EpPackArgs pa{x, ctx->idx, ctx->row_of, ctx->hist, ctx->sched, T, d, E, k, send_rows, send_counts,
+                &ctx->sched->status};
+  if (launch_ep_pack(c.dtype, pa, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  ctx->last_T = T;
+  ctx->last_kernels = 2;
+  return COLIBRI_OK;
+}
+
+int colibri_moe_ep_experts(colibri_moe_t* ctx, const void* recv_rows, const int32_t* recv_counts, void* y_rows,
+                           void* stream) {
+  if (!ctx) return COLIBRI_ERR_INVALID_ARG;
+  if (ctx->ep_size == 0) return COLIBRI_ERR_UNSUPPORTED;
+  if (!ctx->loaded) return COLIBRI_ERR_STATE;
+  if (!recv_counts) return COLIBRI_ERR_INVALID_ARG;
+  const colibri_moe_config_t& c = ctx->cfg;
+  const int El = ctx->n_arena, N = ctx->ep_size, d = c.d_model, f = c.d_ff;
+  // the plan: received rows are source-major (p, j); Xp segments expert-major (j, p), padded to 128
+  EpPlan plan{};
+  plan.n_seg = N * El;
+  plan.El = El;
+  int64_t R = 0;
+  for (int p = 0; p < N; ++p)
+    for (int j = 0; j < El; ++j) {
+      const int32_t n = recv_counts[p * El + j];
+      if (n < 0) return COLIBRI_ERR_INVALID_ARG;
+      plan.src[p * El + j] = static_cast<int32_t>(R < INT32_MAX ? R : INT32_MAX);
+      plan.counts[j] += n;
+      R += n;
+    }
+  if (R > ctx->ep_max_rows) return COLIBRI_ERR_INVALID_ARG;
+  {
+    int32_t off = 0, mt = 0;
+    for (int j = 0; j < El; ++j) {
+      plan.offsets[j] = off;
+      plan.mstart[j] = mt;
+      int32_t fill = off;
+      for (int p = 0; p < N; ++p) {
+        plan.dst[p * El + j] = fill;
+        fill += recv_counts[p * El + j];
+      }
+      const int32_t tiles = (plan.counts[j] + kRowTile - 1) / kRowTile;
+      off += tiles * kRowTile;
+      mt += tiles;
+    }
+    plan.offsets[El] = off;
+    plan.mstart[El] = mt;
+  }
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return COLIBRI_ERR_CUDA;
+  if (R == 0) {
+    ctx->last_kernels = 0;
+    return COLIBRI_OK;
+  }
+  if (!recv_rows || !y_rows) return COLIBRI_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(recv_rows) | reinterpret_cast<uintptr_t>(y_rows)) & 15)
+    return COLIBRI_ERR_INVALID_ARG;
+  if (overlap(recv_rows, static_cast<size_t>(R) * d * ctx->esize, y_rows, static_cast<size_t>(R) * d * 4))
+    return COLIBRI_ERR_INVALID_ARG;
+  if (!is_device_ptr(recv_rows, ctx->device) || !is_device_ptr(y_rows, ctx->device)) return COLIBRI_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool bf16 = c.dtype == COLIBRI_DTYPE_BF16;
+  const bool swiglu = c.act == COLIBRI_ACT_SWIGLU;
+  EpRegroupArgs rg{recv_rows, ctx->xp, static_cast<int>(R), static_cast<int>(d * ctx->esize), ctx->ep_sched, plan};
+  if (launch_ep_regroup(rg, ctx->num_sms, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  int64_t max_mtiles = (R + (kRowTile - 1) * static_cast<int64_t>(El)) / kRowTile;
+  if (max_mtiles > ctx->rows_alloc / kRowTile) max_mtiles = ctx->rows_alloc / kRowTile;
+  Sched* const sc = ctx->ep_sched;
+  int32_t* const status = &ctx->sched->status;
+  if (bf16 && ctx->pair_gemm) {
+    const int bn = tc_gemm_block_n();
+    const int64_t max_pairs = (max_mtiles + El + 1) / 2;
+    GemmArgs up{sc, El, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns, status, nullptr, nullptr,
+                nullptr, ctx->dynamic_tiles ? &sc->tile_ctr[0] : nullptr, nullptr, 0};
+    int64_t ctas = 2 * max_pairs * up.n_tiles;
+    int grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
+    if (launch_pair_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, false, ctx->tm_xp, ctx->tm_w13_dec, up, grid, s) !=
+        cudaSuccess)
+      return COLIBRI_ERR_CUDA;
+    GemmArgs dn{sc, El, f, d, d / bn, ctx->y, d, ctx->b2, d, ctx->timeout_ns, status, nullptr, nullptr, nullptr,
+                ctx->dynamic_tiles ? &sc->tile_ctr[1] : nullptr, nullptr, 0};
+    ctas = 2 * max_pairs * dn.n_tiles;
+    grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
+    if (launch_pair_gemm(kEpiStoreF32, false, ctx->tm_h, ctx->tm_w2_dec, dn, grid, s) != cudaSuccess)
+      return COLIBRI_ERR_CUDA;
+  } else if (bf16) {
+    const int bn = tc_gemm_block_n();
+    GemmArgs up{sc, El, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns, status, nullptr, nullptr,
+                nullptr, nullptr, nullptr, 0};
+    int64_t tiles = max_mtiles * up.n_tiles;
+    int grid = static_cast<int>(tiles < ctx->num_sms ? tiles : ctx->num_sms);
+    if (launch_tc_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, false, ctx->tm_xp, ctx->tm_w13, up, grid, s) != cudaSuccess)
+      return COLIBRI_ERR_CUDA;
+    GemmArgs dn{sc, El, f, d, d / bn, ctx->y, d, ctx->b2, d, ctx->timeout_ns, status, nullptr, nullptr, nullptr,
+                nullptr, nullptr, 0};
+    tiles = max_mtiles * dn.n_tiles;
+    grid = static_cast<int>(tiles < ctx->num_sms ? tiles : ctx->num_sms);
+    if (launch_tc_gemm(kEpiStoreF32, false, ctx->tm_h, ctx->tm_w2, dn, grid, s) != cudaSuccess)
+      return COLIBRI_ERR_CUDA;
+  } else {
+    SimtGemmArgs up{sc, El, d, f, static_cast<const float*>(ctx->xp), static_cast<const float*>(ctx->w13),
+                    static_cast<const float*>(ctx->w3), ctx->b1, static_cast<float*>(ctx->h)};
+    if (launch_simt_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, up, static_cast<int>(max_mtiles), s) != cudaSuccess)
+      return COLIBRI_ERR_CUDA;
+    SimtGemmArgs dn{sc, El, f, d, static_cast<const float*>(ctx->h), static_cast<const float*>(ctx->w2), nullptr,
+                    ctx->b2, ctx->y};
+    if (launch_simt_gemm(kEpiStoreF32, dn, static_cast<int>(max_mtiles), s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  }
+  EpUnregroupArgs ug{ctx->y, static_cast<float*>(y_rows), static_cast<int>(R), d, plan};
+  if (launch_ep_unregroup(ug, ctx->num_sms, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  ctx->last_kernels = 4;
+  return COLIBRI_OK;
+}
+
+int colibri_moe_ep_combine(colibri_moe_t* ctx, const float* y_back, void* out, void* stream) {
+  if (!ctx) return COLIBRI_ERR_INVALID_ARG;
+  if (ctx->ep_size == 0) return COLIBRI_ERR_UNSUPPORTED;
+  if (ctx->last_T < 0) return COLIBRI_ERR_STATE;
+  const int T = ctx->last_T, d = ctx->cfg.d_model;
+  if (T == 0) {
+    ctx->last_kernels = 0;
+    return COLIBRI_OK;
+  }
+  if (!y_back || !out) return COLIBRI_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(y_back) | reinterpret_cast<uintptr_t>(out)) & 15) return COLIBRI_ERR_INVALID_ARG;
+  if (overlap(y_back, static_cast<size_t>(T) * ctx->k * d * 4, out, static_cast<size_t>(T) * d * ctx->out_esize))
+    return COLIBRI_ERR_INVALID_ARG;
+  if (!is_device_ptr(y_back, ctx->device) || !is_device_ptr(out, ctx->device)) return COLIBRI_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return COLIBRI_ERR_CUDA;
+  CombineArgs ca{y_back, ctx->row_of, ctx->gate, T, d, out, ctx->k};
+  if (launch_combine(ctx->cfg.out_dtype, ca, ctx->num_sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return COLIBRI_ERR_CUDA;
+  ctx->last_kernels = 1;
   return COLIBRI_OK;
 }
 

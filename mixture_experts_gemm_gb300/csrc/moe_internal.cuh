@@ -211,6 +211,46 @@ struct SimtGemmArgs {
   float* comb_out = nullptr;
 };
 
+// Expert parallelism (the experts split over several GPUs).
+struct EpPackArgs {
+  const void* x;            // [T, d]
+  const int32_t* idx;       // [T, k]
+  int32_t* row_of;          // [T, k] in: rank inside the router chunk, out: row of the send buffer
+  const int32_t* chunk_base;  // [nchunks, E] first padded row of each (chunk, expert)
+  const Sched* sched;       // the router's summary (counts, padded offsets)
+  int T, d, E, k;
+  void* send;               // [T * k, d]: rows grouped by expert, ascending token inside each
+  int32_t* send_counts;     // [E] rows per expert
+  int32_t* status;
+};
+
+// How the rows an expert rank receives (source-major blocks) map onto its padded expert segments.
+struct EpPlan {
+  int32_t n_seg;              // ep_size * El segments (<= kMaxRouted), source-major
+  int32_t El;                 // local experts
+  int32_t src[kMaxRouted];    // first received row of segment g = (source p, local expert j)
+  int32_t dst[kMaxRouted];    // its first row in Xp: offsets[j] + rows of j from sources before p
+  int32_t counts[kMaxE];      // rows per local expert
+  int32_t offsets[kMaxE + 1]; // 128-row padded segment starts
+  int32_t mstart[kMaxE + 1];  // M tiles before each local expert
+};
+
+struct EpRegroupArgs {
+  const void* recv;         // [R, d] received rows
+  void* xp;                 // Xp
+  int R;
+  int row_bytes;            // d * element size (a multiple of 16)
+  Sched* sched;             // the expert role's schedule
+  EpPlan plan;
+};
+
+struct EpUnregroupArgs {
+  const float* y;           // Y [rows, d] fp32 (padded layout)
+  float* y_out;             // [R, d] fp32 in receive order
+  int R, d;
+  EpPlan plan;
+};
+
 // Programmatic dependent launch: a kernel launched with pdl_launch may start (and run its prologue)
 // while the previous kernel on the stream drains; it must call pdl_wait() before touching anything
 // an earlier kernel wrote (pdl_wait returns once every prerequisite grid has completed and its
@@ -293,6 +333,9 @@ cudaError_t launch_decode_fused(const CUtensorMap& tmW13, const CUtensorMap& tmX
                                 cudaStream_t s);
 cudaError_t launch_decode_combine(int out_dtype, const DecodeCombineArgs& a, cudaStream_t s);
 cudaError_t launch_wait_probe(int32_t* status, uint64_t timeout_ns, cudaStream_t s);
+cudaError_t launch_ep_pack(int dtype, const EpPackArgs& a, cudaStream_t s);
+cudaError_t launch_ep_regroup(const EpRegroupArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_ep_unregroup(const EpUnregroupArgs& a, int num_sms, cudaStream_t s);
 int tc_gemm_block_n();
 int tc_gemm_threads();
 
