@@ -87,6 +87,12 @@ struct colibri_moe {
   float* partial = nullptr;  // decode partial sums [splits][n_pad][E * rows]
   uint32_t* tile_done = nullptr;  // cooperative decode kernel: items done per down-projection tile
   float* split_part = nullptr;    // split router: partial logits of small batches
+  // dispatch fused into the router (bf16 prefill path): in-chunk ranks, grid barrier counter, and
+  // the most chunks each router variant runs with every CTA resident (0: never fused)
+  int32_t* rank_buf = nullptr;    // [max_tokens, S]
+  uint32_t* route_sync = nullptr;
+  int fused_split_chunks = 0;
+  bool fused_dispatch = true;
   int decode_max_t = 0;
   bool pair_gemm = false;    // prefill GEMMs on CTA pairs (256x256 tiles)
   bool fuse_combine = true;  // two-slot fp32 layers: gate-weighted combine inside the down GEMM
@@ -213,6 +219,13 @@ bool env_fuse_combine() {
 bool env_gather_a() {
   const char* s = std::getenv("COLIBRI_MOE_GATHER");
   return s && std::strcmp(s, "fused") == 0;
+}
+
+// bf16 prefill batches of 9..1024 tokens run the dispatch inside the split router (no separate
+// dispatch kernel) unless COLIBRI_MOE_DISPATCH=separate.
+bool env_fused_dispatch() {
+  const char* s = std::getenv("COLIBRI_MOE_DISPATCH");
+  return !(s && std::strcmp(s, "separate") == 0);
 }
 
 // CTA-pair GEMMs hand out tiles in index order at run time unless COLIBRI_MOE_TILE_ORDER=static.
@@ -396,6 +409,8 @@ static int create_impl(const colibri_moe_config_t* cfg, int device, int ep_rank,
                                   : 0;
   const size_t o_part = carve(part_floats * 4);
   const size_t o_tiles = carve((d / 128 + 1) * sizeof(uint32_t));
+  const size_t o_rank = carve(S * T * 4);
+  const size_t o_rsync = carve(sizeof(uint32_t));
   const size_t o_spart = carve(static_cast<size_t>(kRouterSplitMaxChunks) * router_split_factor() * kRouterChunk *
                                16 * sizeof(float));
   size_t o_xs[kHostSlots], o_os[kHostSlots];
@@ -423,6 +438,8 @@ static int create_impl(const colibri_moe_config_t* cfg, int device, int ep_rank,
   c->ep_sched = ep_size > 0 ? reinterpret_cast<Sched*>(b + o_ep_sched) : nullptr;
   c->partial = part_floats > 0 ? reinterpret_cast<float*>(b + o_part) : nullptr;
   c->tile_done = reinterpret_cast<uint32_t*>(b + o_tiles);
+  c->rank_buf = reinterpret_cast<int32_t*>(b + o_rank);
+  c->route_sync = reinterpret_cast<uint32_t*>(b + o_rsync);
   c->split_part = reinterpret_cast<float*>(b + o_spart);
   for (int i = 0; i < kHostSlots; ++i) {
     c->x_stage[i] = b + o_xs[i];
@@ -454,6 +471,10 @@ static int create_impl(const colibri_moe_config_t* cfg, int device, int ep_rank,
   if (c->pair_gemm) {
     c->pair_ctas = pair_gemm_max_ctas();
     if (c->pair_ctas < 2) c->pair_gemm = false;
+  }
+  c->fused_dispatch = env_fused_dispatch() && cfg->dtype == COLIBRI_DTYPE_BF16 && ep_size == 0;
+  if (c->fused_dispatch) {
+    c->fused_split_chunks = router_split_fused_max_chunks(cfg->num_experts, sms);
   }
   c->decode_fused = env_decode_fused() && c->decode_max_t > 0;
   c->direct_h = env_direct_h();
@@ -603,21 +624,44 @@ int colibri_moe_load_weights(colibri_moe_t* ctx, const colibri_moe_weights_t* w,
 // The router variant for this batch.  Large bf16 batches stream x into the router through shared
 // memory by TMA (a per-call map of the caller's buffer); small ones read it straight from global
 // memory.
+enum RouterKind { kRouterSplit, kRouterTma, kRouterPlain };
+
+static RouterKind router_kind(const colibri_moe_t* ctx, int32_t T, int nchunks) {
+  const bool bf16 = ctx->cfg.dtype == COLIBRI_DTYPE_BF16;
+  const int d = ctx->cfg.d_model;
+  // 9..1024 tokens: the hidden dimension split over several CTAs per chunk (fewer tokens gain
+  // nothing from it: one CTA's loads already take one or two rounds; more fill the GPU anyway)
+  if (bf16 && T > kRouterSplitMinT && nchunks <= kRouterSplitMaxChunks && d % (32 * router_split_factor()) == 0)
+    return kRouterSplit;
+  if (bf16 && T >= kRouterTmaMinT && d % router_tma_cols() == 0) return kRouterTma;
+  return kRouterPlain;
+}
+
+// Whether this batch's router runs the dispatch itself: the split router (9..1024 tokens) with every
+// CTA of its grid resident at once.  (Larger batches keep the separate dispatch kernel: measured on
+// GB300, its thousands of warps copy the rows faster than one router CTA per chunk after the
+// barrier -- Mixtral prefill router + dispatch 59 -> 68 us, skewed 16-expert layer no gain -- while
+// at 512 tokens the fused form saves the launch and the last-CTA scan: 1.3B-class step 130.7 -> 128.5 us.)
+static bool can_fuse_dispatch(const colibri_moe_t* ctx, RouterKind kind, int nchunks) {
+  return ctx->fused_dispatch && kind == kRouterSplit && nchunks <= ctx->fused_split_chunks;
+}
+
 static int enqueue_router(const colibri_moe_t* ctx, const RouterArgs& ra, const void* x, int32_t T, int nchunks,
                           cudaStream_t s) {
   const colibri_moe_config_t& c = ctx->cfg;
-  const bool bf16 = c.dtype == COLIBRI_DTYPE_BF16;
   const int d = c.d_model;
+  const RouterKind kind = router_kind(ctx, T, nchunks);
+  const bool fused = ra.xp != nullptr;  // the caller checked can_fuse_dispatch
   CUtensorMap tm_xr;
-  if (bf16 && T > kRouterSplitMinT && nchunks <= kRouterSplitMaxChunks && d % (32 * router_split_factor()) == 0) {
-    // 9..1024 tokens: the hidden dimension split over several CTAs per chunk (fewer tokens gain
-    // nothing from it: one CTA's loads already take one or two rounds; more fill the GPU anyway)
-    if (launch_router_split(ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
-  } else if (bf16 && T >= kRouterTmaMinT && d % router_tma_cols() == 0 &&
-             make_tmap(&tm_xr, x, d, static_cast<uint64_t>(T), kRouterChunk)) {
+  if (kind == kRouterSplit) {
+    if ((fused ? launch_router_split_fused(ra, nchunks, s) : launch_router_split(ra, nchunks, s)) != cudaSuccess)
+      return COLIBRI_ERR_CUDA;
+  } else if (fused) {
+    return COLIBRI_ERR_CUDA;  // (never: can_fuse_dispatch admits the split router only)
+  } else if (kind == kRouterTma && make_tmap(&tm_xr, x, d, static_cast<uint64_t>(T), kRouterChunk)) {
     if (launch_router_tma(tm_xr, ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
-  } else if (launch_router(c.dtype, ra, nchunks, s) != cudaSuccess) {
-    return COLIBRI_ERR_CUDA;
+  } else {
+    if (launch_router(c.dtype, ra, nchunks, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   }
   return COLIBRI_OK;
 }
@@ -654,10 +698,23 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   // the fp32 (SIMT) path.
   float4* const clear_in_gemm = fuse && !gather_a ? static_cast<float4*>(out) : nullptr;
   const int64_t out_vec4 = static_cast<int64_t>(T) * d / 4;
+  // bf16 prefill batches of 9..1024 tokens: the split router writes the dispatch (Xp rows and row
+  // bookkeeping) itself; no dispatch kernel then runs
+  const bool fused_disp = bf16 && !decode && !gather_a && can_fuse_dispatch(ctx, router_kind(ctx, T, nchunks), nchunks);
   RouterArgs ra{x, ctx->w_router, ctx->b_router, T, d, c.num_experts, ctx->dchunk, ctx->idx, ctx->gate,
-                ctx->row_of, ctx->hist, ctx->sched, ctx->k, c.gate_mode, c.has_shared_expert, ctx->S, ctx->Ex,
+                fused_disp ? ctx->rank_buf : ctx->row_of, ctx->hist, ctx->sched, ctx->k, c.gate_mode,
+                c.has_shared_expert, ctx->S, ctx->Ex,
                 fuse && (gather_a || !bf16) ? static_cast<float*>(out) : nullptr, ctx->tile_done, d / 128,
                 ctx->split_part};
+  if (fused_disp) {
+    ra.xp = ctx->xp;
+    ra.row_of = ctx->row_of;
+    ra.token_of_row = ctx->tok_of_row;
+    ra.gate_of_row = fuse ? ctx->gate_of_row : nullptr;
+    ra.rows_alloc = ctx->rows_alloc;
+    ra.route_sync = ctx->route_sync;
+    ra.timeout_ns = ctx->timeout_ns;
+  }
   const int rrc = enqueue_router(ctx, ra, x, T, nchunks, s);
   if (rrc) return rrc;
   mark(1);
@@ -683,7 +740,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     ctx->last_kernels = 2;
     return COLIBRI_OK;
   }
-  if (launch_gather(c.dtype, ga, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  if (!fused_disp && launch_gather(c.dtype, ga, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   mark(2);
   if (decode) {
     // decode-sized batch: weight-streaming GEMMs with K splits, deterministic reductions
@@ -716,7 +773,8 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     const int64_t max_pairs = (max_mtiles + E + 1) / 2;
     GemmArgs up{ctx->sched, E, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns,
                 &ctx->sched->status, ctx->tok_of_row, nullptr, x,
-                ctx->dynamic_tiles ? &ctx->sched->tile_ctr[0] : nullptr, clear_in_gemm, out_vec4};
+                ctx->dynamic_tiles ? &ctx->sched->tile_ctr[0] : nullptr, clear_in_gemm, out_vec4,
+                fused_disp ? ctx->route_sync : nullptr};
     int64_t ctas = 2 * max_pairs * up.n_tiles;
     int grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
     if (launch_pair_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, gather_a, ctx->tm_xp, ctx->tm_w13_dec, up, grid, s) !=
@@ -734,7 +792,8 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   } else if (bf16) {
     const int bn = tc_gemm_block_n();
     GemmArgs up{ctx->sched, E, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns,
-                &ctx->sched->status, ctx->tok_of_row, nullptr, x, nullptr, clear_in_gemm, out_vec4};
+                &ctx->sched->status, ctx->tok_of_row, nullptr, x, nullptr, clear_in_gemm, out_vec4,
+                fused_disp ? ctx->route_sync : nullptr};
     int64_t tiles = max_mtiles * up.n_tiles;
     int grid = static_cast<int>(tiles < ctx->num_sms ? tiles : ctx->num_sms);
     if (launch_tc_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, gather_a, ctx->tm_xp, ctx->tm_w13, up, grid, s) !=
@@ -765,7 +824,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   }
   mark(5);
   ctx->last_T = T;
-  ctx->last_kernels = fuse ? 4 : 5;
+  ctx->last_kernels = (fuse ? 4 : 5) - (fused_disp ? 1 : 0);
   return COLIBRI_OK;
 }
 

@@ -116,6 +116,8 @@ __global__ void __launch_bounds__(GA ? NUM_THREADS_GA : NUM_THREADS_ZERO, 1)
     tmem_relinquish();
   }
   pdl_wait();  // the routing summary and the A operand come from earlier kernels
+  // the router (whose dispatch is fused) has completed: its grid barrier counter is free again
+  if (a.clear_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *a.clear_word = 0u;
   if (threadIdx.x < kMaxE) s_counts[threadIdx.x] = threadIdx.x < E ? a.sched->counts[threadIdx.x] : 0;
   if (threadIdx.x < kMaxE + 1) {
     s_offsets[threadIdx.x] = threadIdx.x <= E ? a.sched->offsets[threadIdx.x] : 0;

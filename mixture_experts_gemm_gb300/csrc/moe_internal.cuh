@@ -32,6 +32,7 @@ enum : int32_t {
   kStatusTimeoutGridSync = 1 << 4,
   kStatusTimeoutRouter = 1 << 5,
   kStatusWaitProbe = 1 << 6,  // the failure-detection probe's wait ran out (as it is meant to)
+  kStatusTimeoutRouteSync = 1 << 7,  // the router's grid barrier (fused dispatch) gave up
 };
 
 // Routing summary in device memory.  Written by the last CTA of the router kernel, read by
@@ -69,6 +70,18 @@ struct RouterArgs {
   uint32_t* tile_done;     // cooperative decode kernel's per-tile counters, cleared by the last CTA
   int n_tile_done;
   float* split_part;       // split router: partial logits [chunks][splits][32][EMAX], or nullptr
+  // Dispatch fused into the split router (bf16 prefill batches of 9..1024 tokens; cooperative launch,
+  // every CTA resident): each CTA finds its chunk's rows from all chunks' histograms after a grid
+  // barrier and writes Xp,
+  // row_of, token_of_row and gate_of_row itself -- no last-CTA scan, no separate dispatch kernel.
+  // `rank` then holds only the in-chunk ranks (a buffer of its own), row_of the rows.
+  void* xp;                // [rows_alloc, d], or nullptr: dispatch not fused
+  int32_t* row_of;         // [T, S]
+  int32_t* token_of_row;   // [rows_alloc]
+  float* gate_of_row;      // [rows_alloc] or nullptr
+  int64_t rows_alloc;
+  uint32_t* route_sync;    // grid barrier arrivals: zero at launch, cleared again by the up GEMM
+  uint64_t timeout_ns;     // bound on the grid barrier
 };
 
 struct GatherArgs {
@@ -120,6 +133,8 @@ struct GemmArgs {
   uint32_t* tile_ctr;           // CTA-pair kernel: next tile index to hand out (cleared by the router)
   float4* zero_out;             // up GEMM with the combine fused downstream: out cleared by two extra
   int64_t zero_vec4;            //   warps per CTA (zero_vec4 float4s), else nullptr
+  uint32_t* clear_word;         // up GEMM after a router with fused dispatch: its grid barrier counter,
+                                //   set to zero by CTA 0 once the router has completed, else nullptr
 };
 
 constexpr int kZeroWarp0 = 6;   // the clearing warps follow producer, MMA and the 4 epilogue warps
@@ -308,6 +323,10 @@ cudaError_t launch_router(int dtype, const RouterArgs& a, int nchunks, cudaStrea
 cudaError_t launch_router_tma(const CUtensorMap& tmx, const RouterArgs& a, int nchunks, cudaStream_t s);
 int router_tma_cols();  // the TMA-staged router needs d to be a multiple of this
 cudaError_t launch_router_split(const RouterArgs& a, int nchunks, cudaStream_t s);
+// The split router with the dispatch fused (a.xp set): a cooperative launch; the most chunks whose
+// CTAs are all resident at once on the current device (0 on error).
+cudaError_t launch_router_split_fused(const RouterArgs& a, int nchunks, cudaStream_t s);
+int router_split_fused_max_chunks(int E, int num_sms);
 int router_split_factor();  // CTAs per chunk of the split router (d must be a multiple of 32 x this)
 cudaError_t launch_gather(int dtype, const GatherArgs& a, cudaStream_t s);
 cudaError_t launch_combine(int out_dtype, const CombineArgs& a, int num_sms, cudaStream_t s);

@@ -16,6 +16,8 @@
 //   router_tma_kernel       bf16, >= 1024 tokens: x staged through shared memory by TMA.
 // Per-chunk histograms make the dispatch deterministic: atomics only count finished CTAs, and every
 // row index comes from a scan in token order.
+#include <utility>
+
 #include "moe_internal.cuh"
 
 namespace colibri {
@@ -142,8 +144,10 @@ __device__ void scan_offsets(const RouterArgs& a, int nchunks) {
 // After the chunk's routing is in s_idx (a __syncthreads() ago): in-chunk ranks, the chunk's expert
 // histogram, and -- in the CTA that finishes last -- the scan of all histograms.  S slots per token
 // (k routed experts, then the shared expert when present); a token names each expert at most once.
+// With the dispatch fused (a.xp set) it stops after the histogram (the ranks also go to s_rank, when
+// given): fused_dispatch takes over.
 __device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[kMaxSlots], int valid, int chunk_t0,
-                             int chunk = blockIdx.x, int nchunks = gridDim.x) {
+                             int chunk = blockIdx.x, int nchunks = gridDim.x, int* s_rank = nullptr) {
   __shared__ int s_last;
   // The chunk's (token, slot) entries in token-major order, one per thread of the first warps.  An
   // entry's rank is the number of earlier entries naming its expert (no token names an expert twice,
@@ -168,16 +172,18 @@ __device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[kMaxSlots],
     int r = __popc(same & ((1u << lane) - 1u));
     for (int w = 0; w < warp; ++w) r += s_wcnt[w][e_ent];
     a.rank[(size_t)S * chunk_t0 + threadIdx.x] = r;
+    if (s_rank) s_rank[threadIdx.x] = r;
   }
   __shared__ int s_cnt[kMaxE];
   if (threadIdx.x < Ex) {
     int c = 0;
     for (int w = 0; w < nw; ++w) c += s_wcnt[w][threadIdx.x];
-    if (nchunks > 1)
+    if (nchunks > 1 || a.xp)
       a.hist[(size_t)chunk * Ex + threadIdx.x] = c;
     else
       s_cnt[threadIdx.x] = c;
   }
+  if (a.xp) return;  // fused dispatch: the grid barrier and the rows follow
   if (nchunks == 1) {
     // one chunk (T <= 32, decode-sized batches): no other CTA to wait for, so the summary comes
     // straight from this CTA's counts; the chunk's first row of each expert is the expert's offset
@@ -210,6 +216,134 @@ __device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[kMaxSlots],
   if (s_last) {
     __threadfence();
     scan_offsets(a, nchunks);
+  }
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t router_now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Fused dispatch, after finish_chunk has stored this chunk's histogram (and, in the CTA that
+// completed the chunk, its ranks).  A grid barrier (every CTA of the cooperative launch arrives
+// once, a gpu-scope release; the spin an acquire, bounded), then every CTA computes its chunk's
+// first row of each expert from all chunks' counts -- the prefix over the chunks before it plus the
+// 128-row padded start of the expert, the same scan the last-CTA path does, in chunk order -- and
+// copies columns [col0, col1) of its tokens' rows of x into Xp (the row of token t, slot s =
+// first row of (chunk, e) + rank).  The `writer` CTA of a chunk also writes row_of, token_of_row and
+// gate_of_row; CTA 0 writes the routing summary.  s_rank / s_idx: the chunk's ranks and experts in
+// shared memory, or nullptr to read them from global memory (the other CTAs of a split chunk).
+template <int ESIZE>
+__device__ void fused_dispatch(const RouterArgs& a, int chunk, int nchunks, int chunk_t0, int valid,
+                               const int* s_rank, const int (*s_idx)[kMaxSlots], int col0, int col1, bool writer) {
+  __shared__ int s_before[kMaxE], s_total[kMaxE], s_off[kMaxE + 1];
+  __shared__ int s_row[kRouterChunk * kMaxSlots];
+  __shared__ int s_go;
+  const int Ex = a.Ex, S = a.S;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.route_sync) : "memory");
+    const uint32_t target = gridDim.x;
+    int go = 1;
+    if (ld_acquire_u32(a.route_sync) < target) {
+      const uint64_t t0 = router_now_ns();
+      while (ld_acquire_u32(a.route_sync) < target) {
+        if (router_now_ns() - t0 > a.timeout_ns) {
+          atomicOr(&a.sched->status, kStatusTimeoutRouteSync);
+          go = 0;
+          break;
+        }
+      }
+    }
+    s_go = go;
+  }
+  __syncthreads();
+  if (!s_go) return;
+  // per expert: rows of all chunks, and of the chunks before this one (one warp per expert)
+  for (int e = warp; e < Ex; e += kRouterThreads / 32) {
+    int tot = 0, bef = 0;
+    for (int c = lane; c < nchunks; c += 32) {
+      const int v = __ldcg(&a.hist[(size_t)c * Ex + e]);
+      tot += v;
+      bef += c < chunk ? v : 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      bef += __shfl_xor_sync(0xffffffffu, bef, o);
+    }
+    if (lane == 0) {
+      s_total[e] = tot;
+      s_before[e] = bef;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int off = 0, mt = 0;
+    const bool summary = blockIdx.x == 0;
+    for (int e = 0; e < Ex; ++e) {
+      s_off[e] = off;
+      const int tiles = (s_total[e] + kRowTile - 1) / kRowTile;
+      if (summary) {
+        a.sched->counts[e] = s_total[e];
+        a.sched->offsets[e] = off;
+        a.sched->mtile_start[e] = mt;
+      }
+      off += tiles * kRowTile;
+      mt += tiles;
+    }
+    s_off[Ex] = off;
+    if (summary) {
+      a.sched->offsets[Ex] = off;
+      a.sched->mtile_start[Ex] = mt;
+      a.sched->ticket = 0;
+      a.sched->grid_sync = 0;
+      a.sched->tile_ctr[0] = a.sched->tile_ctr[1] = 0;
+      for (int i = 0; i < a.n_tile_done; ++i) a.tile_done[i] = 0;
+    }
+  }
+  __syncthreads();
+  // rows of the chunk's (token, slot) entries
+  bool bad = false;
+  for (int i = threadIdx.x; i < valid * S; i += kRouterThreads) {
+    const int t = i / S, sl = i - t * S;
+    const size_t gi = (size_t)S * chunk_t0 + i;
+    const int e = s_idx ? s_idx[t][sl] : __ldcg(&a.idx[gi]);
+    const int r = s_rank ? s_rank[i] : __ldcg(&a.rank[gi]);
+    const int row = s_off[e] + s_before[e] + r;
+    const bool ok = e >= 0 && e < Ex && row >= 0 && row < a.rows_alloc;
+    bad |= !ok;
+    s_row[i] = ok ? row : -1;
+    if (writer && ok) {
+      a.row_of[gi] = row;
+      a.token_of_row[row] = chunk_t0 + t;
+      if (a.gate_of_row) a.gate_of_row[row] = a.gate[gi];
+    }
+  }
+  if (bad) atomicOr(&a.sched->status, kStatusBadRow);
+  __syncthreads();
+  // copy: 16-byte vectors of columns [col0, col1) of every valid token row to its S rows of Xp
+  const int vpr = (col1 - col0) * ESIZE / 16;  // vectors per row
+  const size_t row_bytes = (size_t)a.d * ESIZE;
+  const char* xb = static_cast<const char*>(a.x) + (size_t)col0 * ESIZE;
+  char* pb = static_cast<char*>(a.xp) + (size_t)col0 * ESIZE;
+  for (int i = threadIdx.x; i < valid * vpr; i += kRouterThreads) {
+    const int t = i / vpr, v = i - t * vpr;
+    const uint4 q = __ldg(reinterpret_cast<const uint4*>(xb + (size_t)(chunk_t0 + t) * row_bytes) + v);
+#pragma unroll
+    for (int sl = 0; sl < kMaxSlots; ++sl)
+      if (sl < S) {
+        const int row = s_row[t * S + sl];
+        if (row >= 0) reinterpret_cast<uint4*>(pb + (size_t)row * row_bytes)[v] = q;
+      }
   }
 }
 
@@ -648,7 +782,11 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_split_kernel(RouterA
     if (s_lastsplit) a.sched->split_ticket[chunk] = 0;  // ready for the next forward
   }
   __syncthreads();
-  if (!s_lastsplit) return;
+  if (!s_lastsplit) {
+    // fused dispatch: this CTA copies its own columns of the chunk's rows once all chunks are routed
+    if (a.xp) fused_dispatch<2>(a, chunk, nchunks, chunk_t0, valid, nullptr, nullptr, cb0 * 32, cb1 * 32, false);
+    return;
+  }
   __threadfence();
   // every thread sums (row, expert) logits over the splits in split order, into s_part's space
   float(*s_logit)[EMAX] = reinterpret_cast<float(*)[EMAX]>(&s_part[0][0][0]);
@@ -671,7 +809,9 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_split_kernel(RouterA
     topk_store<EMAX>(a, L, chunk_t0 + threadIdx.x, s_idx[threadIdx.x]);
   }
   __syncthreads();
-  finish_chunk(a, s_idx, valid, chunk_t0, chunk, nchunks);
+  __shared__ int s_rank[kRouterChunk * kMaxSlots];
+  finish_chunk(a, s_idx, valid, chunk_t0, chunk, nchunks, a.xp ? s_rank : nullptr);
+  if (a.xp) fused_dispatch<2>(a, chunk, nchunks, chunk_t0, valid, s_rank, s_idx, cb0 * 32, cb1 * 32, true);
 }
 
 // Large batches: the same logits GEMM with x streamed through shared memory by TMA.  The CTA's 32
@@ -858,6 +998,35 @@ __global__ void __launch_bounds__(kRouterThreads, 2)
   finish_chunk(a, s_idx, valid, chunk_t0);
 }
 
+// Cooperative launch (every CTA resident: the fused dispatch's grid barrier), with programmatic
+// dependent launch like the other kernels.
+template <typename... KArgs, typename... Args>
+cudaError_t coop_launch(void (*kernel)(KArgs...), int grid, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kRouterThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+int resident_per_sm(const void* kernel, size_t smem) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kRouterThreads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return per_sm;
+}
+
 template <typename Tin, int EMAX>
 cudaError_t launch_router_t(const RouterArgs& a, int nchunks, cudaStream_t s) {
   const int smem = EMAX * a.dchunk * (int)sizeof(Tin);
@@ -905,6 +1074,17 @@ cudaError_t launch_router_split(const RouterArgs& a, int nchunks, cudaStream_t s
   return pdl_launch(router_split_kernel<2>, dim3(nchunks * kRsSplit), dim3(kRouterThreads), 0, s, a);
 }
 int router_split_factor() { return kRsSplit; }
+
+cudaError_t launch_router_split_fused(const RouterArgs& a, int nchunks, cudaStream_t s) {
+  if (a.E <= 8) return coop_launch(router_split_kernel<1>, nchunks * kRsSplit, 0, s, a);
+  return coop_launch(router_split_kernel<2>, nchunks * kRsSplit, 0, s, a);
+}
+
+int router_split_fused_max_chunks(int E, int num_sms) {
+  const void* k = E <= 8 ? reinterpret_cast<const void*>(router_split_kernel<1>)
+                         : reinterpret_cast<const void*>(router_split_kernel<2>);
+  return resident_per_sm(k, 0) * num_sms / kRsSplit;
+}
 
 cudaError_t launch_router(int dtype, const RouterArgs& a, int nchunks, cudaStream_t s) {
   if (dtype == 0) {

@@ -375,6 +375,41 @@ def test_fused_combine_fp32_simt_equals_separate_combine(T, monkeypatch):
     assert np.array_equal(out_f, out_s)
 
 
+@pytest.mark.parametrize("case", ["split-t9", "split-t300-ragged", "split-t1024-e16-k4-shared", "split-t1000-e16",
+                                  "tma-t1100", "plain-t8"])
+def test_dispatch_in_the_router_equals_the_dispatch_kernel(case, monkeypatch):
+    """bf16 prefill batches of 9..1024 tokens write the dispatch (Xp rows, row_of, token_of_row) inside
+    the split router after a grid barrier, each CTA scanning all chunks' counts itself and copying
+    its own columns; the result must be bit for bit the separate dispatch kernel's (rows, Xp,
+    output).  Larger batches (the TMA router) and batches of up to 8 tokens (one CTA reading x
+    directly) keep the separate kernel."""
+    T, d, E, k, shared = {"split-t9": (9, 512, 8, 2, False), "split-t300-ragged": (300, 768, 6, 2, False),
+                          "split-t1024-e16-k4-shared": (1024, 256, 16, 4, True),
+                          "split-t1000-e16": (1000, 2048, 16, 2, False), "tma-t1100": (1100, 512, 8, 2, False),
+                          "plain-t8": (8, 512, 8, 2, False)}[case]
+    monkeypatch.setenv("COLIBRI_MOE_DECODE_MAX_T", "0")
+    shape = testgen.LayerShape("fused-dispatch", T, d, 256, E, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True,
+                               top_k=k, shared_expert=shared)
+    li = testgen.make_inputs(shape)
+    layer_f, out_f, r_f, ref, _ = _full_check(li)
+    fused = layer_f.last_kernel_count() == (3 if k == 2 and not shared else 4)
+    assert fused == case.startswith("split"), layer_f.last_kernel_count()
+    monkeypatch.setenv("COLIBRI_MOE_DISPATCH", "separate")
+    layer_s = make_layer(li)
+    out_s, r_s = run(layer_s, x_device(li))
+    for key in r_f:
+        assert np.array_equal(r_f[key], r_s[key]), key
+    assert np.array_equal(out_f, out_s)
+    xp_f, xp_s = layer_f.debug_tensor(0), layer_s.debug_tensor(0)
+    tok_f, tok_s = layer_f.debug_tensor(3).cpu().numpy(), layer_s.debug_tensor(3).cpu().numpy()
+    rows = r_f["row_of"].ravel()
+    assert np.array_equal(tok_f[rows], tok_s[rows])
+    assert np.array_equal(tok_f[rows], np.repeat(np.arange(T), k))
+    idx_rows = torch.from_numpy(rows.astype(np.int64)).cuda()
+    assert torch.equal(xp_f[idx_rows], xp_s[idx_rows])
+    assert layer_f.device_status() == 0 and layer_s.device_status() == 0
+
+
 @pytest.mark.parametrize("gemm", ["2sm", "1sm"])
 def test_gathered_a_rows_equal_copied_xp(gemm, monkeypatch):
     """The up GEMM reading its A rows from x through token_of_row (cp.async gather warps) multiplies the same
@@ -544,7 +579,7 @@ def test_decode_limit_follows_the_expert_size(mixtral):
     """Default decode limit: 128 tokens for experts of >= 2^25 weights per matrix (the Mixtral
     shape), 64 for smaller ones, where the grouped GEMMs are as fast from ~64-96 tokens on."""
     li, layer, L = mixtral
-    for T, kernels in ((100, 2), (128, 2), (129, 4)):
+    for T, kernels in ((100, 2), (128, 2), (129, 3)):
         out, r = run(layer, x_device(li, T))
         assert layer.last_kernel_count() == kernels, T
     # a token's output does not depend on the rest of its batch: the first 129 rows of the oracle's
@@ -555,7 +590,7 @@ def test_decode_limit_follows_the_expert_size(mixtral):
     small = testgen.make_inputs(testgen.LayerShape("limit-small", 100, 512, 384, 8, testgen.ACT_SWIGLU, "bf16"))
     layer_s = make_layer(small)
     run(layer_s, x_device(small))
-    assert layer_s.last_kernel_count() == 4
+    assert layer_s.last_kernel_count() == 3   # router with the dispatch fused, up GEMM, down GEMM + combine
 
 
 @pytest.mark.parametrize("T", testgen.DECODE_TOKENS)
@@ -720,7 +755,7 @@ def test_last_kernel_count_matches_the_path(monkeypatch):
     assert layer.last_kernel_count() == 0
     x = x_device(li)
     layer.forward(x)
-    assert layer.last_kernel_count() == 4          # router, dispatch, up GEMM, down GEMM + combine
+    assert layer.last_kernel_count() == 3          # router with the dispatch, up GEMM, down GEMM + combine
     layer.forward(x[:20].contiguous())
     assert layer.last_kernel_count() == 2          # decode: router + one cooperative kernel
     layer.forward(x[:0])
@@ -729,9 +764,13 @@ def test_last_kernel_count_matches_the_path(monkeypatch):
     monkeypatch.setenv("COLIBRI_MOE_DECODE_FUSED", "0")
     layer2 = make_layer(li)
     layer2.forward(x)
-    assert layer2.last_kernel_count() == 5
+    assert layer2.last_kernel_count() == 4        # router with the dispatch, up GEMM, down GEMM, combine
     layer2.forward(x[:20].contiguous())
     assert layer2.last_kernel_count() == 6        # router, dispatch, 2 x (GEMM, reduction), combine
+    monkeypatch.setenv("COLIBRI_MOE_DISPATCH", "separate")
+    layer3 = make_layer(li)
+    layer3.forward(x)
+    assert layer3.last_kernel_count() == 5        # router, dispatch, up GEMM, down GEMM, combine
     torch.cuda.synchronize()
 
 
