@@ -301,6 +301,76 @@ def other_workloads(peaks, steps, device: int):
     return res
 
 
+def ep_phases(li, shape, x, steps, device: int):
+    """Expert parallelism on this one GPU: ep_size ranks of T / ep_size tokens each (the experts split
+    in ep_size blocks), emulated in one process with the all-to-alls as device copies.  CUDA events
+    time each phase of every rank: dispatch (router + pack), experts (regroup, up GEMM, down GEMM,
+    unregroup), combine, and the copies standing in for the exchange."""
+    import numpy as np
+    import torch
+    import mixture_experts_gemm_gb300 as moe
+    from moe_check import host_weights
+    n = 2
+    T = x.shape[0] // n
+    dev = torch.device("cuda", device)
+    stream = torch.cuda.current_stream(dev)
+    w = host_weights(li)
+    El = shape.num_experts // n
+    layers = []
+    for r in range(n):
+        L = moe.MoELayer(shape.d_model, shape.d_ff, shape.num_experts, T, dtype=shape.dtype, act="swiglu",
+                         out_dtype="f32", device=device, top_k=shape.top_k, ep_rank=r, ep_size=n)
+        own = lambda lst: None if lst is None else [t if r * El <= e < (r + 1) * El else None for e, t in enumerate(lst)]
+        L.load_weights(w["w_router"], own(w["w1"]), own(w["w2"]), w3=own(w["w3"]), b_router=w["b_router"])
+        layers.append(L)
+    xs = [x[r * T:(r + 1) * T].contiguous() for r in range(n)]
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    acc = {"dispatch": 0.0, "exchange": 0.0, "experts": 0.0, "combine": 0.0}
+    rows_recv = 0
+    for it in range(steps + 3):
+        e0, e1, e2, e3, e4, e5 = ev(), ev(), ev(), ev(), ev(), ev()
+        e0.record(stream)
+        sends = [L.ep_dispatch(xr) for L, xr in zip(layers, xs)]
+        e1.record(stream)
+        counts = [sc.cpu().numpy().astype(np.int64).reshape(n, -1) for _, sc in sends]
+        per = [c.sum(axis=1) for c in counts]
+        starts = [np.concatenate([[0], np.cumsum(p)[:-1]]) for p in per]
+        e2.record(stream)
+        recv = [torch.cat([sends[p][0][int(starts[p][q]):int(starts[p][q] + per[p][q])] for p in range(n)])
+                for q in range(n)]
+        rc = [np.stack([counts[p][q] for p in range(n)]).astype(np.int32) for q in range(n)]
+        e3.record(stream)
+        ys = [layers[q].ep_experts(recv[q], rc[q]) for q in range(n)]
+        e4.record(stream)
+        backs = []
+        for p in range(n):
+            pieces = []
+            for q in range(n):
+                before = int(sum(per[s][q] for s in range(p)))
+                pieces.append(ys[q][before:before + int(per[p][q])])
+            backs.append(torch.cat(pieces))
+        e5.record(stream)
+        outs = [layers[p].ep_combine(backs[p]) for p in range(n)]
+        e6 = ev()
+        e6.record(stream)
+        torch.cuda.synchronize(dev)
+        if it >= 3:
+            acc["dispatch"] += e0.elapsed_time(e1)
+            acc["exchange"] += e2.elapsed_time(e3) + e4.elapsed_time(e5)
+            acc["experts"] += e3.elapsed_time(e4)
+            acc["combine"] += e5.elapsed_time(e6)
+            rows_recv = sum(int(r.shape[0]) for r in recv)
+    status = max(L.device_status() for L in layers)
+    for L in layers:
+        L.close()
+    us = {k: v / steps * 1e3 for k, v in acc.items()}  # all ranks, per step
+    return {"ranks": n, "tokens_per_rank": T, "experts_per_rank": El, "rows_exchanged_per_step": rows_recv,
+            "us_per_step_all_ranks": us,
+            "us_per_rank_compute": (us["dispatch"] + us["experts"] + us["combine"]) / n,
+            "steps": steps, "device_status": status,
+            "note": "ranks emulated one after another on this GPU; the exchange as device copies (NCCL unmeasured)"}
+
+
 def main():
     args = parse_args()
     import dataclasses
@@ -499,6 +569,8 @@ def main():
             extra["decode"] = decode_sweep(layer, shape, x, out, stream,
                                            float(peaks_x.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])), n_x)
         extra["workloads"] = other_workloads(peaks_x, n_x, local)
+        if shape.name == "mixtral-prefill" and shape.top_k == 2 and not shape.shared_expert and shape.gate_mode == 0:
+            extra["ep"] = ep_phases(li, shape, x, 20, local)
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -540,9 +612,11 @@ def main():
     if extra:
         line["decode"] = extra.get("decode")
         line["workloads"] = extra.get("workloads")
+        line["ep"] = extra.get("ep")
         line["extra_note"] = ("decode: the Mixtral-shaped layer's weights on the first T rows of the batch, HBM "
                               "fraction over the distinct active experts' weights; workloads: the other layers' "
-                              "step times; both timed after the main region, CUDA events around back-to-back steps")
+                              "step times; ep: the expert-parallel calls on two emulated ranks; all timed after "
+                              "the main region with CUDA events")
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
