@@ -1,7 +1,7 @@
 #!/usr/bin/env python3
 """Throughput of the MoE layer forward on GB300: tokens/s on the Mixtral-8x7B-shaped prefill layer.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME] [--T T]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME] [--T T] [--ep]
 
 One step = one colibri_moe_forward (router, gather, grouped up-GEMM, grouped down-GEMM, combine) over
 a batch of T tokens already resident in HBM.  Prints one JSON line (rank 0).  Under torchrun each
@@ -62,6 +62,9 @@ def parse_args():
     p.add_argument("--top-k", type=int, default=None, help="routed experts per token (default: the workload's, 2)")
     p.add_argument("--gate-mode", type=int, default=None, help="0 softmax over the selected experts, 1 full softmax")
     p.add_argument("--shared-expert", action="store_true", help="add an always-on shared expert")
+    p.add_argument("--ep", action="store_true",
+                   help="expert parallelism over the launched ranks (E / N experts per GPU, NCCL all-to-alls); "
+                        "each rank routes its own batch of T tokens")
     p.add_argument("--no-extra", action="store_true",
                    help="skip the decode sweep and the other workloads' step times that follow the main line")
     return p.parse_args()
@@ -371,6 +374,72 @@ def ep_phases(li, shape, x, steps, device: int):
             "note": "ranks emulated one after another on this GPU; the exchange as device copies (NCCL unmeasured)"}
 
 
+def run_ep(args, shape, T):
+    """--ep: one expert-parallel step per iteration on every rank (ep_dispatch, count and row
+    all-to-alls, ep_experts, all-to-all back, ep_combine), each rank with its own T tokens (weak
+    scaling).  Without torchrun it runs as a one-rank group (the exchange is then NCCL to itself)."""
+    import socket
+    import torch
+    import torch.distributed as dist
+    import testgen
+    import mixture_experts_gemm_gb300 as moe
+    from mixture_experts_gemm_gb300 import ep
+    from moe_check import host_weights, torch_from_bits
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if "MASTER_ADDR" in os.environ:
+        dist.init_process_group(backend="nccl", device_id=dev)
+    else:
+        with socket.socket() as so:
+            so.bind(("127.0.0.1", 0))
+            port = so.getsockname()[1]
+        dist.init_process_group(backend="nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                                device_id=dev)
+    if shape.num_experts % world or shape.shared_expert or shape.dtype != "bf16":
+        raise SystemExit("--ep needs E divisible by the number of ranks, bf16 and no shared expert")
+    li = testgen.make_inputs(shape.with_T(T * world), want_f32=False)
+    El = shape.num_experts // world
+    layer = moe.MoELayer(shape.d_model, shape.d_ff, shape.num_experts, T, dtype="bf16",
+                         act="swiglu" if shape.act == testgen.ACT_SWIGLU else "relu_bias",
+                         has_router_bias=shape.zipf_router_bias, out_dtype="f32", device=local, top_k=shape.top_k,
+                         gate_mode=shape.gate_mode, ep_rank=rank, ep_size=world)
+    w = host_weights(li)
+    own = lambda lst: None if lst is None else [t if rank * El <= e < (rank + 1) * El else None
+                                                for e, t in enumerate(lst)]
+    layer.load_weights(w["w_router"], own(w["w1"]), own(w["w2"]), w3=own(w["w3"]), b_router=w["b_router"],
+                       b1=own(w["b1"]), b2=own(w["b2"]))
+    x = torch_from_bits(li.x_bits)[rank * T:(rank + 1) * T].contiguous().to(dev)
+    backend = ep.LayerEP(layer)
+    for _ in range(max(3, args.warmup)):
+        ep.ep_forward(backend, x)
+    stream = torch.cuda.current_stream(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(args.steps):
+        ep.ep_forward(backend, x)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    status = layer.device_status()
+    layer.close()
+    if rank == 0:
+        line = {"metric": METRIC, "value": whole_job_rate(world, T, args.steps, ms / 1e3), "unit": UNIT,
+                "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
+                "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": workload_desc(shape, T), "tokens_per_step_per_gpu": T,
+                           "parallelism": f"expert parallel x{world} ({El} experts per GPU, NCCL all-to-alls)"},
+                "gpu_launches": args.steps * 7, "device_status": status}
+        print(json.dumps(line), flush=True)
+    dist.destroy_process_group()
+
+
 def main():
     args = parse_args()
     import dataclasses
@@ -383,6 +452,9 @@ def main():
     T = args.T if args.T is not None else shape.T
     if args.impl == "reference":
         run_reference(args, shape, T)
+        return
+    if args.ep:
+        run_ep(args, shape, T)
         return
 
     import numpy as np
