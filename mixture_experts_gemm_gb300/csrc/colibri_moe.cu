@@ -98,6 +98,7 @@ struct colibri_moe {
   bool fuse_combine = true;  // two-slot fp32 layers: gate-weighted combine inside the down GEMM
   bool gather_a = false;     // bf16 prefill: up GEMM reads A rows from x through token_of_row
   bool dynamic_tiles = true; // CTA-pair GEMMs take tiles in index order from a shared counter
+  bool half_tiles = true;    // CTA-pair GEMMs run an expert's odd last M tile as an M=128 pair tile
   int pair_ctas = 0;         // co-resident CTAs of the pair kernel (persistent grid size)
   bool decode_fused = true;  // decode batches: one cooperative kernel after the router
   bool direct_h = true;      // ... whose unsplit up projection writes H in its epilogue
@@ -119,6 +120,7 @@ struct colibri_moe {
 namespace {
 
 constexpr int kNumStages = 5;  // router, gather, up GEMM, down GEMM, combine
+constexpr int kBox64 = 64 / 16 - 1;  // tm_xp_dec / tm_h_dec entry with 64-row boxes (the pair GEMM's half tiles)
 // Cooperative decode kernel: batches up to this size combine per tile (no third grid barrier);
 // measured on GB300 at the Mixtral shape: T=1 2 us faster, T=4 even, T >= 16 slower.
 constexpr int kTileCombineMaxT = 4;
@@ -226,6 +228,13 @@ bool env_gather_a() {
 bool env_fused_dispatch() {
   const char* s = std::getenv("COLIBRI_MOE_DISPATCH");
   return !(s && std::strcmp(s, "separate") == 0);
+}
+
+// CTA-pair GEMMs compute an expert's odd last 128-row M tile as an M=128 pair tile (64 rows per
+// CTA) unless COLIBRI_MOE_PAIR_HALF=0, which pads it to a 256-row pair tile.
+bool env_half_tiles() {
+  const char* s = std::getenv("COLIBRI_MOE_PAIR_HALF");
+  return !(s && s[0] == '0');
 }
 
 // CTA-pair GEMMs hand out tiles in index order at run time unless COLIBRI_MOE_TILE_ORDER=static.
@@ -353,6 +362,7 @@ static int create_impl(const colibri_moe_config_t* cfg, int device, int ep_rank,
   c->fuse_combine = env_fuse_combine();
   c->gather_a = env_gather_a();
   c->dynamic_tiles = env_dynamic_tiles();
+  c->half_tiles = env_half_tiles();
   const int64_t d = cfg->d_model, f = cfg->d_ff, E = cfg->num_experts, T = cfg->max_tokens;
   c->esize = cfg->dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
   c->out_esize = cfg->out_dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
@@ -774,19 +784,21 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     GemmArgs up{ctx->sched, E, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns,
                 &ctx->sched->status, ctx->tok_of_row, nullptr, x,
                 ctx->dynamic_tiles ? &ctx->sched->tile_ctr[0] : nullptr, clear_in_gemm, out_vec4,
-                fused_disp ? ctx->route_sync : nullptr};
+                fused_disp ? ctx->route_sync : nullptr, ctx->half_tiles ? 1 : 0};
     int64_t ctas = 2 * max_pairs * up.n_tiles;
     int grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
-    if (launch_pair_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, gather_a, ctx->tm_xp, ctx->tm_w13_dec, up, grid, s) !=
+    if (launch_pair_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, gather_a, ctx->tm_xp, ctx->tm_xp_dec[kBox64], ctx->tm_w13_dec, up,
+                         grid, s) !=
         cudaSuccess)
       return COLIBRI_ERR_CUDA;
     mark(3);
     GemmArgs dn{ctx->sched, E, f, d, d / bn, fuse ? out : ctx->y, d, ctx->b2, d, ctx->timeout_ns,
                 &ctx->sched->status, ctx->tok_of_row, ctx->gate_of_row, nullptr,
-                ctx->dynamic_tiles ? &ctx->sched->tile_ctr[1] : nullptr};
+                ctx->dynamic_tiles ? &ctx->sched->tile_ctr[1] : nullptr, nullptr, 0, nullptr, ctx->half_tiles ? 1 : 0};
     ctas = 2 * max_pairs * dn.n_tiles;
     grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
-    if (launch_pair_gemm(fuse ? kEpiCombineF32 : kEpiStoreF32, false, ctx->tm_h, ctx->tm_w2_dec, dn, grid, s) !=
+    if (launch_pair_gemm(fuse ? kEpiCombineF32 : kEpiStoreF32, false, ctx->tm_h, ctx->tm_h_dec[kBox64], ctx->tm_w2_dec, dn, grid,
+                         s) !=
         cudaSuccess)
       return COLIBRI_ERR_CUDA;
   } else if (bf16) {
@@ -1039,17 +1051,18 @@ int colibri_moe_ep_experts(colibri_moe_t* ctx, const void* recv_rows, const int3
     const int bn = tc_gemm_block_n();
     const int64_t max_pairs = (max_mtiles + El + 1) / 2;
     GemmArgs up{sc, El, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns, status, nullptr, nullptr,
-                nullptr, ctx->dynamic_tiles ? &sc->tile_ctr[0] : nullptr, nullptr, 0};
+                nullptr, ctx->dynamic_tiles ? &sc->tile_ctr[0] : nullptr, nullptr, 0, nullptr, ctx->half_tiles ? 1 : 0};
     int64_t ctas = 2 * max_pairs * up.n_tiles;
     int grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
-    if (launch_pair_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, false, ctx->tm_xp, ctx->tm_w13_dec, up, grid, s) !=
+    if (launch_pair_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, false, ctx->tm_xp, ctx->tm_xp_dec[kBox64], ctx->tm_w13_dec, up,
+                         grid, s) !=
         cudaSuccess)
       return COLIBRI_ERR_CUDA;
     GemmArgs dn{sc, El, f, d, d / bn, ctx->y, d, ctx->b2, d, ctx->timeout_ns, status, nullptr, nullptr, nullptr,
-                ctx->dynamic_tiles ? &sc->tile_ctr[1] : nullptr, nullptr, 0};
+                ctx->dynamic_tiles ? &sc->tile_ctr[1] : nullptr, nullptr, 0, nullptr, ctx->half_tiles ? 1 : 0};
     ctas = 2 * max_pairs * dn.n_tiles;
     grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
-    if (launch_pair_gemm(kEpiStoreF32, false, ctx->tm_h, ctx->tm_w2_dec, dn, grid, s) != cudaSuccess)
+    if (launch_pair_gemm(kEpiStoreF32, false, ctx->tm_h, ctx->tm_h_dec[kBox64], ctx->tm_w2_dec, dn, grid, s) != cudaSuccess)
       return COLIBRI_ERR_CUDA;
   } else if (bf16) {
     const int bn = tc_gemm_block_n();

@@ -56,9 +56,14 @@ static_assert(PSTAGES % kForwarders == 0, "a stage keeps its forwarder across ri
 
 struct PairCoord {
   int e, pm, n;
+  bool half;  // the expert's odd last 128-row M tile alone: an M=128 pair tile (64 rows per CTA)
 };
 
-__device__ __forceinline__ PairCoord decode_pair(int p, const int* pstart, int E, int n_tiles) {
+// Tile p -> (expert, pair of 128-row M tiles, N tile).  An expert with an odd number of M tiles
+// ends with a pair whose second tile lies past its rows; with allow_half that pair is computed as
+// one M=128 tile instead of an M=256 tile half of padding.
+__device__ __forceinline__ PairCoord decode_pair(int p, const int* pstart, const int* mstart, int E, int n_tiles,
+                                                 bool allow_half) {
   int e = 0;
   while (e + 1 < E && pstart[e + 1] * n_tiles <= p) ++e;
   const int local = p - pstart[e] * n_tiles;
@@ -67,13 +72,23 @@ __device__ __forceinline__ PairCoord decode_pair(int p, const int* pstart, int E
   c.e = e;
   c.n = local / pme;
   c.pm = local - c.n * pme;
+  c.half = allow_half && 2 * c.pm + 1 == mstart[e + 1] - mstart[e];
   return c;
+}
+
+// Epilogue warps q and q ^ 2 of a half tile hold the two column halves of the same 32 rows (see the
+// M=128 TMEM layout in the kernel); they meet at named barrier 2 + (q & 1), 64 threads.
+__device__ __forceinline__ void pair_warps_sync(int q) {
+  if (q & 1)
+    asm volatile("bar.sync 3, 64;" ::: "memory");
+  else
+    asm volatile("bar.sync 2, 64;" ::: "memory");
 }
 
 template <int EPI, bool GA>
 __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
     tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const GemmArgs a) {
+                        const __grid_constant__ CUtensorMap tmA64, const GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -97,6 +112,7 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
   const uint32_t tqf0 = smem_u32(bars + 3 * PSTAGES + 5);     // tile queue: slot written (each CTA)
   const uint32_t tqe0 = smem_u32(bars + 3 * PSTAGES + 5 + PTQ);  // tile queue: slot read (leader's)
   const bool DYN = !GA && a.tile_ctr != nullptr;  // tiles handed out in order at run time (see below)
+  const bool HALF = !GA && a.half_tiles != 0;     // an expert's odd last M tile as an M=128 pair tile
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E;
@@ -123,7 +139,10 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
     }
     *s_abort = 0;
     fence_mbar_init();
-    if constexpr (!GA) prefetch_tmap(&tmA);
+    if constexpr (!GA) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmA64);
+    }
     prefetch_tmap(&tmB);
   }
   if (warp == 1) {
@@ -222,9 +241,12 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
       };
       int p = seq_first(sq, true), p_next = -1;
       for (; ok && p >= 0;) {
-        const PairCoord c = decode_pair(p, s_pstart, E, a.n_tiles);
-        const int a_row = s_offsets[c.e] + (2 * c.pm + static_cast<int>(rank)) * PBM;
+        const PairCoord c = decode_pair(p, s_pstart, s_mstart, E, a.n_tiles, HALF);
+        // full tile: this CTA's 128-row M tile; half tile: its 64 rows of the one M tile
+        const int a_row = c.half ? s_offsets[c.e] + 2 * c.pm * PBM + static_cast<int>(rank) * (PBM / 2)
+                                 : s_offsets[c.e] + (2 * c.pm + static_cast<int>(rank)) * PBM;
         const int b_row = c.e * a.n_per_expert + c.n * PBN + static_cast<int>(rank) * (PBN / 2);
+        const uint32_t stage_tx = GA ? 2 * PB_BYTES : (c.half ? 2 * (PA_BYTES / 2 + PB_BYTES) : 2 * PSTAGE_BYTES);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, s_abort, a.timeout_ns)) {
             ok = false;
@@ -232,12 +254,12 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
           }
           const uint32_t full_leader = mapa_shared(full0 + 8 * stage, 0);
           if (leader) {
-            mbar_arrive_expect_tx(full0 + 8 * stage, GA ? 2 * PB_BYTES : 2 * PSTAGE_BYTES);
+            mbar_arrive_expect_tx(full0 + 8 * stage, stage_tx);
             armed |= 1u << stage;
             armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           }
           if constexpr (!GA)
-            tma_load_2d_pair(smem_u32(sA + stage * PA_BYTES), &tmA, full_leader, kb * PBK, a_row);
+            tma_load_2d_pair(smem_u32(sA + stage * PA_BYTES), c.half ? &tmA64 : &tmA, full_leader, kb * PBK, a_row);
           tma_load_2d_pair(smem_u32(sB + stage * PB_BYTES), &tmB, full_leader, kb * PBK, b_row);
           if (++stage == PSTAGES) {
             stage = 0;
@@ -281,7 +303,7 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
     bool ok = true;
     auto prefetch = [&](int p) {
       if (p >= total) return;
-      const PairCoord c = decode_pair(p, s_pstart, E, a.n_tiles);
+      const PairCoord c = decode_pair(p, s_pstart, s_mstart, E, a.n_tiles, false);
       g.prefetch_tokens(a.token_of_row, s_offsets[c.e] + (2 * c.pm + static_cast<int>(rank)) * PBM,
                         s_offsets[c.e] + s_counts[c.e]);
     };
@@ -341,7 +363,8 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------------------ MMA issuer (leader only)
-      constexpr uint32_t idesc = make_idesc_bf16(2 * PBM, PBN);
+      constexpr uint32_t idesc_full = make_idesc_bf16(2 * PBM, PBN);
+      constexpr uint32_t idesc_half = make_idesc_bf16(PBM, PBN);  // M=128: 64 rows from each CTA
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       Seq sq;
@@ -353,6 +376,7 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
           break;
         }
         tc_fence_after();
+        const uint32_t idesc = decode_pair(p, s_pstart, s_mstart, E, a.n_tiles, HALF).half ? idesc_half : idesc_full;
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PBN);
         for (int kb = 0; kb < num_kb; ++kb) {
           const bool got = GA ? mbar_wait_cluster(full0 + 8 * stage, phase, s_abort, a.timeout_ns)
@@ -396,7 +420,7 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
     uint32_t acc_phase = 0;
     Seq sq;
     for (int p = seq_first(sq, lane == 0); __all_sync(0xffffffffu, sq.ok) && p >= 0; p = seq_next(sq, p, lane == 0)) {
-      const PairCoord c = decode_pair(p, s_pstart, E, a.n_tiles);
+      const PairCoord c = decode_pair(p, s_pstart, s_mstart, E, a.n_tiles, HALF);
       bool ok = mbar_wait(tfull0 + 8 * acc, acc_phase, s_abort, a.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -405,7 +429,14 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
         break;
       }
       tc_fence_after();
-      const int row0 = s_offsets[c.e] + (2 * c.pm + static_cast<int>(rank)) * PBM + q * 32;  // this warp's rows
+      // this warp's rows.  Full tile (M=256): TMEM lane l of this CTA = row l of its 128-row M tile.
+      // Half tile (M=128, measured on GB300): this CTA's 64 rows sit in lanes 0..63 with output
+      // columns 0..127 of the tile and again in lanes 64..127 with columns 128..255, both in
+      // accumulator columns 0..127 -- so warp q holds rows 32 * (q & 1) + lane, column half q >> 1.
+      const int row0 = c.half ? s_offsets[c.e] + 2 * c.pm * PBM + static_cast<int>(rank) * (PBM / 2) + (q & 1) * 32
+                              : s_offsets[c.e] + (2 * c.pm + static_cast<int>(rank)) * PBM + q * 32;
+      const int nch = c.half ? 4 : PBN / 32;          // 32-column accumulator chunks this warp drains
+      const int coff = c.half ? (q >> 1) * 128 : 0;   // first output column of the tile those hold
       const int seg_end = s_offsets[c.e] + s_counts[c.e];
       const bool valid = row0 + lane < seg_end;  // this thread's row (the TMEM lane it reads)
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * PBN);
@@ -432,6 +463,46 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
       if constexpr (EPI == kEpiSwiGLU) {
         // columns [0,128) = gate (B half of the leader), [128,256) = up (B half of the peer)
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + c.n * (PBN / 2);
+        if (c.half) {
+          // half tile: the gate values of rows 32 * (q & 1) + lane are with warp q < 2, their up values
+          // with warp q + 2, which hands each 32-column chunk over through its own staging tile
+          const uint4* stg_up = reinterpret_cast<const uint4*>(s_stage + (q ^ 2) * (32 * PSTG_LD) + lane * PSTG_LD);
+#pragma unroll 1
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t v[32];
+            tmem_ld32_sync(tbase + ch * 32, v);
+            if (q >= 2) {
+              uint4* dst = reinterpret_cast<uint4*>(stg_mine);
+#pragma unroll
+              for (int w = 0; w < 8; ++w) dst[w] = make_uint4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+              pair_warps_sync(q);  // up values in place
+              pair_warps_sync(q);  // taken by the gate warp
+            } else {
+              uint32_t u[32];
+              pair_warps_sync(q);
+#pragma unroll
+              for (int w = 0; w < 8; ++w) {
+                const uint4 t = stg_up[w];
+                u[4 * w] = t.x;
+                u[4 * w + 1] = t.y;
+                u[4 * w + 2] = t.z;
+                u[4 * w + 3] = t.w;
+              }
+              pair_warps_sync(q);
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float g0 = __uint_as_float(v[2 * i]), g1 = __uint_as_float(v[2 * i + 1]);
+                const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+                pk[i] = pack_bf16(silu_fast(g0) * u0, silu_fast(g1) * u1);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(stg_mine + 16 * (ch & 1));
+#pragma unroll
+              for (int w = 0; w < 4; ++w) dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+              if (ch & 1) write_bf16_rows(out + (ch - 1) * 32, a.ldo);
+            }
+          }
+        } else
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t g[32], u[32];
@@ -450,10 +521,10 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
           if (ch & 1) write_bf16_rows(out + (ch - 1) * 32, a.ldo);
         }
       } else if constexpr (EPI == kEpiReluBias) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + c.n * PBN;
-        const float* bias = a.bias + static_cast<size_t>(c.e) * a.out_cols + c.n * PBN;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + c.n * PBN + coff;
+        const float* bias = a.bias + static_cast<size_t>(c.e) * a.out_cols + c.n * PBN + coff;
 #pragma unroll 1
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int ch = 0; ch < nch; ++ch) {
           uint32_t v[32];
           tmem_ld32_sync(tbase + ch * 32, v);
           uint32_t pk[16];
@@ -483,14 +554,14 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
           gr[i] = __shfl_sync(0xffffffffu, my_g, 4 * i + rr);
         }
 #pragma unroll 1
-        for (int ch = 0; ch < PBN / 32; ++ch) {
+        for (int ch = 0; ch < nch; ++ch) {
           uint32_t v[32];
           tmem_ld32_sync(tbase + ch * 32, v);
           uint4* dst = reinterpret_cast<uint4*>(stg_mine);
 #pragma unroll
           for (int w = 0; w < 8; ++w) dst[w] = make_uint4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
           __syncwarp();
-          const int col = ch * 32 + 4 * cg;  // this lane's 4 columns of the chunk
+          const int col = coff + ch * 32 + 4 * cg;  // this lane's 4 columns of the chunk
           float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
           if (bias) b4 = make_float4(bias[col], bias[col + 1], bias[col + 2], bias[col + 3]);
 #pragma unroll
@@ -548,8 +619,8 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
 }
 
 template <int EPI, bool GA>
-cudaError_t launch_pair_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int grid,
-                          cudaStream_t s) {
+cudaError_t launch_pair_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmA64, const GemmArgs& a,
+                          int grid, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(GA ? PNUM_THREADS_GA : (a.zero_out ? PNUM_THREADS_ZERO : PNUM_THREADS));
@@ -564,7 +635,7 @@ cudaError_t launch_pair_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const 
   attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<EPI, GA>, tmA, tmB, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<EPI, GA>, tmA, tmB, tmA64, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -606,25 +677,26 @@ int pair_gemm_max_ctas() {
   return 2 * clusters;
 }
 
-// grid: an even number of CTAs (one pair per two SMs).  gather_a: A rows are gathered from
-// a.gather_x through a.token_of_row (up-projection epilogues only) and tmA is not read.
-cudaError_t launch_pair_gemm(int epi, bool gather_a, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                             const GemmArgs& a, int grid, cudaStream_t s) {
+// grid: an even number of CTAs (one pair per two SMs).  tmA64: the A operand with 64-row boxes (an
+// expert's odd last M tile runs as an M=128 pair tile).  gather_a: A rows are gathered from
+// a.gather_x through a.token_of_row (up-projection epilogues only) and tmA / tmA64 are not read.
+cudaError_t launch_pair_gemm(int epi, bool gather_a, const CUtensorMap& tmA, const CUtensorMap& tmA64,
+                             const CUtensorMap& tmB, const GemmArgs& a, int grid, cudaStream_t s) {
   grid &= ~1;
   if (grid <= 0) return cudaSuccess;
   switch (epi) {
     case kEpiSwiGLU:
-      return gather_a ? launch_pair_t<kEpiSwiGLU, true>(tmA, tmB, a, grid, s)
-                      : launch_pair_t<kEpiSwiGLU, false>(tmA, tmB, a, grid, s);
+      return gather_a ? launch_pair_t<kEpiSwiGLU, true>(tmA, tmB, tmA64, a, grid, s)
+                      : launch_pair_t<kEpiSwiGLU, false>(tmA, tmB, tmA64, a, grid, s);
     case kEpiReluBias:
-      return gather_a ? launch_pair_t<kEpiReluBias, true>(tmA, tmB, a, grid, s)
-                      : launch_pair_t<kEpiReluBias, false>(tmA, tmB, a, grid, s);
+      return gather_a ? launch_pair_t<kEpiReluBias, true>(tmA, tmB, tmA64, a, grid, s)
+                      : launch_pair_t<kEpiReluBias, false>(tmA, tmB, tmA64, a, grid, s);
     case kEpiCombineF32:
       if (gather_a) return cudaErrorInvalidValue;
-      return launch_pair_t<kEpiCombineF32, false>(tmA, tmB, a, grid, s);
+      return launch_pair_t<kEpiCombineF32, false>(tmA, tmB, tmA64, a, grid, s);
     default:
       if (gather_a) return cudaErrorInvalidValue;
-      return launch_pair_t<kEpiStoreF32, false>(tmA, tmB, a, grid, s);
+      return launch_pair_t<kEpiStoreF32, false>(tmA, tmB, tmA64, a, grid, s);
   }
 }
 

@@ -135,6 +135,8 @@ struct GemmArgs {
   int64_t zero_vec4;            //   warps per CTA (zero_vec4 float4s), else nullptr
   uint32_t* clear_word;         // up GEMM after a router with fused dispatch: its grid barrier counter,
                                 //   set to zero by CTA 0 once the router has completed, else nullptr
+  int half_tiles;               // CTA-pair kernel: an expert's odd last 128-row M tile runs as an M=128
+                                //   pair tile (64 rows per CTA) instead of an M=256 tile half of padding
 };
 
 constexpr int kZeroWarp0 = 6;   // the clearing warps follow producer, MMA and the 4 epilogue warps
@@ -340,8 +342,8 @@ cudaError_t prepare_tc_gemm();
 cudaError_t prepare_decode_gemm();
 cudaError_t prepare_pair_gemm();
 int pair_gemm_max_ctas();
-cudaError_t launch_pair_gemm(int epi, bool gather_a, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                             const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_pair_gemm(int epi, bool gather_a, const CUtensorMap& tmA, const CUtensorMap& tmA64,
+                             const CUtensorMap& tmB, const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_decode_gemm(const CUtensorMap& tmW, const CUtensorMap& tmX, const DecodeArgs& a, int grid,
                                cudaStream_t s);
 cudaError_t launch_decode_act(bool swiglu, const DecodeActArgs& a, cudaStream_t s);
