@@ -39,9 +39,9 @@ STAGES = ["router", "gather", "gemm_up", "gemm_down", "combine"]
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture of the kernel as it now
 # stands; None where no capture of the current kernel exists.
 DOM_EVERY = 8  # the dominant kernel is timed with events on every 8th step of the timed region
-NCU_TRAFFIC = {("mixtral-prefill", 8192, "gemm_up", "2sm"): 2.619e9, ("mixtral-prefill", 8192, "gemm_down", "2sm"): 3.022e9,
+NCU_TRAFFIC = {("mixtral-prefill", 8192, "gemm_up", "2sm"): 2.618e9, ("mixtral-prefill", 8192, "gemm_down", "2sm"): 2.816e9,
                ("mixtral-decode", 1, "gemm_up", "decode"): 0.7092e9, ("mixtral-decode", 16, "gemm_up", "decode"): 2.8339e9,
-               ("1.3b-8e", 512, "gemm_up", "2sm"): 0.3913e9}
+               ("1.3b-8e", 512, "gemm_up", "2sm"): 0.3911e9, ("1.3b-8e", 512, "gemm_down", "2sm"): 0.2076e9}
 
 
 def log(*a):
