@@ -410,6 +410,41 @@ def test_dispatch_in_the_router_equals_the_dispatch_kernel(case, monkeypatch):
     assert layer_f.device_status() == 0 and layer_s.device_status() == 0
 
 
+@pytest.mark.parametrize("case", ["swiglu-fused", "swiglu-separate", "relu-fused", "relu-separate-bf16-out"])
+def test_half_pair_tiles_equal_padded_pair_tiles(case, monkeypatch):
+    """An expert's odd last 128-row M tile runs as an M=128 CTA-pair tile (64 rows per CTA, half-row
+    epilogues, SwiGLU up values handed over through shared memory); H, Y and the output must be bit
+    for bit those of the 256-row tile padded with unused rows (COLIBRI_MOE_PAIR_HALF=0).  Row counts
+    chosen so that every expert ends on an odd tile, some with a single tile."""
+    act = testgen.ACT_SWIGLU if case.startswith("swiglu") else testgen.ACT_RELU_BIAS
+    shape = testgen.LayerShape("half-tiles", 700, 512, 512, 8, act, "bf16", zipf_router_bias=True)
+    li = testgen.make_inputs(shape)
+    out_dtype = "bf16" if case.endswith("bf16-out") else "f32"
+    if "separate" in case:
+        monkeypatch.setenv("COLIBRI_MOE_FUSED_COMBINE", "0")
+    layer_h = make_layer(li, out_dtype=out_dtype)
+    out_h, r_h = run(layer_h, x_device(li))
+    ref = oracle.OracleLayer.from_inputs(li).forward(li.x_f32)
+    check_routing(r_h, ref["logits"], ref["idx"], ref["gate"], shape.num_experts, ref["row_of"], ref["offsets_raw"])
+    rms = math.sqrt(float(np.mean(ref["out"] ** 2)))
+    # a bf16 output adds one rounding of the result: half an ulp, 2^-8 relative
+    bound = TOL_BF16 * rms + (np.abs(ref["out"]) * 2.0 ** -8 if out_dtype == "bf16" else 0.0)
+    assert np.all(np.abs(out_h - ref["out"]) <= bound)
+    counts = r_h["counts"]
+    mt = (counts + 127) // 128
+    assert (mt % 2 == 1).any(), counts          # some experts end on a half tile
+    monkeypatch.setenv("COLIBRI_MOE_PAIR_HALF", "0")
+    layer_p = make_layer(li, out_dtype=out_dtype)
+    out_p, r_p = run(layer_p, x_device(li))
+    assert np.array_equal(out_h, out_p)
+    rows = r_h["row_of"].ravel()
+    idx_rows = torch.from_numpy(rows.astype(np.int64)).cuda()
+    assert torch.equal(layer_h.debug_tensor(1)[idx_rows], layer_p.debug_tensor(1)[idx_rows])   # H
+    if "separate" in case:
+        assert torch.equal(layer_h.debug_tensor(2)[idx_rows], layer_p.debug_tensor(2)[idx_rows])  # Y
+    assert layer_h.device_status() == 0 and layer_p.device_status() == 0
+
+
 @pytest.mark.parametrize("gemm", ["2sm", "1sm"])
 def test_gathered_a_rows_equal_copied_xp(gemm, monkeypatch):
     """The up GEMM reading its A rows from x through token_of_row (cp.async gather warps) multiplies the same
