@@ -542,6 +542,7 @@ def main():
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
+    kernels_per_step = layer.last_kernel_count()  # (later legs run other batch sizes on this layer)
     lib.colibri_moe_set_stage_events(layer._h, None, 0)
     ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     dom_ms = np.array([evs[dominant].elapsed_time(evs[dominant + 1]) for evs in dom_sets])
@@ -618,11 +619,11 @@ def main():
         n_w = active + int(shape.shared_expert)
         byts = {2: n_w * n_up * shape.d_model * shape.d_ff * es,
                 3: n_w * shape.d_model * shape.d_ff * es}.get(dominant, alg["bytes"])
-        if layer.last_kernel_count() == 2:  # cooperative decode kernel: streams both projections' weights
+        if kernels_per_step == 2:  # cooperative decode kernel: streams both projections' weights
             byts = n_w * (n_up + 1) * shape.d_model * shape.d_ff * es
         ach = byts / dur / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        path = "decode" if layer.last_kernel_count() == 2 else \
+        path = "decode" if kernels_per_step == 2 else \
             ("1sm" if os.environ.get("COLIBRI_MOE_GEMM") == "1sm" else "2sm")
         roof = {"bound": "hbm", "kernel": STAGES[dominant], "achieved": ach, "peak": peak, "unit": "GB/s",
                 "frac": ach / peak, "traffic": NCU_TRAFFIC.get((shape.name, T, STAGES[dominant], path)),
@@ -676,7 +677,7 @@ def main():
                     "it runs before the timed region, so at a cooler clock it can also come out below "
                     "ms_per_step); dominant: the kernel timed for the roofline, inside the timed region"},
         "e2e": e2e,
-        "gpu_launches": args.steps * layer.last_kernel_count(),
+        "gpu_launches": args.steps * kernels_per_step,
         "clocks": clk,
         "cpu_baseline": cpu,
         "device_status": status,
