@@ -76,7 +76,25 @@ def test_null_arguments(cuda_lib):
     assert L.colibri_moe_num_stages(None, ctypes.byref(n)) == -1
     assert L.colibri_moe_last_kernel_count(None, ctypes.byref(n)) == -1
     assert L.colibri_moe_probe_wait_timeout(None, 1000, None) == -1
+    assert L.colibri_moe_ep_dispatch(None, None, 4, None, None, None) == -1
+    assert L.colibri_moe_ep_experts(None, None, None, None, None) == -1
+    assert L.colibri_moe_ep_combine(None, None, None, None) == -1
     L.colibri_moe_destroy(None)  # NULL-safe
+
+
+@pytest.mark.parametrize("ep_rank,ep_size,max_rows,kw,code", [
+    (0, 0, 64, {}, -1),                       # no ranks
+    (0, 3, 64, {}, -1),                       # 4 experts do not split over 3 ranks
+    (2, 2, 64, {}, -1),                       # rank out of range
+    (0, 2, 0, {}, -1),                        # no receive rows
+    (0, 2, 64, {"has_shared_expert": 1}, -6),  # a shared expert would run replicated on every rank
+])
+def test_ep_create_rejects_bad_partitions_without_a_device(cuda_lib, ep_rank, ep_size, max_rows, kw, code):
+    """Expert-parallel contexts check the partition before touching the GPU."""
+    import mixture_experts_gemm_gb300 as m
+    h = ctypes.c_void_p()
+    rc = m.lib().colibri_moe_ep_create(ctypes.byref(_cfg(m, **kw)), ep_rank, ep_size, max_rows, 0, ctypes.byref(h))
+    assert rc == code and h.value is None
 
 
 def test_create_without_gpu_reports_cuda_error(cuda_lib):
