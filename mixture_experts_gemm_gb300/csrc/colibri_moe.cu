@@ -1041,7 +1041,12 @@ int colibri_moe_ep_experts(colibri_moe_t* ctx, const void* recv_rows, const int3
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool bf16 = c.dtype == COLIBRI_DTYPE_BF16;
   const bool swiglu = c.act == COLIBRI_ACT_SWIGLU;
-  EpRegroupArgs rg{recv_rows, ctx->xp, static_cast<int>(R), static_cast<int>(d * ctx->esize), ctx->ep_sched, plan};
+  // CTA-pair GEMMs: the down projection writes each row straight into y_rows at its receive index
+  // (tok_of_row holds it; an expert rank has no other use for it); other kernels write Y and an
+  // unregroup kernel copies it back
+  const bool direct_y = bf16 && ctx->pair_gemm;
+  EpRegroupArgs rg{recv_rows, ctx->xp, static_cast<int>(R), static_cast<int>(d * ctx->esize), ctx->ep_sched, plan,
+                   direct_y ? ctx->tok_of_row : nullptr};
   if (launch_ep_regroup(rg, ctx->num_sms, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   int64_t max_mtiles = (R + (kRowTile - 1) * static_cast<int64_t>(El)) / kRowTile;
   if (max_mtiles > ctx->rows_alloc / kRowTile) max_mtiles = ctx->rows_alloc / kRowTile;
@@ -1058,8 +1063,9 @@ int colibri_moe_ep_experts(colibri_moe_t* ctx, const void* recv_rows, const int3
                          grid, s) !=
         cudaSuccess)
       return COLIBRI_ERR_CUDA;
-    GemmArgs dn{sc, El, f, d, d / bn, ctx->y, d, ctx->b2, d, ctx->timeout_ns, status, nullptr, nullptr, nullptr,
-                ctx->dynamic_tiles ? &sc->tile_ctr[1] : nullptr, nullptr, 0, nullptr, ctx->half_tiles ? 1 : 0};
+    GemmArgs dn{sc, El, f, d, d / bn, y_rows, d, ctx->b2, d, ctx->timeout_ns, status, nullptr, nullptr, nullptr,
+                ctx->dynamic_tiles ? &sc->tile_ctr[1] : nullptr, nullptr, 0, nullptr, ctx->half_tiles ? 1 : 0,
+                ctx->tok_of_row};
     ctas = 2 * max_pairs * dn.n_tiles;
     grid = static_cast<int>(ctas < ctx->pair_ctas ? ctas : ctx->pair_ctas);
     if (launch_pair_gemm(kEpiStoreF32, false, ctx->tm_h, ctx->tm_h_dec[kBox64], ctx->tm_w2_dec, dn, grid, s) != cudaSuccess)
@@ -1087,9 +1093,11 @@ int colibri_moe_ep_experts(colibri_moe_t* ctx, const void* recv_rows, const int3
                     ctx->b2, ctx->y};
     if (launch_simt_gemm(kEpiStoreF32, dn, static_cast<int>(max_mtiles), s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   }
-  EpUnregroupArgs ug{ctx->y, static_cast<float*>(y_rows), static_cast<int>(R), d, plan};
-  if (launch_ep_unregroup(ug, ctx->num_sms, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
-  ctx->last_kernels = 4;
+  if (!direct_y) {
+    EpUnregroupArgs ug{ctx->y, static_cast<float*>(y_rows), static_cast<int>(R), d, plan};
+    if (launch_ep_unregroup(ug, ctx->num_sms, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  }
+  ctx->last_kernels = direct_y ? 3 : 4;
   return COLIBRI_OK;
 }
 

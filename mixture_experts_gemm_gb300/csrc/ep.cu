@@ -10,7 +10,9 @@
 //   exchange:     all-to-all of the per-expert counts, then of the rows (caller's communicator)
 //   expert rank:  ep_regroup: received rows (source-major: source p, local expert j) into 128-row
 //                 padded expert segments (expert-major: j, then p) and the local schedule ->
-//                 grouped up / down GEMMs (fp32 Y) -> ep_unregroup: Y rows back to receive order
+//                 grouped up / down GEMMs; the CTA-pair down GEMM writes each fp32 row straight to its
+//                 receive position (a row map the regroup fills), other kernels write Y and
+//                 ep_unregroup copies it back to receive order
 //   exchange:     all-to-all of the output rows back to their sources
 //   source rank:  combine over the returned rows (the forward's combine kernel).
 // Every copy is a plain HBM-bound row copy: one warp per row, 16-byte vectors.
@@ -104,6 +106,7 @@ __global__ void __launch_bounds__(kEpThreads) ep_regroup_kernel(EpRegroupArgs a)
   for (int i = blockIdx.x * (kEpThreads / 32) + (threadIdx.x >> 5); i < a.R; i += warps) {
     const int g = ep_segment(a.plan, i);
     const int dst = a.plan.dst[g] + (i - a.plan.src[g]);
+    if (a.recv_of_row != nullptr && (threadIdx.x & 31) == 0) a.recv_of_row[dst] = i;
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(a.recv) + (size_t)i * a.row_bytes);
     uint4* out = reinterpret_cast<uint4*>(static_cast<char*>(a.xp) + (size_t)dst * a.row_bytes);
     for (int v = threadIdx.x & 31; v < nvec; v += 32) out[v] = __ldg(src + v);

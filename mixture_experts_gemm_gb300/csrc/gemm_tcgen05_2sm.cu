@@ -544,7 +544,9 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
         constexpr bool kCombine = EPI == kEpiCombineF32;
         const float* bias = a.bias ? a.bias + static_cast<size_t>(c.e) * a.out_cols + c.n * PBN : nullptr;
         // token and gate of the write-back side's rows (those of row 4 * i + rr sit in lane 4 * i + rr)
-        const int my_tok = kCombine && valid ? __ldcg(a.token_of_row + row0 + lane) : 0;
+        // (kEpiStoreF32 with a row map: the output row of each A row, e.g. receive order on an expert rank)
+        const int my_tok = kCombine && valid ? __ldcg(a.token_of_row + row0 + lane)
+                           : (!kCombine && a.row_map != nullptr && valid ? __ldcg(a.row_map + row0 + lane) : 0);
         const float my_g = kCombine && valid ? __ldcg(a.gate_of_row + row0 + lane) : 0.f;
         int tok[8];
         float gr[8];
@@ -581,7 +583,8 @@ __global__ void __launch_bounds__(GA ? PNUM_THREADS_GA : PNUM_THREADS_ZERO, 1)
                 red_add_v4(o, __fmul_rn(gr[i], y[0]), __fmul_rn(gr[i], y[1]), __fmul_rn(gr[i], y[2]),
                            __fmul_rn(gr[i], y[3]));
               } else {
-                float* o = static_cast<float*>(a.out) + static_cast<size_t>(row0 + 4 * i + rr) * a.ldo + c.n * PBN + col;
+                const int orow = a.row_map != nullptr ? tok[i] : row0 + 4 * i + rr;
+                float* o = static_cast<float*>(a.out) + static_cast<size_t>(orow) * a.ldo + c.n * PBN + col;
                 *reinterpret_cast<float4*>(o) = make_float4(y[0], y[1], y[2], y[3]);
               }
             }

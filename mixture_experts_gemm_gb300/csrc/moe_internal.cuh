@@ -137,6 +137,7 @@ struct GemmArgs {
                                 //   set to zero by CTA 0 once the router has completed, else nullptr
   int half_tiles;               // CTA-pair kernel: an expert's odd last 128-row M tile runs as an M=128
                                 //   pair tile (64 rows per CTA) instead of an M=256 tile half of padding
+  const int32_t* row_map;       // CTA-pair kernel, kEpiStoreF32: output row of each A row, or nullptr
 };
 
 constexpr int kZeroWarp0 = 6;   // the clearing warps follow producer, MMA and the 4 epilogue warps
@@ -259,6 +260,7 @@ struct EpRegroupArgs {
   int row_bytes;            // d * element size (a multiple of 16)
   Sched* sched;             // the expert role's schedule
   EpPlan plan;
+  int32_t* recv_of_row;     // [rows of Xp] receive index of each row it fills, or nullptr
 };
 
 struct EpUnregroupArgs {
