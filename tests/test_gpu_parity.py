@@ -689,6 +689,52 @@ def test_zero_router_gives_empty_experts_and_ties():
     assert list(r["counts"]) == [200, 200] + [0] * 6
 
 
+@pytest.mark.parametrize("dtype,T,k", [("bf16", 16, 2), ("bf16", 300, 2), ("bf16", 300, 3), ("bf16", 1500, 2),
+                                       ("bf16", 1500, 3), ("f32", 300, 2), ("f32", 300, 3)])
+def test_exact_logit_ties_go_to_the_lowest_expert_index(dtype, T, k):
+    """Router rows duplicated so that experts 2 and 5 (and 1 and 6) have equal logits for every token,
+    with a +5 bias on the four so they always lead: every token's top-k holds an exact tie.  The
+    selection must follow the lowest-index rule whatever the router kernel (decode T=16, split
+    T=300, TMA T=1500, fp32): the tied pair in ascending expert order, and with k=3 the tie that
+    straddles the last slot resolved to the lower index.  Tied experts get bit-equal gates.  Tokens
+    whose two pairs lie within 1e-4 of each other (a genuine near tie between different logits)
+    are left out of the exact comparison."""
+    E, d = 8, 512
+    shape = testgen.LayerShape(f"ties-{dtype}-{T}-{k}", T, d, 256, E, testgen.ACT_SWIGLU, dtype, top_k=k)
+    li = testgen.make_inputs(shape)
+    w = li.w_router_f32.copy()
+    w[[0, 3, 4, 7]] *= 0.01
+    w[5] = w[2]
+    w[6] = w[1]
+    li.w_router_f32 = w
+    li.w_router_bits = testgen.f32_to_bf16_bits(w) if dtype == "bf16" else None
+    if dtype == "bf16":
+        li.w_router_f32 = testgen.bf16_bits_to_f32(li.w_router_bits)
+    li.b_router = np.array([0, 5, 5, 0, 0, 5, 5, 0], dtype=np.float32)
+    layer = make_layer(li)
+    out, r = run(layer, x_device(li))
+    L = oracle.OracleLayer.from_inputs(li)
+    logits = L.router_logits(li.x_f32)
+    o_idx, o_gate = L.topk(logits)
+    assert np.array_equal(logits[:, 2], logits[:, 5]) and np.array_equal(logits[:, 1], logits[:, 6])
+    lead = np.where(logits[:, 2] > logits[:, 1], 2, 1)
+    if k == 3:
+        # the leading pair ascending, then the lower index of the other pair
+        want = np.stack([lead, np.where(lead == 2, 5, 6), np.where(lead == 2, 1, 2)], axis=1)
+    else:
+        want = np.stack([lead, np.where(lead == 2, 5, 6)], axis=1)
+    clear = np.abs(logits[:, 2] - logits[:, 1]) >= 1e-4
+    assert clear.sum() >= T * 0.9
+    assert np.array_equal(o_idx[clear], want[clear])                  # the oracle follows the rule
+    assert np.array_equal(r["idx"][clear], want[clear])               # so does the GPU
+    g = r["gate"][clear]
+    assert np.array_equal(g[:, 0], g[:, 1])                           # the tied pair's gates
+    np.testing.assert_allclose(g, o_gate[clear], rtol=0, atol=1e-5)
+    ref = L.forward(li.x_f32)
+    assert rel_err(out[clear], ref["out"][clear]) <= (TOL_F32 if dtype == "f32" else TOL_BF16)
+    assert layer.device_status() == 0
+
+
 def test_t0_is_noop_and_max_tokens():
     shape = testgen.LayerShape("edge", 256, 256, 256, 4, testgen.ACT_SWIGLU, "bf16")
     li = testgen.make_inputs(shape)
