@@ -99,6 +99,7 @@ struct colibri_moe {
   bool gather_a = false;     // bf16 prefill: up GEMM reads A rows from x through token_of_row
   bool dynamic_tiles = true; // CTA-pair GEMMs take tiles in index order from a shared counter
   bool half_tiles = true;    // CTA-pair GEMMs run an expert's odd last M tile as an M=128 pair tile
+  int wm_env = -1;           // weight-major GEMMs: -1 by batch size (wm_tile_rows), 0 never, n: token tile n
   int pair_ctas = 0;         // co-resident CTAs of the pair kernel (persistent grid size)
   bool decode_fused = true;  // decode batches: one cooperative kernel after the router
   bool direct_h = true;      // ... whose unsplit up projection writes H in its epilogue
@@ -237,6 +238,15 @@ bool env_half_tiles() {
   return !(s && s[0] == '0');
 }
 
+// Weight-major GEMMs for batches with few rows per expert: COLIBRI_MOE_WM=0 never, =n (a multiple of
+// 32 in [32, 256]) always with token tiles of n rows, unset: by batch size (wm_tile_rows).
+int env_wm() {
+  const char* s = std::getenv("COLIBRI_MOE_WM");
+  if (!s) return -1;
+  const int n = std::atoi(s);
+  return (n >= 32 && n <= 256 && n % 32 == 0) ? n : 0;
+}
+
 // CTA-pair GEMMs hand out tiles in index order at run time unless COLIBRI_MOE_TILE_ORDER=static.
 bool env_dynamic_tiles() {
   const char* s = std::getenv("COLIBRI_MOE_TILE_ORDER");
@@ -363,6 +373,7 @@ static int create_impl(const colibri_moe_config_t* cfg, int device, int ep_rank,
   c->gather_a = env_gather_a();
   c->dynamic_tiles = env_dynamic_tiles();
   c->half_tiles = env_half_tiles();
+  c->wm_env = env_wm();
   const int64_t d = cfg->d_model, f = cfg->d_ff, E = cfg->num_experts, T = cfg->max_tokens;
   c->esize = cfg->dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
   c->out_esize = cfg->out_dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
@@ -473,7 +484,8 @@ static int create_impl(const colibri_moe_config_t* cfg, int device, int ep_rank,
   }
   if (prepare_router(cfg->dtype, cfg->num_experts) != cudaSuccess ||
       (cfg->dtype == COLIBRI_DTYPE_BF16 && (prepare_tc_gemm() != cudaSuccess || prepare_decode_gemm() != cudaSuccess ||
-                                             prepare_pair_gemm() != cudaSuccess || prepare_decode_fused() != cudaSuccess))) {
+                                             prepare_pair_gemm() != cudaSuccess || prepare_wm_gemm() != cudaSuccess ||
+                                             prepare_decode_fused() != cudaSuccess))) {
     cudaGetLastError();
     colibri_moe_destroy(c);
     return COLIBRI_ERR_CUDA;
@@ -676,6 +688,22 @@ static int enqueue_router(const colibri_moe_t* ctx, const RouterArgs& ra, const 
   return COLIBRI_OK;
 }
 
+// Token tile of the weight-major GEMMs for a prefill batch of T tokens, or 0 for the CTA-pair kernel.
+// With about 256 rows or fewer per routed expert the CTA-pair kernel pads every expert to 256-row
+// tiles and half of each ring stage holds token rows; the weight-major kernel sizes its token
+// tiles to the rows (a quarter over the mean, rounded up to 32, so that most experts fit one tile)
+// and keeps more weights in flight.
+constexpr int64_t kWmMaxRows = 256;
+static int wm_tile_rows(const colibri_moe_t* ctx, int32_t T) {
+  if (ctx->wm_env >= 0) return ctx->wm_env;
+  const int64_t rows = static_cast<int64_t>(ctx->k) * T / ctx->cfg.num_experts;
+  if (rows > kWmMaxRows) return 0;
+  int64_t nt = (rows + rows / 4 + 31) / 32 * 32;
+  if (nt < 64) nt = 64;
+  if (nt > 256) nt = 256;
+  return static_cast<int>(nt);
+}
+
 static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t T, cudaStream_t s) {
   const colibri_moe_config_t& c = ctx->cfg;
   const int E = ctx->Ex, d = c.d_model, f = c.d_ff;  // scheduled experts (routed + shared)
@@ -777,7 +805,34 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     ctx->last_kernels = 6;
     return COLIBRI_OK;
   }
-  if (bf16 && ctx->pair_gemm) {
+  const int wm_nt = bf16 && ctx->pair_gemm && !gather_a ? wm_tile_rows(ctx, T) : 0;
+  if (wm_nt > 0) {
+    // weight-major CTA pairs: 256 weight rows x a token tile of at most wm_nt rows per item
+    const int64_t tok_tiles = ctx->S * static_cast<int64_t>(T) / wm_nt + E;
+    WmMaps mu, md;
+    mu.w = swiglu ? ctx->tm_w13_half : ctx->tm_w13_dec;
+    md.w = ctx->tm_w2_dec;
+    for (int i = 0; i < kWmTokMaps; ++i) {
+      mu.tok[i] = ctx->tm_xp_dec[i];
+      md.tok[i] = ctx->tm_h_dec[i];
+    }
+    GemmArgs up{ctx->sched, E, d, ctx->n_up, 0, ctx->h, f, ctx->b1, f, ctx->timeout_ns,
+                &ctx->sched->status, ctx->tok_of_row, nullptr, nullptr,
+                ctx->dynamic_tiles ? &ctx->sched->tile_ctr[0] : nullptr, clear_in_gemm, out_vec4,
+                fused_disp ? ctx->route_sync : nullptr, 0};
+    up.wm_ntok = wm_nt;
+    const int64_t ctas_up = 2 * (ctx->n_up / 256) * tok_tiles;
+    int grid = static_cast<int>(ctas_up < ctx->pair_ctas ? ctas_up : ctx->pair_ctas);
+    if (launch_wm_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, mu, up, grid, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+    mark(3);
+    GemmArgs dn{ctx->sched, E, f, d, 0, fuse ? out : ctx->y, d, ctx->b2, d, ctx->timeout_ns,
+                &ctx->sched->status, ctx->tok_of_row, ctx->gate_of_row, nullptr,
+                ctx->dynamic_tiles ? &ctx->sched->tile_ctr[1] : nullptr, nullptr, 0, nullptr, 0};
+    dn.wm_ntok = wm_nt;
+    const int64_t ctas_dn = 2 * (d / 256) * tok_tiles;
+    grid = static_cast<int>(ctas_dn < ctx->pair_ctas ? ctas_dn : ctx->pair_ctas);
+    if (launch_wm_gemm(fuse ? kEpiCombineF32 : kEpiStoreF32, md, dn, grid, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+  } else if (bf16 && ctx->pair_gemm) {
     // CTA pairs: 256-row tiles made of two 128-row tiles of one expert sharing the weight tile
     const int bn = tc_gemm_block_n();
     const int64_t max_pairs = (max_mtiles + E + 1) / 2;

@@ -138,6 +138,16 @@ struct GemmArgs {
   int half_tiles;               // CTA-pair kernel: an expert's odd last 128-row M tile runs as an M=128
                                 //   pair tile (64 rows per CTA) instead of an M=256 tile half of padding
   const int32_t* row_map;       // CTA-pair kernel, kEpiStoreF32: output row of each A row, or nullptr
+  int wm_ntok;                  // weight-major kernel: token rows per tile (a multiple of 32, <= 256)
+};
+
+// Weight-major CTA-pair GEMM (gemm_tcgen05_wm.cu): the weight operand's tensor map (128-row boxes, or
+// 64-row boxes for the SwiGLU up projection's gate / up halves) and the token operand's (Xp or H) with
+// boxes of 16, 32, ..., 128 rows: tok[i] loads 16 (i + 1) rows, half of a token tile of 32 (i + 1).
+constexpr int kWmTokMaps = 8;
+struct WmMaps {
+  CUtensorMap w;
+  CUtensorMap tok[kWmTokMaps];
 };
 
 constexpr int kZeroWarp0 = 6;   // the clearing warps follow producer, MMA and the 4 epilogue warps
@@ -344,6 +354,8 @@ cudaError_t prepare_tc_gemm();
 cudaError_t prepare_decode_gemm();
 cudaError_t prepare_pair_gemm();
 int pair_gemm_max_ctas();
+cudaError_t prepare_wm_gemm();
+cudaError_t launch_wm_gemm(int epi, const WmMaps& maps, const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_pair_gemm(int epi, bool gather_a, const CUtensorMap& tmA, const CUtensorMap& tmA64,
                              const CUtensorMap& tmB, const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_decode_gemm(const CUtensorMap& tmW, const CUtensorMap& tmX, const DecodeArgs& a, int grid,

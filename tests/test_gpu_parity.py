@@ -265,6 +265,7 @@ def test_pair_gemm_kernel(case, monkeypatch):
     """The CTA-pair (cta_group::2) grouped GEMM (the default; COLIBRI_MOE_GEMM=2sm): exact-integer
     layer bit for bit, experts with an odd number of 128-row tiles, and a skewed router."""
     monkeypatch.setenv("COLIBRI_MOE_GEMM", "2sm")
+    monkeypatch.setenv("COLIBRI_MOE_WM", "0")     # not the weight-major kernel
     if case == "int-relu":
         shape = testgen.LayerShape("pair-int", 300, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")
         li, h, y = _integer_inputs(shape, 300, lo=-1, hi=2, wlo=-1, whi=2, seed=3)
@@ -279,6 +280,77 @@ def test_pair_gemm_kernel(case, monkeypatch):
         shape = testgen.LayerShape("pair-skewed", 1500, 512, 256, 16, testgen.ACT_SWIGLU, "bf16",
                                    zipf_router_bias=True)
         _full_check(testgen.make_inputs(shape))
+
+
+@pytest.mark.parametrize("case", ["swiglu", "relu-bias", "k4-shared", "separate-combine", "bf16-out", "tiles64",
+                                  "static-order", "int-relu"])
+def test_weight_major_gemm_kernel(case, monkeypatch):
+    """The weight-major CTA-pair GEMM (weight rows on M, an expert's token rows on N in tiles of at most
+    NT rows; the default for batches of up to ~256 rows per expert) against the oracle on every row,
+    and against the CTA-pair kernel (COLIBRI_MOE_WM=0): both multiply the same bf16 values and
+    accumulate each output in fp32 in the same K order, so H and the output agree bit for bit.
+    Cases: SwiGLU (gate / up halves in two 64-row boxes), ReLU+bias with router bias, top-4 with a
+    shared expert (whose T rows span two token tiles), the separate combine (Y rows), a bf16 output,
+    64-row token tiles on 750 rows per expert (12 token tiles per weight tile), the static item order,
+    and an exact-integer layer bit for bit against int64 arithmetic."""
+    out_dtype = "bf16" if case == "bf16-out" else "f32"
+    if case == "separate-combine":
+        monkeypatch.setenv("COLIBRI_MOE_FUSED_COMBINE", "0")
+    if case == "static-order":
+        monkeypatch.setenv("COLIBRI_MOE_TILE_ORDER", "static")
+    nt = None
+    if case == "swiglu":
+        shape = testgen.LayerShape("wm-swiglu", 700, 1024, 512, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True)
+    elif case == "relu-bias":
+        shape = testgen.LayerShape("wm-relu", 500, 512, 768, 6, testgen.ACT_RELU_BIAS, "bf16", zipf_router_bias=True)
+    elif case == "k4-shared":
+        shape = testgen.LayerShape("wm-k4", 300, 512, 384, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True,
+                                   top_k=4, shared_expert=True)
+    elif case == "tiles64":
+        shape = testgen.LayerShape("wm-t64", 3000, 512, 256, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True)
+        nt = "64"
+    elif case == "int-relu":
+        shape = testgen.LayerShape("wm-int", 300, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")
+        nt = "96"
+    else:
+        shape = testgen.LayerShape(f"wm-{case}", 600, 512, 384, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True)
+    if nt:
+        monkeypatch.setenv("COLIBRI_MOE_WM", nt)
+    if case == "int-relu":
+        li, h, y = _integer_inputs(shape, 300, lo=-1, hi=2, wlo=-1, whi=2, seed=5)
+        layer = make_layer(li)
+        out, r = run(layer, x_device(li))
+        assert np.array_equal(out, y.astype(np.float64))
+        Hd = layer.debug_tensor(1).float().cpu().numpy()
+        for t in (0, 1, 150, 299):
+            assert np.array_equal(Hd[r["row_of"][t, 0]], h[t].astype(np.float32))
+        assert layer.device_status() == 0
+        return
+    li = testgen.make_inputs(shape)
+    if out_dtype == "bf16":
+        layer = make_layer(li, out_dtype="bf16")
+        out, r = run(layer, x_device(li))
+        ref = oracle.OracleLayer.from_inputs(li).forward(li.x_f32)
+        rms = math.sqrt(float(np.mean(ref["out"] ** 2)))
+        assert np.all(np.abs(out - ref["out"]) <= TOL_BF16 * rms + np.abs(ref["out"]) * 2.0 ** -8)
+    else:
+        layer, out, r, _, _ = _full_check(li)
+    monkeypatch.setenv("COLIBRI_MOE_WM", "0")
+    layer_p = make_layer(li, out_dtype=out_dtype)
+    out_p, r_p = run(layer_p, x_device(li))
+    assert np.array_equal(r["row_of"], r_p["row_of"])
+    rows = np.sort(r["row_of"].ravel())
+    if shape.shared_expert:
+        off = r["offsets"]
+        rows = np.concatenate([rows, np.arange(off[-1], off[-1] + shape.T)])
+    idx_rows = torch.from_numpy(rows.astype(np.int64)).cuda()
+    assert torch.equal(layer.debug_tensor(1)[idx_rows], layer_p.debug_tensor(1)[idx_rows])   # H
+    if case in ("separate-combine", "bf16-out"):
+        assert torch.equal(layer.debug_tensor(2)[idx_rows], layer_p.debug_tensor(2)[idx_rows])  # Y
+    assert np.array_equal(out, out_p)
+    out2, _ = run(layer, x_device(li))
+    assert np.array_equal(out, out2)
+    assert layer.device_status() == 0 and layer_p.device_status() == 0
 
 
 @pytest.mark.parametrize("case", ["int-relu", "swiglu", "skewed"])
@@ -341,11 +413,15 @@ def test_shared_expert_relu_bias_bf16_and_pair_kernel(monkeypatch):
     _full_check(li)
 
 
-@pytest.mark.parametrize("gemm", ["2sm", "1sm"])
+@pytest.mark.parametrize("gemm", ["2sm", "1sm", "wm"])
 def test_fused_combine_equals_separate_combine(gemm, monkeypatch):
     """Two slots, fp32 output: the down GEMM adds g*y into the zeroed output; with two fp32 additions
-    onto zero the result is the separate combine's RN(g0*y0 + g1*y1) bit for bit."""
-    monkeypatch.setenv("COLIBRI_MOE_GEMM", gemm)
+    onto zero the result is the separate combine's RN(g0*y0 + g1*y1) bit for bit (CTA-pair,
+    single-CTA and weight-major kernels; the batches here have few enough rows per expert for the
+    weight-major kernel by default)."""
+    monkeypatch.setenv("COLIBRI_MOE_GEMM", "2sm" if gemm == "wm" else gemm)
+    if gemm == "2sm":
+        monkeypatch.setenv("COLIBRI_MOE_WM", "0")
     shape = testgen.LayerShape("fused", 900, 512, 384, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True)
     li = testgen.make_inputs(shape)
     layer, out_f, r, ref, err = _full_check(li)
@@ -416,6 +492,7 @@ def test_half_pair_tiles_equal_padded_pair_tiles(case, monkeypatch):
     epilogues, SwiGLU up values handed over through shared memory); H, Y and the output must be bit
     for bit those of the 256-row tile padded with unused rows (COLIBRI_MOE_PAIR_HALF=0).  Row counts
     chosen so that every expert ends on an odd tile, some with a single tile."""
+    monkeypatch.setenv("COLIBRI_MOE_WM", "0")     # half tiles are the CTA-pair kernel's
     act = testgen.ACT_SWIGLU if case.startswith("swiglu") else testgen.ACT_RELU_BIAS
     shape = testgen.LayerShape("half-tiles", 700, 512, 512, 8, act, "bf16", zipf_router_bias=True)
     li = testgen.make_inputs(shape)
@@ -477,6 +554,7 @@ def test_in_order_tile_handout_equals_static_order(monkeypatch):
     """The CTA-pair GEMM hands tiles out in index order at run time (a shared counter, a per-pair id
     queue); every tile is computed the same way in either order, so outputs and H agree bit for bit
     with the static round-robin order -- also when there are fewer tiles than pairs."""
+    monkeypatch.setenv("COLIBRI_MOE_WM", "0")
     for shape in (testgen.LayerShape("order", 3000, 512, 1024, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True),
                   testgen.LayerShape("order-few", 130, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")):
         li = testgen.make_inputs(shape)
