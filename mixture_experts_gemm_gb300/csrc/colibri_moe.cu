@@ -100,6 +100,8 @@ struct colibri_moe {
   bool dynamic_tiles = true; // CTA-pair GEMMs take tiles in index order from a shared counter
   bool half_tiles = true;    // CTA-pair GEMMs run an expert's odd last M tile as an M=128 pair tile
   int wm_env = -1;           // weight-major GEMMs: -1 by batch size (wm_tile_rows), 0 never, n: token tile n
+  bool wm_fused = true;      // ... both projections in one launch (needs the in-order tile hand-out)
+  int wm_ctas = 0;           // co-resident CTAs of the weight-major kernel
   int pair_ctas = 0;         // co-resident CTAs of the pair kernel (persistent grid size)
   bool decode_fused = true;  // decode batches: one cooperative kernel after the router
   bool direct_h = true;      // ... whose unsplit up projection writes H in its epilogue
@@ -374,6 +376,10 @@ static int create_impl(const colibri_moe_config_t* cfg, int device, int ep_rank,
   c->dynamic_tiles = env_dynamic_tiles();
   c->half_tiles = env_half_tiles();
   c->wm_env = env_wm();
+  {
+    const char* wf = std::getenv("COLIBRI_MOE_WM_FUSED");
+    c->wm_fused = !(wf && wf[0] == '0');
+  }
   const int64_t d = cfg->d_model, f = cfg->d_ff, E = cfg->num_experts, T = cfg->max_tokens;
   c->esize = cfg->dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
   c->out_esize = cfg->out_dtype == COLIBRI_DTYPE_F32 ? 4 : 2;
@@ -492,7 +498,8 @@ static int create_impl(const colibri_moe_config_t* cfg, int device, int ep_rank,
   }
   if (c->pair_gemm) {
     c->pair_ctas = pair_gemm_max_ctas();
-    if (c->pair_ctas < 2) c->pair_gemm = false;
+    c->wm_ctas = wm_gemm_max_ctas();
+    if (c->pair_ctas < 2 || c->wm_ctas < 2) c->pair_gemm = false;
   }
   c->fused_dispatch = env_fused_dispatch() && cfg->dtype == COLIBRI_DTYPE_BF16 && ep_size == 0;
   if (c->fused_dispatch) {
@@ -690,18 +697,27 @@ static int enqueue_router(const colibri_moe_t* ctx, const RouterArgs& ra, const 
 
 // Token tile of the weight-major GEMMs for a prefill batch of T tokens, or 0 for the CTA-pair kernel.
 // With about 256 rows or fewer per routed expert the CTA-pair kernel pads every expert to 256-row
-// tiles and half of each ring stage holds token rows; the weight-major kernel sizes its token
-// tiles to the rows (a quarter over the mean, rounded up to 32, so that most experts fit one tile)
-// and keeps more weights in flight.
-constexpr int64_t kWmMaxRows = 256;
+// tiles and half of each ring stage holds token rows; the weight-major kernel sizes its token tiles
+// to the rows (a quarter over the mean, rounded up to 32, so that most experts fit one tile) and
+// keeps more weights in flight.  With more rows it keeps 256-row token tiles and is only ahead in its
+// fused form (both projections in one launch) when the up projection is a few waves of items: then
+// the last wave, which the separate launches leave part-empty, fills with down items (skewed 16
+// experts, T=4096: 166 -> 158 us).  With many waves the CTA-pair kernel is ahead (1.3B-class T=2048:
+// 216 vs 224 us, Mixtral-shaped T=3000: 1.32 vs 1.36 ms).
+constexpr int64_t kWmMaxRowsSized = 256;  // rows per expert up to which token tiles follow the rows
+constexpr int64_t kWmMaxWaves = 8;        // up-projection waves up to which the fused form is used
 static int wm_tile_rows(const colibri_moe_t* ctx, int32_t T) {
   if (ctx->wm_env >= 0) return ctx->wm_env;
   const int64_t rows = static_cast<int64_t>(ctx->k) * T / ctx->cfg.num_experts;
-  if (rows > kWmMaxRows) return 0;
-  int64_t nt = (rows + rows / 4 + 31) / 32 * 32;
-  if (nt < 64) nt = 64;
-  if (nt > 256) nt = 256;
-  return static_cast<int>(nt);
+  if (rows <= kWmMaxRowsSized) {
+    int64_t nt = (rows + rows / 4 + 31) / 32 * 32;
+    if (nt < 64) nt = 64;
+    if (nt > 256) nt = 256;
+    return static_cast<int>(nt);
+  }
+  if (!ctx->wm_fused || !ctx->dynamic_tiles) return 0;
+  const int64_t items = (ctx->n_up / 256) * (ctx->S * static_cast<int64_t>(T) / 256 + ctx->Ex / 2);
+  return items <= kWmMaxWaves * (ctx->wm_ctas / 2) ? 256 : 0;
 }
 
 static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t T, cudaStream_t s) {
@@ -806,6 +822,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     return COLIBRI_OK;
   }
   const int wm_nt = bf16 && ctx->pair_gemm && !gather_a ? wm_tile_rows(ctx, T) : 0;
+  const bool wm_one = wm_nt > 0 && ctx->wm_fused && ctx->dynamic_tiles;  // both projections in one launch
   if (wm_nt > 0) {
     // weight-major CTA pairs: 256 weight rows x a token tile of at most wm_nt rows per item
     const int64_t tok_tiles = ctx->S * static_cast<int64_t>(T) / wm_nt + E;
@@ -821,17 +838,30 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
                 ctx->dynamic_tiles ? &ctx->sched->tile_ctr[0] : nullptr, clear_in_gemm, out_vec4,
                 fused_disp ? ctx->route_sync : nullptr, 0};
     up.wm_ntok = wm_nt;
-    const int64_t ctas_up = 2 * (ctx->n_up / 256) * tok_tiles;
-    int grid = static_cast<int>(ctas_up < ctx->pair_ctas ? ctas_up : ctx->pair_ctas);
-    if (launch_wm_gemm(swiglu ? kEpiSwiGLU : kEpiReluBias, mu, up, grid, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
-    mark(3);
     GemmArgs dn{ctx->sched, E, f, d, 0, fuse ? out : ctx->y, d, ctx->b2, d, ctx->timeout_ns,
                 &ctx->sched->status, ctx->tok_of_row, ctx->gate_of_row, nullptr,
                 ctx->dynamic_tiles ? &ctx->sched->tile_ctr[1] : nullptr, nullptr, 0, nullptr, 0};
     dn.wm_ntok = wm_nt;
-    const int64_t ctas_dn = 2 * (d / 256) * tok_tiles;
-    grid = static_cast<int>(ctas_dn < ctx->pair_ctas ? ctas_dn : ctx->pair_ctas);
-    if (launch_wm_gemm(fuse ? kEpiCombineF32 : kEpiStoreF32, md, dn, grid, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+    const int64_t ctas_up = 2 * (ctx->n_up / 256) * tok_tiles, ctas_dn = 2 * (d / 256) * tok_tiles;
+    const int epi_up = swiglu ? kEpiSwiGLU : kEpiReluBias, epi_dn = fuse ? kEpiCombineF32 : kEpiStoreF32;
+    if (wm_one) {
+      // one launch: a pair that runs out of up items goes on with down items of finished experts
+      WmFused fz;
+      fz.maps[0] = mu;
+      fz.maps[1] = md;
+      fz.args[0] = up;
+      fz.args[1] = dn;
+      const int64_t ctas = ctas_up + ctas_dn;
+      const int grid = static_cast<int>(ctas < ctx->wm_ctas ? ctas : ctx->wm_ctas);
+      if (launch_wm_fused(epi_up, epi_dn, fz, grid, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+      mark(3);
+    } else {
+      int grid = static_cast<int>(ctas_up < ctx->wm_ctas ? ctas_up : ctx->wm_ctas);
+      if (launch_wm_gemm(epi_up, mu, up, grid, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+      mark(3);
+      grid = static_cast<int>(ctas_dn < ctx->wm_ctas ? ctas_dn : ctx->wm_ctas);
+      if (launch_wm_gemm(epi_dn, md, dn, grid, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
+    }
   } else if (bf16 && ctx->pair_gemm) {
     // CTA pairs: 256-row tiles made of two 128-row tiles of one expert sharing the weight tile
     const int bn = tc_gemm_block_n();
@@ -891,7 +921,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   }
   mark(5);
   ctx->last_T = T;
-  ctx->last_kernels = (fuse ? 4 : 5) - (fused_disp ? 1 : 0);
+  ctx->last_kernels = (fuse ? 4 : 5) - (fused_disp ? 1 : 0) - (wm_one ? 1 : 0);
   return COLIBRI_OK;
 }
 

@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kEpThreads) ep_regroup_kernel(EpRegroupArgs a)
       a.sched->offsets[threadIdx.x] = a.plan.offsets[threadIdx.x];
       a.sched->mtile_start[threadIdx.x] = a.plan.mstart[threadIdx.x];
     }
-    if (threadIdx.x == 0) a.sched->tile_ctr[0] = a.sched->tile_ctr[1] = 0;
+    if (threadIdx.x == 0) reset_gemm_counters(a.sched);
   }
   const int nvec = a.row_bytes / 16;
   const int warps = gridDim.x * (kEpThreads / 32);

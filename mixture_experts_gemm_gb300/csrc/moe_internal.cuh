@@ -48,7 +48,16 @@ struct Sched {
   uint32_t tile_ctr[2];            // next tile of the up / down CTA-pair GEMM (reset by the router)
   uint32_t split_ticket[kRouterSplitMaxChunks];  // split router: CTAs done per chunk (self-resetting)
   int32_t status;                  // device status word (kStatus* bits)
+  uint32_t wm_done[kMaxE];         // fused weight-major GEMM: up items' epilogue warps done per expert
+  uint32_t wm_cleared;             // fused weight-major GEMM: warps done clearing out (both reset by the router)
 };
+
+// The GEMMs' run-time counters, cleared by the router of every forward (one thread).
+__device__ __forceinline__ void reset_gemm_counters(Sched* s) {
+  s->tile_ctr[0] = s->tile_ctr[1] = 0;
+  for (int e = 0; e < kMaxE; ++e) s->wm_done[e] = 0;
+  s->wm_cleared = 0;
+}
 
 struct RouterArgs {
   const void* x;           // [T, d] dtype
@@ -148,6 +157,12 @@ constexpr int kWmTokMaps = 8;
 struct WmMaps {
   CUtensorMap w;
   CUtensorMap tok[kWmTokMaps];
+};
+// Both projections in one launch (launch_wm_fused): the up projection's items, then the down
+// projection's; a down item of expert e starts once every up item of e has written its H rows.
+struct WmFused {
+  WmMaps maps[2];  // up, down
+  GemmArgs args[2];
 };
 
 constexpr int kZeroWarp0 = 6;   // the clearing warps follow producer, MMA and the 4 epilogue warps
@@ -356,6 +371,8 @@ cudaError_t prepare_pair_gemm();
 int pair_gemm_max_ctas();
 cudaError_t prepare_wm_gemm();
 cudaError_t launch_wm_gemm(int epi, const WmMaps& maps, const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_wm_fused(int epi_up, int epi_dn, const WmFused& f, int grid, cudaStream_t s);
+int wm_gemm_max_ctas();
 cudaError_t launch_pair_gemm(int epi, bool gather_a, const CUtensorMap& tmA, const CUtensorMap& tmA64,
                              const CUtensorMap& tmB, const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_decode_gemm(const CUtensorMap& tmW, const CUtensorMap& tmX, const DecodeArgs& a, int grid,

@@ -121,7 +121,7 @@ __device__ void scan_offsets(const RouterArgs& a, int nchunks) {
     a.sched->mtile_start[E] = mt;
     a.sched->ticket = 0;  // ready for the next forward
     a.sched->grid_sync = 0;
-    a.sched->tile_ctr[0] = a.sched->tile_ctr[1] = 0;
+    reset_gemm_counters(a.sched);
     for (int i = 0; i < a.n_tile_done; ++i) a.tile_done[i] = 0;  // (normally already 0: self-resetting)
   }
   __syncthreads();
@@ -204,7 +204,7 @@ __device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[kMaxSlots],
       a.sched->mtile_start[Ex] = mt;
       a.sched->ticket = 0;
       a.sched->grid_sync = 0;
-      a.sched->tile_ctr[0] = a.sched->tile_ctr[1] = 0;
+      reset_gemm_counters(a.sched);
       for (int i = 0; i < a.n_tile_done; ++i) a.tile_done[i] = 0;
     }
     return;
@@ -306,7 +306,7 @@ __device__ void fused_dispatch(const RouterArgs& a, int chunk, int nchunks, int 
       a.sched->mtile_start[Ex] = mt;
       a.sched->ticket = 0;
       a.sched->grid_sync = 0;
-      a.sched->tile_ctr[0] = a.sched->tile_ctr[1] = 0;
+      reset_gemm_counters(a.sched);
       for (int i = 0; i < a.n_tile_done; ++i) a.tile_done[i] = 0;
     }
   }

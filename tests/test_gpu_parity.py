@@ -464,6 +464,7 @@ def test_dispatch_in_the_router_equals_the_dispatch_kernel(case, monkeypatch):
                           "split-t1000-e16": (1000, 2048, 16, 2, False), "tma-t1100": (1100, 512, 8, 2, False),
                           "plain-t8": (8, 512, 8, 2, False)}[case]
     monkeypatch.setenv("COLIBRI_MOE_DECODE_MAX_T", "0")
+    monkeypatch.setenv("COLIBRI_MOE_WM_FUSED", "0")   # kernel counts below: one launch per projection
     shape = testgen.LayerShape("fused-dispatch", T, d, 256, E, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True,
                                top_k=k, shared_expert=shared)
     li = testgen.make_inputs(shape)
@@ -692,7 +693,7 @@ def test_decode_limit_follows_the_expert_size(mixtral):
     """Default decode limit: 128 tokens for experts of >= 2^25 weights per matrix (the Mixtral
     shape), 64 for smaller ones, where the grouped GEMMs are as fast from ~64-96 tokens on."""
     li, layer, L = mixtral
-    for T, kernels in ((100, 2), (128, 2), (129, 3)):
+    for T, kernels in ((100, 2), (128, 2), (129, 2)):   # 129: router + both weight-major GEMMs
         out, r = run(layer, x_device(li, T))
         assert layer.last_kernel_count() == kernels, T
     # a token's output does not depend on the rest of its batch: the first 129 rows of the oracle's
@@ -703,7 +704,7 @@ def test_decode_limit_follows_the_expert_size(mixtral):
     small = testgen.make_inputs(testgen.LayerShape("limit-small", 100, 512, 384, 8, testgen.ACT_SWIGLU, "bf16"))
     layer_s = make_layer(small)
     run(layer_s, x_device(small))
-    assert layer_s.last_kernel_count() == 3   # router with the dispatch fused, up GEMM, down GEMM + combine
+    assert layer_s.last_kernel_count() == 2   # router with the dispatch fused, both weight-major GEMMs + combine
 
 
 @pytest.mark.parametrize("T", testgen.DECODE_TOKENS)
@@ -914,7 +915,12 @@ def test_last_kernel_count_matches_the_path(monkeypatch):
     assert layer.last_kernel_count() == 0
     x = x_device(li)
     layer.forward(x)
-    assert layer.last_kernel_count() == 3          # router with the dispatch, up GEMM, down GEMM + combine
+    assert layer.last_kernel_count() == 2          # router with the dispatch, both weight-major GEMMs + combine
+    monkeypatch.setenv("COLIBRI_MOE_WM_FUSED", "0")
+    layer_s = make_layer(li)
+    layer_s.forward(x)
+    assert layer_s.last_kernel_count() == 3        # router with the dispatch, up GEMM, down GEMM + combine
+    monkeypatch.delenv("COLIBRI_MOE_WM_FUSED")
     layer.forward(x[:20].contiguous())
     assert layer.last_kernel_count() == 2          # decode: router + one cooperative kernel
     layer.forward(x[:0])
@@ -923,13 +929,17 @@ def test_last_kernel_count_matches_the_path(monkeypatch):
     monkeypatch.setenv("COLIBRI_MOE_DECODE_FUSED", "0")
     layer2 = make_layer(li)
     layer2.forward(x)
-    assert layer2.last_kernel_count() == 4        # router with the dispatch, up GEMM, down GEMM, combine
+    assert layer2.last_kernel_count() == 3        # router with the dispatch, both GEMMs, combine
     layer2.forward(x[:20].contiguous())
     assert layer2.last_kernel_count() == 6        # router, dispatch, 2 x (GEMM, reduction), combine
     monkeypatch.setenv("COLIBRI_MOE_DISPATCH", "separate")
     layer3 = make_layer(li)
     layer3.forward(x)
-    assert layer3.last_kernel_count() == 5        # router, dispatch, up GEMM, down GEMM, combine
+    assert layer3.last_kernel_count() == 4        # router, dispatch, both GEMMs, combine
+    monkeypatch.setenv("COLIBRI_MOE_WM", "0")
+    layer4 = make_layer(li)
+    layer4.forward(x)
+    assert layer4.last_kernel_count() == 5        # router, dispatch, up GEMM (CTA pairs), down GEMM, combine
     torch.cuda.synchronize()
 
 
