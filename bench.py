@@ -42,8 +42,9 @@ STAGES = ["router", "gather", "gemm_up", "gemm_down", "combine"]
 # stands; None where no capture of the current kernel exists.
 DOM_EVERY = 8  # the dominant kernel is timed with events on every 8th step of the timed region
 NCU_TRAFFIC = {("mixtral-prefill", 8192, "gemm_up", "2sm"): 2.618e9, ("mixtral-prefill", 8192, "gemm_down", "2sm"): 2.816e9,
-               ("mixtral-decode", 1, "gemm_up", "decode"): 0.7092e9, ("mixtral-decode", 16, "gemm_up", "decode"): 2.8339e9,
-               ("1.3b-8e", 512, "gemm_up", "2sm"): 0.3911e9, ("1.3b-8e", 512, "gemm_down", "2sm"): 0.2076e9}
+               ("mixtral-decode", 1, "gemm_up", "1kernel"): 0.7092e9, ("mixtral-decode", 16, "gemm_up", "1kernel"): 2.8339e9,
+               ("1.3b-8e", 512, "gemm_up", "2sm"): 0.3911e9, ("1.3b-8e", 512, "gemm_down", "2sm"): 0.2076e9,
+               ("1.3b-8e", 512, "gemm_up", "1kernel"): 0.5947e9, ("skewed-16e", 4096, "gemm_up", "1kernel"): 0.4574e9}
 
 
 def log(*a):
@@ -262,7 +263,7 @@ def decode_sweep(layer, shape, x, out, stream, hbm_gbs, steps):
         res[str(Td)] = {"us_per_step": ms * 1e3, "tokens_per_s": Td / (ms / 1e3), "active_experts": active,
                         "weight_bytes": wbytes, "hbm_gbs": wbytes / (ms / 1e3) / 1e9,
                         "hbm_frac": wbytes / (ms / 1e3) / 1e9 / hbm_gbs, "steps": steps,
-                        "kernels_per_step": layer.last_kernel_count()}
+                        "kernels_per_step": layer.last_kernel_count(), "gemm_form": layer.last_gemm()}
     return res
 
 
@@ -292,7 +293,8 @@ def other_workloads(peaks, steps, device: int):
         alg = algorithmic(s, s.T, int((counts > 0).sum()))
         sec = ms / 1e3
         r = {"workload": workload_desc(s, s.T), "us_per_step": ms * 1e3, "tokens_per_s": s.T / sec,
-             "tflops": alg["flops"] / sec / 1e12, "steps": steps, "kernels_per_step": layer.last_kernel_count()}
+             "tflops": alg["flops"] / sec / 1e12, "steps": steps, "kernels_per_step": layer.last_kernel_count(),
+             "gemm_form": layer.last_gemm()}
         if s.dtype == "bf16":
             r["hbm_frac_over_weights"] = alg["bytes"] / sec / 1e9 / hbm
             r["tensor_frac_of_burst"] = alg["flops"] / sec / 1e12 / burst
@@ -545,6 +547,8 @@ def main():
     torch.cuda.synchronize(dev)
     barrier()
     kernels_per_step = layer.last_kernel_count()  # (later legs run other batch sizes on this layer)
+    gemm_form = layer.last_gemm()
+    both_in_one = gemm_form in ("decode_fused", "weight_major_fused")  # one launch, both projections
     lib.colibri_moe_set_stage_events(layer._h, None, 0)
     ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     dom_ms = np.array([evs[dominant].elapsed_time(evs[dominant + 1]) for evs in dom_sets])
@@ -594,7 +598,8 @@ def main():
         (float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])) * 1e9)
     tensor_bound = alg["flops"] / alg["bytes"] > ridge
     if shape.dtype == "bf16" and tensor_bound and dominant in (2, 3):
-        fl = alg["flops_up"] if dominant == 2 else alg["flops_down"]
+        fl = alg["flops_up"] + alg["flops_down"] if both_in_one else \
+            (alg["flops_up"] if dominant == 2 else alg["flops_down"])
         ach = fl / dur / 1e12
         burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
         sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
@@ -603,8 +608,9 @@ def main():
         region_s = ms_total / 1e3
         long_region = region_s >= SUSTAINED_AFTER_S
         peak = sustained if long_region else burst
-        gemm = "1sm" if os.environ.get("COLIBRI_MOE_GEMM") == "1sm" else "2sm"
-        roof = {"bound": "tensor", "kernel": STAGES[dominant], "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+        gemm = {"single_cta": "1sm", "weight_major_fused": "1kernel"}.get(gemm_form, "2sm")
+        roof = {"bound": "tensor", "kernel": STAGES[dominant] + (" (both projections, one launch)" if both_in_one else ""),
+                "gemm_form": gemm_form, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                 "frac": ach / peak, "traffic": NCU_TRAFFIC.get((shape.name, T, STAGES[dominant], gemm)),
                 "peak_source": (f"{peak_src} bf16 {'sustained' if long_region else 'burst'}: timed region "
                                 f"{region_s:.3f} s {'>=' if long_region else '<'} {SUSTAINED_AFTER_S:.0f} s"),
@@ -621,13 +627,14 @@ def main():
         n_w = active + int(shape.shared_expert)
         byts = {2: n_w * n_up * shape.d_model * shape.d_ff * es,
                 3: n_w * shape.d_model * shape.d_ff * es}.get(dominant, alg["bytes"])
-        if kernels_per_step == 2:  # cooperative decode kernel: streams both projections' weights
+        if both_in_one:  # one kernel streams both projections' weights: the cooperative decode
+            # kernel, or the fused weight-major GEMM
             byts = n_w * (n_up + 1) * shape.d_model * shape.d_ff * es
         ach = byts / dur / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        path = "decode" if kernels_per_step == 2 else \
-            ("1sm" if os.environ.get("COLIBRI_MOE_GEMM") == "1sm" else "2sm")
-        roof = {"bound": "hbm", "kernel": STAGES[dominant], "achieved": ach, "peak": peak, "unit": "GB/s",
+        path = "1kernel" if both_in_one else {"single_cta": "1sm"}.get(gemm_form, "2sm")
+        roof = {"bound": "hbm", "kernel": STAGES[dominant] + (" (both projections, one launch)" if both_in_one else ""),
+                "gemm_form": gemm_form, "achieved": ach, "peak": peak, "unit": "GB/s",
                 "frac": ach / peak, "traffic": NCU_TRAFFIC.get((shape.name, T, STAGES[dominant], path)),
                 "peak_source": f"{peak_src} copy", "algorithmic_bytes_per_launch": byts,
                 "dominant_ms": dur * 1e3, "frac_of_nominal": ach / NOMINAL_HBM_GBS,

@@ -74,6 +74,16 @@ extern "C" {
 #define COLIBRI_GATE_SOFTMAX_SELECTED 0 /* softmax over the k selected logits (sums to 1)          */
 #define COLIBRI_GATE_SOFTMAX_ALL 1      /* softmax over all experts, at the selected ones (sum < 1) */
 
+/* Grouped-GEMM form of the most recent call (colibri_moe_last_gemm) */
+#define COLIBRI_GEMM_NONE 0                /* no forward yet, T = 0, or a call without GEMMs        */
+#define COLIBRI_GEMM_DECODE_FUSED 1        /* decode batch: the cooperative weight-streaming kernel  */
+#define COLIBRI_GEMM_DECODE_SPLIT 2        /* decode batch: separate weight-streaming kernels        */
+#define COLIBRI_GEMM_PAIR 3                /* CTA-pair GEMMs, token rows on M, one launch each       */
+#define COLIBRI_GEMM_SINGLE_CTA 4          /* single-CTA tcgen05 GEMMs                               */
+#define COLIBRI_GEMM_SIMT 5                /* fp32 SIMT GEMMs                                        */
+#define COLIBRI_GEMM_WEIGHT_MAJOR 6        /* CTA-pair GEMMs, weight rows on M, one launch each      */
+#define COLIBRI_GEMM_WEIGHT_MAJOR_FUSED 7  /* the same, both projections in one launch               */
+
 #define COLIBRI_MAX_EXPERTS 16
 #define COLIBRI_MAX_TOP_K 4
 
@@ -185,6 +195,14 @@ COLIBRI_API int colibri_moe_num_stages(const colibri_moe_t* ctx, int32_t* n_stag
  * decode kernels (COLIBRI_MOE_DECODE_FUSED=0, T <= 64); 0 before the first forward and after a
  * forward with T = 0; after an expert-parallel call, the kernels that call enqueued. */
 COLIBRI_API int colibri_moe_last_kernel_count(const colibri_moe_t* ctx, int32_t* n);
+
+/* *kind = the grouped-GEMM form (COLIBRI_GEMM_*) the most recent forward, forward_host or
+ * ep_experts call ran: which of the Compute-stage implementations (zskr.cn/news/2272131, "Colibri:
+ * a lightweight C MoE inference engine for edge devices", 2.1: one GEMM per expert over its rows)
+ * served the batch, chosen from its size and the build's switches.  A debugging and benchmarking
+ * aid; results are the same whichever form runs (bit for bit between the bf16 prefill forms).
+ * Errors: COLIBRI_ERR_INVALID_ARG for a NULL argument. */
+COLIBRI_API int colibri_moe_last_gemm(const colibri_moe_t* ctx, int32_t* kind);
 
 /* Stage timing: with n == num_stages + 1 cudaEvent_t values (passed as void*), every later forward
  * records events[i] just before stage i and events[n-1] after the last stage, on its stream; NULL

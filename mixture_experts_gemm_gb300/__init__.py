@@ -35,7 +35,7 @@ _ACTS = {"relu_bias": ACT_RELU_BIAS, "relu": ACT_RELU_BIAS, "swiglu": ACT_SWIGLU
 EXPORTED = ("colibri_moe_create", "colibri_moe_load_weights", "colibri_moe_forward", "colibri_moe_forward_host",
             "colibri_moe_get_routing", "colibri_moe_debug_buffer", "colibri_moe_num_stages",
             "colibri_moe_forward_host_async", "colibri_moe_host_sync",
-            "colibri_moe_last_kernel_count", "colibri_moe_set_stage_events", "colibri_moe_device_status",
+            "colibri_moe_last_kernel_count", "colibri_moe_last_gemm", "colibri_moe_set_stage_events", "colibri_moe_device_status",
             "colibri_moe_probe_wait_timeout", "colibri_moe_route_noalloc",
             "colibri_moe_ep_create", "colibri_moe_ep_dispatch", "colibri_moe_ep_experts", "colibri_moe_ep_combine",
             "colibri_moe_destroy", "colibri_moe_strerror")
@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
             "colibri_moe_debug_buffer": ([vp, i32, ctypes.POINTER(vp), ctypes.POINTER(i64)], ctypes.c_int),
             "colibri_moe_num_stages": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
             "colibri_moe_last_kernel_count": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
+            "colibri_moe_last_gemm": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
             "colibri_moe_set_stage_events": ([vp, vp, i32], ctypes.c_int),
             "colibri_moe_device_status": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
             "colibri_moe_probe_wait_timeout": ([vp, i32, vp], ctypes.c_int),
@@ -350,6 +351,15 @@ class MoELayer:
         n = ctypes.c_int32()
         _check(lib().colibri_moe_last_kernel_count(self._h, ctypes.byref(n)), "colibri_moe_last_kernel_count")
         return n.value
+
+    GEMM_KINDS = ("none", "decode_fused", "decode_split", "pair", "single_cta", "simt", "weight_major",
+                  "weight_major_fused")
+
+    def last_gemm(self) -> str:
+        """The grouped-GEMM form the most recent forward ran (one of GEMM_KINDS)."""
+        n = ctypes.c_int32()
+        _check(lib().colibri_moe_last_gemm(self._h, ctypes.byref(n)), "colibri_moe_last_gemm")
+        return self.GEMM_KINDS[n.value]
 
     def set_stage_events(self, events):
         """events: list of num_stages()+1 torch.cuda.Event (or None to turn timing off)."""

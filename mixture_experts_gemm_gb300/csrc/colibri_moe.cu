@@ -116,6 +116,7 @@ struct colibri_moe {
   Sched* ep_sched = nullptr; // schedule of the local experts' GEMMs (ep_experts)
   int32_t last_T = -1;
   int32_t last_kernels = 0;  // kernels enqueued by the last forward
+  int32_t last_gemm = COLIBRI_GEMM_NONE;  // its grouped-GEMM form
   std::vector<cudaEvent_t> events;
   uint64_t timeout_ns = 2000000000ull;
 };
@@ -792,6 +793,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     mark(5);
     ctx->last_T = T;
     ctx->last_kernels = 2;
+    ctx->last_gemm = COLIBRI_GEMM_DECODE_FUSED;
     return COLIBRI_OK;
   }
   if (!fused_disp && launch_gather(c.dtype, ga, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
@@ -819,6 +821,7 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
     mark(5);
     ctx->last_T = T;
     ctx->last_kernels = 6;
+    ctx->last_gemm = COLIBRI_GEMM_DECODE_SPLIT;
     return COLIBRI_OK;
   }
   const int wm_nt = bf16 && ctx->pair_gemm && !gather_a ? wm_tile_rows(ctx, T) : 0;
@@ -922,6 +925,10 @@ static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t
   mark(5);
   ctx->last_T = T;
   ctx->last_kernels = (fuse ? 4 : 5) - (fused_disp ? 1 : 0) - (wm_one ? 1 : 0);
+  ctx->last_gemm = wm_one ? COLIBRI_GEMM_WEIGHT_MAJOR_FUSED
+                   : wm_nt > 0 ? COLIBRI_GEMM_WEIGHT_MAJOR
+                   : !bf16 ? COLIBRI_GEMM_SIMT
+                   : ctx->pair_gemm ? COLIBRI_GEMM_PAIR : COLIBRI_GEMM_SINGLE_CTA;
   return COLIBRI_OK;
 }
 
@@ -932,6 +939,7 @@ int colibri_moe_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t T,
   if (!ctx->loaded) return COLIBRI_ERR_STATE;
   if (T == 0) {
     ctx->last_kernels = 0;
+    ctx->last_gemm = COLIBRI_GEMM_NONE;
     return COLIBRI_OK;
   }
   if (!x || !out) return COLIBRI_ERR_INVALID_ARG;
@@ -952,6 +960,7 @@ int colibri_moe_forward_host(colibri_moe_t* ctx, const void* x_host, void* out_h
   if (!ctx->loaded) return COLIBRI_ERR_STATE;
   if (T == 0) {
     ctx->last_kernels = 0;
+    ctx->last_gemm = COLIBRI_GEMM_NONE;
     return COLIBRI_OK;
   }
   if (!x_host || !out_host) return COLIBRI_ERR_INVALID_ARG;
@@ -988,6 +997,7 @@ int colibri_moe_forward_host_async(colibri_moe_t* ctx, const void* x_host, void*
   if (!ctx->loaded) return COLIBRI_ERR_STATE;
   if (T == 0) {
     ctx->last_kernels = 0;
+    ctx->last_gemm = COLIBRI_GEMM_NONE;
     return COLIBRI_OK;
   }
   if (!x_host || !out_host) return COLIBRI_ERR_INVALID_ARG;
@@ -1050,6 +1060,7 @@ int colibri_moe_ep_dispatch(colibri_moe_t* ctx, const void* x, int32_t T, void* 
     }
     ctx->last_T = 0;
     ctx->last_kernels = 0;
+    ctx->last_gemm = COLIBRI_GEMM_NONE;
     return COLIBRI_OK;
   }
   if (!x || !send_rows) return COLIBRI_ERR_INVALID_ARG;
@@ -1115,6 +1126,7 @@ int colibri_moe_ep_experts(colibri_moe_t* ctx, const void* recv_rows, const int3
   if (!g.ok) return COLIBRI_ERR_CUDA;
   if (R == 0) {
     ctx->last_kernels = 0;
+    ctx->last_gemm = COLIBRI_GEMM_NONE;
     return COLIBRI_OK;
   }
   if (!recv_rows || !y_rows) return COLIBRI_ERR_INVALID_ARG;
@@ -1183,6 +1195,7 @@ int colibri_moe_ep_experts(colibri_moe_t* ctx, const void* recv_rows, const int3
     if (launch_ep_unregroup(ug, ctx->num_sms, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   }
   ctx->last_kernels = direct_y ? 3 : 4;
+  ctx->last_gemm = !bf16 ? COLIBRI_GEMM_SIMT : ctx->pair_gemm ? COLIBRI_GEMM_PAIR : COLIBRI_GEMM_SINGLE_CTA;
   return COLIBRI_OK;
 }
 
@@ -1193,6 +1206,7 @@ int colibri_moe_ep_combine(colibri_moe_t* ctx, const float* y_back, void* out, v
   const int T = ctx->last_T, d = ctx->cfg.d_model;
   if (T == 0) {
     ctx->last_kernels = 0;
+    ctx->last_gemm = COLIBRI_GEMM_NONE;
     return COLIBRI_OK;
   }
   if (!y_back || !out) return COLIBRI_ERR_INVALID_ARG;
@@ -1270,6 +1284,12 @@ int colibri_moe_num_stages(const colibri_moe_t* ctx, int32_t* n_stages) {
 int colibri_moe_last_kernel_count(const colibri_moe_t* ctx, int32_t* n) {
   if (!ctx || !n) return COLIBRI_ERR_INVALID_ARG;
   *n = ctx->last_kernels;
+  return COLIBRI_OK;
+}
+
+int colibri_moe_last_gemm(const colibri_moe_t* ctx, int32_t* kind) {
+  if (!ctx || !kind) return COLIBRI_ERR_INVALID_ARG;
+  *kind = ctx->last_gemm;
   return COLIBRI_OK;
 }
 

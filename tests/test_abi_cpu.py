@@ -75,6 +75,7 @@ def test_null_arguments(cuda_lib):
     n = ctypes.c_int32()
     assert L.colibri_moe_num_stages(None, ctypes.byref(n)) == -1
     assert L.colibri_moe_last_kernel_count(None, ctypes.byref(n)) == -1
+    assert L.colibri_moe_last_gemm(None, ctypes.byref(n)) == -1
     assert L.colibri_moe_probe_wait_timeout(None, 1000, None) == -1
     assert L.colibri_moe_ep_dispatch(None, None, 4, None, None, None) == -1
     assert L.colibri_moe_ep_experts(None, None, None, None, None) == -1

@@ -271,6 +271,7 @@ def test_pair_gemm_kernel(case, monkeypatch):
         li, h, y = _integer_inputs(shape, 300, lo=-1, hi=2, wlo=-1, whi=2, seed=3)
         layer = make_layer(li)
         out, r = run(layer, x_device(li))
+        assert layer.last_gemm() == "pair"
         assert np.array_equal(out, y.astype(np.float64))
         assert layer.device_status() == 0
     elif case == "swiglu-odd-tiles":
@@ -335,9 +336,12 @@ def test_weight_major_gemm_kernel(case, monkeypatch):
         assert np.all(np.abs(out - ref["out"]) <= TOL_BF16 * rms + np.abs(ref["out"]) * 2.0 ** -8)
     else:
         layer, out, r, _, _ = _full_check(li)
+    # the fused form takes its items from the in-order counter: with the static order, one launch each
+    assert layer.last_gemm() == ("weight_major" if case == "static-order" else "weight_major_fused")
     monkeypatch.setenv("COLIBRI_MOE_WM", "0")
     layer_p = make_layer(li, out_dtype=out_dtype)
     out_p, r_p = run(layer_p, x_device(li))
+    assert layer_p.last_gemm() == "pair"
     assert np.array_equal(r["row_of"], r_p["row_of"])
     rows = np.sort(r["row_of"].ravel())
     if shape.shared_expert:
@@ -353,6 +357,26 @@ def test_weight_major_gemm_kernel(case, monkeypatch):
     assert layer.device_status() == 0 and layer_p.device_status() == 0
 
 
+def test_gemm_form_follows_the_batch():
+    """The grouped-GEMM form by batch: the weight-major fused launch up to 256 rows per expert and
+    for layers of few waves (the skewed 16-expert shape at 4096 tokens: 512 rows per expert, 11
+    weight tiles per expert), the CTA-pair kernel for many-wave layers (1.3B-class at 2048 tokens),
+    the cooperative decode kernel for decode batches, SIMT for fp32; outputs checked on every row."""
+    cases = [
+        (testgen.LayerShape("form-small", 600, 512, 384, 8, testgen.ACT_SWIGLU, "bf16"), "weight_major_fused"),
+        (testgen.LayerShape("form-skewed", 4096, 2048, 1408, 16, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True),
+         "weight_major_fused"),
+        (testgen.LayerShape("form-1p3b-2k", 2048, 2048, 5632, 8, testgen.ACT_SWIGLU, "bf16"), "pair"),
+        (testgen.LayerShape("form-decode", 16, 512, 384, 8, testgen.ACT_SWIGLU, "bf16"), "decode_fused"),
+        (testgen.LayerShape("form-f32", 300, 256, 512, 4, testgen.ACT_RELU_BIAS, "f32"), "simt"),
+    ]
+    for shape, form in cases:
+        li = testgen.make_inputs(shape)
+        layer, _, _, _, _ = _full_check(li)
+        assert layer.last_gemm() == form, (shape.name, layer.last_gemm())
+        layer.close()
+
+
 @pytest.mark.parametrize("case", ["int-relu", "swiglu", "skewed"])
 def test_single_cta_gemm_kernel(case, monkeypatch):
     """The single-CTA grouped GEMM (COLIBRI_MOE_GEMM=1sm) on the same cases as the pair kernel."""
@@ -362,6 +386,7 @@ def test_single_cta_gemm_kernel(case, monkeypatch):
         li, h, y = _integer_inputs(shape, 300, lo=-1, hi=2, wlo=-1, whi=2, seed=4)
         layer = make_layer(li)
         out, r = run(layer, x_device(li))
+        assert layer.last_gemm() == "single_cta"
         assert np.array_equal(out, y.astype(np.float64))
         assert layer.device_status() == 0
     elif case == "swiglu":
@@ -916,15 +941,19 @@ def test_last_kernel_count_matches_the_path(monkeypatch):
     x = x_device(li)
     layer.forward(x)
     assert layer.last_kernel_count() == 2          # router with the dispatch, both weight-major GEMMs + combine
+    assert layer.last_gemm() == "weight_major_fused"
     monkeypatch.setenv("COLIBRI_MOE_WM_FUSED", "0")
     layer_s = make_layer(li)
     layer_s.forward(x)
     assert layer_s.last_kernel_count() == 3        # router with the dispatch, up GEMM, down GEMM + combine
+    assert layer_s.last_gemm() == "weight_major"
     monkeypatch.delenv("COLIBRI_MOE_WM_FUSED")
     layer.forward(x[:20].contiguous())
     assert layer.last_kernel_count() == 2          # decode: router + one cooperative kernel
+    assert layer.last_gemm() == "decode_fused"
     layer.forward(x[:0])
     assert layer.last_kernel_count() == 0
+    assert layer.last_gemm() == "none"
     monkeypatch.setenv("COLIBRI_MOE_FUSED_COMBINE", "0")
     monkeypatch.setenv("COLIBRI_MOE_DECODE_FUSED", "0")
     layer2 = make_layer(li)
@@ -932,6 +961,7 @@ def test_last_kernel_count_matches_the_path(monkeypatch):
     assert layer2.last_kernel_count() == 3        # router with the dispatch, both GEMMs, combine
     layer2.forward(x[:20].contiguous())
     assert layer2.last_kernel_count() == 6        # router, dispatch, 2 x (GEMM, reduction), combine
+    assert layer2.last_gemm() == "decode_split"
     monkeypatch.setenv("COLIBRI_MOE_DISPATCH", "separate")
     layer3 = make_layer(li)
     layer3.forward(x)
@@ -940,6 +970,7 @@ def test_last_kernel_count_matches_the_path(monkeypatch):
     layer4 = make_layer(li)
     layer4.forward(x)
     assert layer4.last_kernel_count() == 5        # router, dispatch, up GEMM (CTA pairs), down GEMM, combine
+    assert layer4.last_gemm() == "pair"
     torch.cuda.synchronize()
 
 
