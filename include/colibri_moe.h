@@ -190,8 +190,10 @@ COLIBRI_API int colibri_moe_num_stages(const colibri_moe_t* ctx, int32_t* n_stag
  * GEMM path (bf16 prefill or fp32) with the combine fused into the down GEMM (two slots, fp32
  * output), 5 with a separate combine, one fewer for bf16 prefill batches of 9..1024 tokens (the
  * router writes the dispatch itself), 2 on the
- * decode path (by default T <= 128 for experts of at least 2^25 weights per matrix, else T <= 64:
- * the router and one cooperative kernel), 6 on the separate
+ * decode path (by default T <= 32 for experts of at least 2^25 weights per matrix, else T <= 16;
+ * 128 / 64 when the build runs single-CTA GEMMs: the router and one cooperative kernel), one fewer
+ * than the grouped-GEMM counts where the weight-major GEMM runs both projections in one launch
+ * (colibri_moe_last_gemm tells which), 6 on the separate
  * decode kernels (COLIBRI_MOE_DECODE_FUSED=0, T <= 64); 0 before the first forward and after a
  * forward with T = 0; after an expert-parallel call, the kernels that call enqueued. */
 COLIBRI_API int colibri_moe_last_kernel_count(const colibri_moe_t* ctx, int32_t* n);

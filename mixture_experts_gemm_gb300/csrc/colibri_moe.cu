@@ -280,13 +280,20 @@ bool env_decode_fused() {
 // per matrix (d_model x d_ff; at the Mixtral shape the cooperative kernel wins up to 128 tokens),
 // else 64 (with smaller experts the grouped GEMMs catch up between 64 and 96 tokens).
 // COLIBRI_MOE_DECODE_MAX_T overrides (0 .. kDecodeMaxT; 0 turns the decode path off).
-int env_decode_max_t(int64_t d, int64_t f) {
+// Decode-path limit: batches of up to this many tokens run the cooperative weight-streaming kernel.
+// With the weight-major GEMM available its fused form is as fast from ~32 tokens on for experts of at
+// least 2^25 weights per matrix and from ~16 for smaller ones (Mixtral shape: 427 vs 427 us at 32
+// tokens, 430 vs 440 at 64, 434 vs 470 at 128; 1.3B class: 112 vs 116 at 48; skewed 16 experts:
+// 55 vs 58 at 32); without it (single-CTA GEMMs) the cooperative kernel serves up to 128 / 64.
+int env_decode_max_t(int64_t d, int64_t f, bool weight_major) {
   const char* s = std::getenv("COLIBRI_MOE_DECODE_MAX_T");
   if (s) {
     long v = std::strtol(s, nullptr, 10);
     if (v >= 0 && v <= kDecodeMaxT) return static_cast<int>(v);
   }
-  return d * f >= (int64_t{1} << 25) ? kDecodeMaxT : kDecodeSepMaxT;
+  const bool large = d * f >= (int64_t{1} << 25);
+  if (weight_major) return large ? 32 : 16;
+  return large ? kDecodeMaxT : kDecodeSepMaxT;
 }
 
 uint64_t env_timeout_ns() {
@@ -428,7 +435,9 @@ static int create_impl(const colibri_moe_config_t* cfg, int device, int ep_rank,
   const size_t o_ep_sched = ep_size > 0 ? carve(sizeof(Sched)) : 0;
   // decode partial sums: bf16 layers whose batches can be decode-sized (an expert rank always runs
   // the grouped GEMMs: its rows come from every source)
-  c->decode_max_t = (cfg->dtype == COLIBRI_DTYPE_BF16 && ep_size == 0) ? env_decode_max_t(d, f) : 0;
+  c->decode_max_t = (cfg->dtype == COLIBRI_DTYPE_BF16 && ep_size == 0)
+                        ? env_decode_max_t(d, f, c->pair_gemm && c->wm_env != 0)
+                        : 0;
   if (c->decode_max_t > T) c->decode_max_t = static_cast<int>(T);
   const int64_t npad_max = (c->decode_max_t + 15) / 16 * 16;
   const int64_t part_floats = c->decode_max_t > 0

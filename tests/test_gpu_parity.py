@@ -137,8 +137,10 @@ def test_small_bf16_relu_bias_with_router_bias():
 
 @pytest.mark.parametrize("T", [1, 5, 16, 33, 64])
 def test_decode_path_matches_oracle_and_prefill_path(T, monkeypatch):
-    """Batches of <= 64 tokens take the weight-streaming decode kernels; the same inputs through the
-    prefill kernels (decode threshold 0) must agree, and both must match the oracle."""
+    """Batches of up to 64 tokens (COLIBRI_MOE_DECODE_MAX_T=64) take the weight-streaming decode kernels;
+    the same inputs through the prefill kernels (decode threshold 0) must agree, and both must match
+    the oracle."""
+    monkeypatch.setenv("COLIBRI_MOE_DECODE_MAX_T", "64")
     shape = testgen.LayerShape("decode-small", T, 512, 384, 8, testgen.ACT_SWIGLU, "bf16", zipf_router_bias=True)
     li = testgen.make_inputs(shape)
     _, out_d, r_d, ref, _ = _full_check(li)
@@ -155,6 +157,7 @@ def test_cooperative_decode_kernel_equals_separate_kernels(case, monkeypatch):
     and combine; x itself as the up GEMM's token operand).  It sums the same partials in the same order
     as the separate kernels, so outputs and routing bookkeeping agree bit for bit.  Batches of <= 4
     tokens combine per output tile in the CTA finishing the tile; larger ones after a grid barrier."""
+    monkeypatch.setenv("COLIBRI_MOE_DECODE_MAX_T", "64")   # the decode path up to 64 tokens
     if case == "relu":
         shape = testgen.LayerShape("coop-relu", 20, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")
     elif case.startswith("k4-shared"):
@@ -193,6 +196,7 @@ def test_cooperative_decode_kernel_writes_h_in_the_up_epilogue(case, monkeypatch
     and their up rows in one 128-row tile, the up values handed over through shared memory) and the
     activation phase and one grid barrier drop out.  H and the output equal the activation-phase
     form bit for bit, and the separate kernels'.  The shapes give one full wave of unsplit items."""
+    monkeypatch.setenv("COLIBRI_MOE_DECODE_MAX_T", "64")
     E, k, shared = 4, 2, False
     if case.startswith("relu"):
         act, f = testgen.ACT_RELU_BIAS, 4864
@@ -254,7 +258,8 @@ def test_cooperative_decode_kernel_up_to_128_tokens(case, monkeypatch):
     assert np.array_equal(out_c, out_c2)
 
 
-def test_decode_path_relu_bias():
+def test_decode_path_relu_bias(monkeypatch):
+    monkeypatch.setenv("COLIBRI_MOE_DECODE_MAX_T", "64")
     shape = testgen.LayerShape("decode-relu", 20, 256, 512, 4, testgen.ACT_RELU_BIAS, "bf16")
     li = testgen.make_inputs(shape)
     _full_check(li)
@@ -597,7 +602,7 @@ def test_in_order_tile_handout_equals_static_order(monkeypatch):
         assert np.array_equal(out_d, out_d2), shape.name
 
 
-@pytest.mark.parametrize("T", [24, 900])
+@pytest.mark.parametrize("T", [12, 900])
 def test_forward_replays_from_a_cuda_graph(T):
     """forward allocates nothing and never synchronises, so it can be captured into a CUDA graph; the
     replay must reproduce the eager output bit for bit (prefill and decode paths)."""
@@ -715,12 +720,13 @@ def test_large_batch_many_router_chunks(dtype, T, k, shared):
 
 
 def test_decode_limit_follows_the_expert_size(mixtral):
-    """Default decode limit: 128 tokens for experts of >= 2^25 weights per matrix (the Mixtral
-    shape), 64 for smaller ones, where the grouped GEMMs are as fast from ~64-96 tokens on."""
+    """Default decode limit: 32 tokens for experts of >= 2^25 weights per matrix (the Mixtral
+    shape), 16 for smaller ones; above it the fused weight-major GEMM (as fast from there on)."""
     li, layer, L = mixtral
-    for T, kernels in ((100, 2), (128, 2), (129, 2)):   # 129: router + both weight-major GEMMs
+    for T, form in ((32, "decode_fused"), (33, "weight_major_fused"), (129, "weight_major_fused")):
         out, r = run(layer, x_device(li, T))
-        assert layer.last_kernel_count() == kernels, T
+        assert layer.last_kernel_count() == 2, T
+        assert layer.last_gemm() == form, T
     # a token's output does not depend on the rest of its batch: the first 129 rows of the oracle's
     # full forward are the oracle's forward of the first 129 tokens
     ref = mixtral.oracle_forward()
@@ -730,6 +736,11 @@ def test_decode_limit_follows_the_expert_size(mixtral):
     layer_s = make_layer(small)
     run(layer_s, x_device(small))
     assert layer_s.last_kernel_count() == 2   # router with the dispatch fused, both weight-major GEMMs + combine
+    assert layer_s.last_gemm() == "weight_major_fused"
+    run(layer_s, x_device(small, 16))
+    assert layer_s.last_gemm() == "decode_fused"
+    run(layer_s, x_device(small, 17))
+    assert layer_s.last_gemm() == "weight_major_fused"
 
 
 @pytest.mark.parametrize("T", testgen.DECODE_TOKENS)
@@ -948,7 +959,7 @@ def test_last_kernel_count_matches_the_path(monkeypatch):
     assert layer_s.last_kernel_count() == 3        # router with the dispatch, up GEMM, down GEMM + combine
     assert layer_s.last_gemm() == "weight_major"
     monkeypatch.delenv("COLIBRI_MOE_WM_FUSED")
-    layer.forward(x[:20].contiguous())
+    layer.forward(x[:12].contiguous())
     assert layer.last_kernel_count() == 2          # decode: router + one cooperative kernel
     assert layer.last_gemm() == "decode_fused"
     layer.forward(x[:0])
@@ -959,7 +970,7 @@ def test_last_kernel_count_matches_the_path(monkeypatch):
     layer2 = make_layer(li)
     layer2.forward(x)
     assert layer2.last_kernel_count() == 3        # router with the dispatch, both GEMMs, combine
-    layer2.forward(x[:20].contiguous())
+    layer2.forward(x[:12].contiguous())
     assert layer2.last_kernel_count() == 6        # router, dispatch, 2 x (GEMM, reduction), combine
     assert layer2.last_gemm() == "decode_split"
     monkeypatch.setenv("COLIBRI_MOE_DISPATCH", "separate")
@@ -980,7 +991,7 @@ def test_two_contexts_on_two_streams_concurrently():
     synchronisation in between, and each output equals its own sequential run bit for bit."""
     la = testgen.make_inputs(testgen.LayerShape("conc-a", 900, 512, 384, 8, testgen.ACT_SWIGLU, "bf16",
                                                 zipf_router_bias=True))
-    lb = testgen.make_inputs(testgen.LayerShape("conc-b", 24, 512, 768, 16, testgen.ACT_SWIGLU, "bf16",
+    lb = testgen.make_inputs(testgen.LayerShape("conc-b", 12, 512, 768, 16, testgen.ACT_SWIGLU, "bf16",
                                                 top_k=4, shared_expert=True))
     layer_a, layer_b = make_layer(la), make_layer(lb)
     xa, xb = x_device(la), x_device(lb)
