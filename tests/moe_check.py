@@ -136,3 +136,37 @@ def sample_tokens(idx: np.ndarray, E: int, n_random: int, seed: int = 0):
         if 0 < counts[e] <= 8:
             pick.update(int(t) for t in toks)
     return np.array(sorted(pick), dtype=np.int32)
+
+
+def bf16_h_bound(li: testgen.LayerInputs, idx: np.ndarray, gate: np.ndarray) -> np.ndarray:
+    """Per output element, what the bf16 path's one intermediate rounding can add to its error: H, the
+    activation between the two projections, is stored in bf16, each element within one bf16 ulp
+    (2^-8 relative, one half-ulp rounding plus fp32 accumulation ahead of it) of its exact value, so
+    out[t, i] moves by at most 2^-8 * sum over t's slots of g * sum_j |W2[i, j] * H[t, j]|.  Exact H
+    in fp64; routing (idx, gate: the routed slots) given; the shared expert adds with weight 1.  This
+    matters beside the max|err| / RMS budget only for output outliers (top-1, unnormalised gates,
+    short K), where that rounding alone can exceed 2e-2 x RMS."""
+    s = li.shape
+    x = li.x_f32.astype(np.float64)
+    acc = np.zeros(x.shape)
+    swiglu = s.act == testgen.ACT_SWIGLU
+
+    def abs_terms(xr, w1, w3, w2, b1):
+        if swiglu:
+            g = xr @ w1.astype(np.float64).T
+            u = xr @ w3.astype(np.float64).T
+            h = g / (1.0 + np.exp(-g)) * u
+        else:
+            h = np.maximum(xr @ w1.astype(np.float64).T + b1, 0.0)
+        return np.abs(h) @ np.abs(w2.astype(np.float64)).T
+
+    for e in range(s.num_experts):
+        toks, slots = np.nonzero(idx == e)
+        if len(toks) == 0:
+            continue
+        a = abs_terms(x[toks], li.w1_f32[e], li.w3_f32[e] if swiglu else None, li.w2_f32[e],
+                      None if swiglu else li.b1[e])
+        np.add.at(acc, toks, gate[toks, slots][:, None] * a)
+    if s.shared_expert:
+        acc += abs_terms(x, li.ws1_f32, li.ws3_f32 if swiglu else None, li.ws2_f32, None if swiglu else li.bs1)
+    return acc * 2.0 ** -8
