@@ -716,9 +716,9 @@ static int enqueue_router(const colibri_moe_t* ctx, const RouterArgs& ra, const 
 // 216 vs 224 us, Mixtral-shaped T=3000: 1.32 vs 1.36 ms).
 constexpr int64_t kWmMaxRowsSized = 256;  // rows per expert up to which token tiles follow the rows
 constexpr int64_t kWmMaxWaves = 8;        // up-projection waves up to which the fused form is used
-static int wm_tile_rows(const colibri_moe_t* ctx, int32_t T) {
+// rows: mean rows per routed expert; total_rows: rows over all scheduled experts (n_sched of them)
+static int wm_tile_rows_for(const colibri_moe_t* ctx, int64_t rows, int64_t total_rows, int64_t n_sched) {
   if (ctx->wm_env >= 0) return ctx->wm_env;
-  const int64_t rows = static_cast<int64_t>(ctx->k) * T / ctx->cfg.num_experts;
   if (rows <= kWmMaxRowsSized) {
     int64_t nt = (rows + rows / 4 + 31) / 32 * 32;
     if (nt < 64) nt = 64;
@@ -726,8 +726,12 @@ static int wm_tile_rows(const colibri_moe_t* ctx, int32_t T) {
     return static_cast<int>(nt);
   }
   if (!ctx->wm_fused || !ctx->dynamic_tiles) return 0;
-  const int64_t items = (ctx->n_up / 256) * (ctx->S * static_cast<int64_t>(T) / 256 + ctx->Ex / 2);
+  const int64_t items = (ctx->n_up / 256) * (total_rows / 256 + n_sched / 2);
   return items <= kWmMaxWaves * (ctx->wm_ctas / 2) ? 256 : 0;
+}
+static int wm_tile_rows(const colibri_moe_t* ctx, int32_t T) {
+  return wm_tile_rows_for(ctx, static_cast<int64_t>(ctx->k) * T / ctx->cfg.num_experts,
+                          ctx->S * static_cast<int64_t>(T), ctx->Ex);
 }
 
 static int enqueue_forward(colibri_moe_t* ctx, const void* x, void* out, int32_t T, cudaStream_t s) {
@@ -1158,7 +1162,45 @@ int colibri_moe_ep_experts(colibri_moe_t* ctx, const void* recv_rows, const int3
   if (max_mtiles > ctx->rows_alloc / kRowTile) max_mtiles = ctx->rows_alloc / kRowTile;
   Sched* const sc = ctx->ep_sched;
   int32_t* const status = &ctx->sched->status;
-  if (bf16 && ctx->pair_gemm) {
+  // the weight-major GEMMs for few rows per local expert (the received counts are known here)
+  const int wm_nt = bf16 && ctx->pair_gemm ? wm_tile_rows_for(ctx, R / El, R, El) : 0;
+  const bool wm_one = wm_nt > 0 && ctx->wm_fused && ctx->dynamic_tiles;
+  if (wm_nt > 0) {
+    const int64_t tok_tiles = R / wm_nt + El;
+    WmMaps mu, md;
+    mu.w = swiglu ? ctx->tm_w13_half : ctx->tm_w13_dec;
+    md.w = ctx->tm_w2_dec;
+    for (int i = 0; i < kWmTokMaps; ++i) {
+      mu.tok[i] = ctx->tm_xp_dec[i];
+      md.tok[i] = ctx->tm_h_dec[i];
+    }
+    GemmArgs up{sc, El, d, ctx->n_up, 0, ctx->h, f, ctx->b1, f, ctx->timeout_ns, status, nullptr, nullptr, nullptr,
+                ctx->dynamic_tiles ? &sc->tile_ctr[0] : nullptr, nullptr, 0, nullptr, 0};
+    up.wm_ntok = wm_nt;
+    // the down projection writes each row at its receive index (tok_of_row, filled by the regroup)
+    GemmArgs dn{sc, El, f, d, 0, y_rows, d, ctx->b2, d, ctx->timeout_ns, status, nullptr, nullptr, nullptr,
+                ctx->dynamic_tiles ? &sc->tile_ctr[1] : nullptr, nullptr, 0, nullptr, 0, ctx->tok_of_row};
+    dn.wm_ntok = wm_nt;
+    const int64_t ctas_up = 2 * (ctx->n_up / 256) * tok_tiles, ctas_dn = 2 * (d / 256) * tok_tiles;
+    const int epi_up = swiglu ? kEpiSwiGLU : kEpiReluBias;
+    if (wm_one) {
+      WmFused fz;
+      fz.maps[0] = mu;
+      fz.maps[1] = md;
+      fz.args[0] = up;
+      fz.args[1] = dn;
+      const int64_t ctas = ctas_up + ctas_dn;
+      if (launch_wm_fused(epi_up, kEpiStoreF32, fz, static_cast<int>(ctas < ctx->wm_ctas ? ctas : ctx->wm_ctas), s) !=
+          cudaSuccess)
+        return COLIBRI_ERR_CUDA;
+    } else {
+      if (launch_wm_gemm(epi_up, mu, up, static_cast<int>(ctas_up < ctx->wm_ctas ? ctas_up : ctx->wm_ctas), s) !=
+              cudaSuccess ||
+          launch_wm_gemm(kEpiStoreF32, md, dn, static_cast<int>(ctas_dn < ctx->wm_ctas ? ctas_dn : ctx->wm_ctas), s) !=
+              cudaSuccess)
+        return COLIBRI_ERR_CUDA;
+    }
+  } else if (bf16 && ctx->pair_gemm) {
     const int bn = tc_gemm_block_n();
     const int64_t max_pairs = (max_mtiles + El + 1) / 2;
     GemmArgs up{sc, El, d, ctx->n_up, ctx->n_up / bn, ctx->h, f, ctx->b1, f, ctx->timeout_ns, status, nullptr, nullptr,
@@ -1203,8 +1245,11 @@ int colibri_moe_ep_experts(colibri_moe_t* ctx, const void* recv_rows, const int3
     EpUnregroupArgs ug{ctx->y, static_cast<float*>(y_rows), static_cast<int>(R), d, plan};
     if (launch_ep_unregroup(ug, ctx->num_sms, s) != cudaSuccess) return COLIBRI_ERR_CUDA;
   }
-  ctx->last_kernels = direct_y ? 3 : 4;
-  ctx->last_gemm = !bf16 ? COLIBRI_GEMM_SIMT : ctx->pair_gemm ? COLIBRI_GEMM_PAIR : COLIBRI_GEMM_SINGLE_CTA;
+  ctx->last_kernels = (direct_y ? 3 : 4) - (wm_one ? 1 : 0);
+  ctx->last_gemm = wm_one ? COLIBRI_GEMM_WEIGHT_MAJOR_FUSED
+                   : wm_nt > 0 ? COLIBRI_GEMM_WEIGHT_MAJOR
+                   : !bf16 ? COLIBRI_GEMM_SIMT
+                   : ctx->pair_gemm ? COLIBRI_GEMM_PAIR : COLIBRI_GEMM_SINGLE_CTA;
   return COLIBRI_OK;
 }
 

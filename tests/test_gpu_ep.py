@@ -90,9 +90,11 @@ def test_expert_parallel_step_equals_forward_and_oracle(case):
         got = out.cpu().numpy().astype(np.float64)
         ref_fwd = full.forward(x)
         torch.cuda.synchronize()
-        grouped = full.last_kernel_count() != 2   # the decode path sums in another order
+        grouped = full.last_gemm() not in ("decode_fused", "decode_split")   # the decode path sums in another order
         if grouped:
             assert np.array_equal(got, ref_fwd.cpu().numpy().astype(np.float64)), (case, r)
+            if shape.dtype == "bf16":   # the ranks' GEMMs: weight-major or CTA pairs, the same result
+                assert layers[r].last_gemm() in ("weight_major_fused", "weight_major", "pair"), layers[r].last_gemm()
         a = int(starts[r])
         ref = L.forward(li.x_f32[a:a + T])
         assert rel_err(got, ref["out"]) <= tol, (case, r)
