@@ -209,14 +209,18 @@ __device__ void finish_chunk(const RouterArgs& a, const int (*s_idx)[kMaxSlots],
     }
     return;
   }
-  __threadfence();
+  // The ticket: an acquire-release add by thread 0 after the block barrier.  Its release covers the
+  // whole CTA's rank and count stores (ordered before it by the barrier; release is cumulative) and,
+  // in the CTA that takes the last ticket, its acquire orders every other CTA's counts before the
+  // scan's loads (the barrier after it carries that to the other threads).
   __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(&a.sched->ticket, 1u) == static_cast<unsigned>(nchunks) - 1u);
-  __syncthreads();
-  if (s_last) {
-    __threadfence();
-    scan_offsets(a, nchunks);
+  if (threadIdx.x == 0) {
+    unsigned before;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(before) : "l"(&a.sched->ticket) : "memory");
+    s_last = before == static_cast<unsigned>(nchunks) - 1u;
   }
+  __syncthreads();
+  if (s_last) scan_offsets(a, nchunks);
 }
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
