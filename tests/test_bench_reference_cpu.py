@@ -49,3 +49,26 @@ def test_reference_arm_other_ranks_exit_without_work(oracle_built):
              "--workload", "tiny-moe-4e2r", "--gpus", "2")
     assert r.returncode == 0, r.stderr[-2000:]
     assert not [l for l in r.stdout.splitlines() if l.startswith("{")]
+
+
+def test_roofline_counts_follow_the_layer_shape():
+    """The roofline's algorithmic FLOPs and bytes, written out by hand from the layer's shape: the up
+    projection's two (SwiGLU) or one matrices over every routed row, the down projection's one, the
+    router's logits; bytes = the active experts' three (or two) matrices + x in + fp32 out + W_r."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import testgen
+    s = testgen.CONFIGS["mixtral-prefill"]          # T=8192, d=4096, f=14336, E=8, top-2, SwiGLU, bf16
+    a = bench.algorithmic(s, s.T)
+    rows = 2 * 8192
+    assert a["flops_up"] == 2.0 * rows * 4096 * 14336 * 2 == 3848290697216.0
+    assert a["flops_down"] == 2.0 * rows * 4096 * 14336
+    assert a["flops"] == a["flops_up"] + a["flops_down"] + 2.0 * 8192 * 8 * 4096
+    assert a["bytes"] == 8 * 3 * 4096 * 14336 * 2 + 8192 * 4096 * 2 + 8192 * 4096 * 4 + 8 * 4096 * 2
+    # decode-sized: only the distinct active experts' weights are streamed
+    d1 = bench.algorithmic(s, 1, active_experts=2)
+    assert d1["w_bytes_up"] == 2 * 2 * 4096 * 14336 * 2 and d1["w_bytes_expert"] == 3 * 4096 * 14336 * 2
+    r = testgen.CONFIGS["tiny-moe-4e2r"]            # ReLU+bias: one up matrix, fp32
+    t = bench.algorithmic(r, r.T)
+    assert t["flops_up"] == t["flops_down"] == 2.0 * 2 * r.T * r.d_model * r.d_ff
+    assert t["w_bytes_expert"] == 2 * r.d_model * r.d_ff * 4
